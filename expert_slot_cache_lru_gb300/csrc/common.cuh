@@ -1,0 +1,162 @@
+// common.cuh -- device-side state of the slot cache, block-wide primitives and
+// the kernel launchers shared by the translation units of libmoecache.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/moe_cache.h"
+
+namespace moe {
+
+// Everything a kernel needs to reach the cache state; passed by value.
+struct DevState {
+  int L, E, S, P;          // layers, experts per layer, slots per pool, pools
+  int per_layer;           // 1: pool = layer, 0: one shared pool
+  int32_t* map;            // [L*E] key -> slot, -1 = not resident
+  uint32_t* decode_freq;   // [L*E]
+  uint32_t* demand_freq;   // [L*E]
+  uint64_t* last_demand;   // [L*E]
+  int32_t* slot_key;       // [P*S] slot -> key, -1 = empty
+  uint64_t* stamp;         // [P*S] 0 = empty
+  uint8_t* pinned;         // [P*S]
+  uint64_t* clock;         // [P]
+  moe_stats* stats;        // [L]
+  int32_t* plan_demand;    // [1 + 3*max_routes]
+  int32_t* plan_pf[2];     // [1 + 3*max(max_pred,1)] each; a prefetch for layer l uses
+                           // buffer l & 1, so the gather of one layer's prefetch can still
+                           // be reading its plan while the next layer's prefetch is admitted
+  int32_t* groups;         // [1 + max_routes + (max_routes+1) + max_routes]
+  // victim-selection scratch, [vcap] each
+  int32_t* vict;
+  uint64_t* lo_stamp;
+  int32_t* lo_slot;
+  int vcap;
+  const uint8_t* const* host_blob;  // [L*E] device-visible addresses of the host blobs
+  uint8_t* slots;          // slot storage (NULL: admission only)
+  size_t stride;           // bytes between slots
+  size_t slot_bytes;       // bytes copied per expert
+  int max_routes, max_pred;
+};
+
+__host__ __device__ inline int pool_of(const DevState& st, int layer) {
+  return st.per_layer ? layer : 0;
+}
+
+constexpr int kAdmitThreads = 1024;  // admission / prefetch: one CTA of 32 warps
+
+// ---------------------------------------------------------------- block helpers
+// All helpers assume blockDim.x == kAdmitThreads and are called by every thread.
+
+struct BlockScratch {
+  int warp_i[32];
+  unsigned long long warp_u[32];
+  unsigned long long warp_v[32];
+};
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Exclusive prefix sum over the block in thread order; *total receives the sum.
+__device__ __forceinline__ int block_excl_scan(int v, BlockScratch& bs, int* total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int incl = warp_incl_scan(v);
+  if (lane == 31) bs.warp_i[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int t = bs.warp_i[lane];
+    t = warp_incl_scan(t);
+    bs.warp_i[lane] = t;
+  }
+  __syncthreads();
+  const int excl = incl - v + (w > 0 ? bs.warp_i[w - 1] : 0);
+  *total = bs.warp_i[31];
+  __syncthreads();
+  return excl;
+}
+
+__device__ __forceinline__ int block_sum(int v, BlockScratch& bs) {
+  int total;
+  (void)block_excl_scan(v, bs, &total);
+  return total;
+}
+
+// Block-wide min and max of 64-bit values.
+__device__ __forceinline__ void block_minmax_u64(unsigned long long mn, unsigned long long mx,
+                                                 BlockScratch& bs, unsigned long long* omin,
+                                                 unsigned long long* omax) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+    unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+    mn = a < mn ? a : mn;
+    mx = b > mx ? b : mx;
+  }
+  if (lane == 0) {
+    bs.warp_u[w] = mn;
+    bs.warp_v[w] = mx;
+  }
+  __syncthreads();
+  if (w == 0) {
+    mn = bs.warp_u[lane];
+    mx = bs.warp_v[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
+      unsigned long long b = __shfl_xor_sync(0xffffffffu, mx, o);
+      mn = a < mn ? a : mn;
+      mx = b > mx ? b : mx;
+    }
+    if (lane == 0) {
+      bs.warp_u[0] = mn;
+      bs.warp_v[0] = mx;
+    }
+  }
+  __syncthreads();
+  *omin = bs.warp_u[0];
+  *omax = bs.warp_v[0];
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- launchers
+// Each returns the cudaError_t of the launch.
+
+size_t admit_smem_bytes(int E);
+cudaError_t launch_admit(const DevState& st, int layer, const int32_t* ids, int32_t* out, int R,
+                         int cap, cudaStream_t s);
+cudaError_t launch_prefetch(const DevState& st, int layer, const int32_t* pred, int n,
+                            int32_t* plan, cudaStream_t s);
+cudaError_t launch_gather(const DevState& st, const int32_t* plan, int grid, cudaStream_t s);
+cudaError_t launch_rollback(const DevState& st, const int32_t* plan, cudaStream_t s);
+cudaError_t launch_pin(const DevState& st, int layer, int slot, int pinned, cudaStream_t s);
+
+// Expert math (gemv.cu).
+struct FfnScratch {
+  float* h;         // [max_routes * I] routed intermediate
+  float* hs;        // [max_rows * Is] shared intermediate
+  float* gate;      // [max_rows] sigmoid gate of the shared expert
+  float* ys;        // [max_rows * H] shared expert output (gated)
+};
+
+cudaError_t launch_shared_expert(int wfmt, int H, int Is, const void* x, int n_rows,
+                                 const uint8_t* blob, const void* gate_w, FfnScratch sc,
+                                 cudaStream_t s);
+cudaError_t launch_routed_up(const DevState& st, int wfmt, int H, int I, int layer,
+                             const void* x, const int32_t* slot_ids, int n_rows, int k,
+                             FfnScratch sc, cudaStream_t s);
+cudaError_t launch_routed_down_combine(const DevState& st, int wfmt, int H, int I, int layer,
+                                       const int32_t* slot_ids, const float* w, int n_rows,
+                                       int k, const float* shared_y, void* out, FfnScratch sc,
+                                       cudaStream_t s);
+
+}  // namespace moe

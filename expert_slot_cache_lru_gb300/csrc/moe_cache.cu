@@ -1,0 +1,471 @@
+// moe_cache.cu -- host side of the C ABI: descriptor checks, state and
+// scratch allocation, and the ordering of kernels, streams and events.
+//
+// The per-layer order and the fork/join follow FreeToken issue #753 ("[Perf]
+// Offloaded decode: overlap the expert-miss gather with the same layer's
+// shared expert, event-ordered inside the CUDA graph", What we changed):
+//   compute: admit -> record(ready) -> shared expert + gate -> wait(done) -> routed
+//   side:    wait(ready) -> gather -> record(done)
+// Both events are created with the cache, before any capture; the join is
+// made on every exit path once the side stream has been forked, so no side
+// work outlives the layer and a capture never ends with an unjoined fork.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+namespace moe {
+cudaError_t admit_set_smem_limits(int E);
+cudaError_t gemv_set_smem_limits(int H, int I, int Is, int k_max);
+}  // namespace moe
+
+using moe::DevState;
+using moe::FfnScratch;
+
+struct moe_cache {
+  moe_cache_desc d{};
+  int P = 0;
+  int device = 0;
+  DevState st{};
+  FfnScratch sc{};
+  void* mem = nullptr;       // one allocation for all state and scratch
+  size_t mem_bytes = 0;
+  cudaEvent_t ev_ready = nullptr, ev_done = nullptr;
+  int fail_gathers = 0;
+  int gather_grid = 38;
+  int down_k_max = 0;        // largest k the down kernel's shared memory was sized for
+  int last_pf_layer = 0;     // target layer of the last prefetch enqueued (selects its plan)
+};
+
+namespace {
+
+thread_local char g_cuda_err[256] = "";
+
+int cuda_fail(cudaError_t e, const char* what) {
+  std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  return MOE_ERR_CUDA;
+}
+
+#define CK(call)                                     \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call); \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+size_t blob_bytes(int fmt, int H, int I) {
+  const size_t ih = (size_t)H * I;
+  if (fmt == MOE_W_BF16) return 6 * ih;
+  if (fmt == MOE_W_NVFP4) return 3 * ih / 2 + 3 * ih / 16 + 16;
+  return 0;
+}
+
+// Sub-allocator over one device allocation (256-byte aligned pieces).
+struct Carve {
+  size_t off = 0;
+  template <typename T>
+  size_t take(size_t n) {
+    size_t o = align_up(off, 256);
+    off = o + n * sizeof(T);
+    return o;
+  }
+};
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int check_layer(const moe_cache* c, int layer) {
+  return (c && layer >= 0 && layer < c->d.n_layers) ? MOE_OK : MOE_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_CACHE_ABI_VERSION; }
+
+const char* moe_strerror(int err) {
+  switch (err) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CONFIG: return "invalid cache descriptor";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_CAPACITY: return "request exceeds the cache's sizes";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case MOE_ERR_STATE: return "call not valid in the cache's state";
+    case MOE_ERR_INJECTED: return "injected failure";
+    default: return "unknown error";
+  }
+}
+
+const char* moe_last_cuda_error(void) { return g_cuda_err; }
+
+int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
+  if (!desc || !out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const moe_cache_desc& d = *desc;
+  if (d.n_layers <= 0 || d.n_experts <= 0 || d.n_experts > 16384 || d.n_slots < 0 ||
+      d.n_slots >= (1 << 20) || (d.pool_mode != MOE_POOL_SHARED && d.pool_mode != MOE_POOL_PER_LAYER) ||
+      d.max_routes < 1 || d.max_routes > 16384 || d.max_rows < 1 || d.max_rows > d.max_routes ||
+      d.max_pred < 0 || d.max_pred > 4096 || d.gather_ctas < 0 || d.gather_ctas > 4096)
+    return MOE_ERR_CONFIG;
+  if ((long long)d.n_layers * d.n_experts > 0x7fffffffLL) return MOE_ERR_CONFIG;
+  if (d.max_pred > 0 && d.n_slots == 0) return MOE_ERR_CONFIG;  // prefetch needs a cache
+  const bool compute = d.hidden > 0 || d.inter > 0;
+  if (compute) {
+    if (d.hidden <= 0 || d.inter <= 0 || d.hidden % 32 || d.inter % 32 || d.shared_inter < 0 ||
+        d.shared_inter % 32 || (d.wfmt != MOE_W_BF16 && d.wfmt != MOE_W_NVFP4))
+      return MOE_ERR_CONFIG;
+    if (d.slot_bytes != blob_bytes(d.wfmt, d.hidden, d.inter)) return MOE_ERR_CONFIG;
+    if ((size_t)d.hidden * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
+  }
+  if (d.slot_bytes > 0) {
+    if (!d.slot_storage || !d.host_experts || d.slot_bytes % 16 ||
+        (reinterpret_cast<uintptr_t>(d.slot_storage) & 255) || d.n_slots == 0)
+      return MOE_ERR_CONFIG;
+    if (d.slot_stride && (d.slot_stride < d.slot_bytes || d.slot_stride % 256)) return MOE_ERR_CONFIG;
+  }
+
+  moe_cache* c = new (std::nothrow) moe_cache;
+  if (!c) return MOE_ERR_CUDA;
+  c->d = d;
+  if (d.slot_bytes > 0 && !d.slot_stride) c->d.slot_stride = align_up(d.slot_bytes, 256);
+  c->P = d.pool_mode == MOE_POOL_PER_LAYER ? d.n_layers : 1;
+  c->gather_grid = d.gather_ctas ? d.gather_ctas : 38;
+  auto fail = [&](int r) {
+    moe_cache_destroy(c);
+    return r;
+  };
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e != cudaSuccess) return fail(cuda_fail(e, "cudaGetDevice"));
+
+  const size_t K = (size_t)d.n_layers * d.n_experts;
+  const size_t PS = (size_t)c->P * d.n_slots;
+  const int vcap = std::max(std::max(d.max_routes, d.max_pred), 1);
+  const int I = d.inter, H = d.hidden, Is = d.shared_inter;
+  Carve cv;
+  const size_t o_map = cv.take<int32_t>(K), o_dfq = cv.take<uint32_t>(K),
+               o_dmq = cv.take<uint32_t>(K), o_ld = cv.take<uint64_t>(K),
+               o_sk = cv.take<int32_t>(PS), o_stamp = cv.take<uint64_t>(PS),
+               o_pin = cv.take<uint8_t>(PS), o_clk = cv.take<uint64_t>(c->P),
+               o_stats = cv.take<moe_stats>(d.n_layers),
+               o_pd = cv.take<int32_t>(1 + 3 * (size_t)d.max_routes),
+               o_pp = cv.take<int32_t>(1 + 3 * (size_t)std::max(d.max_pred, 1)),
+               o_pp2 = cv.take<int32_t>(1 + 3 * (size_t)std::max(d.max_pred, 1)),
+               o_grp = cv.take<int32_t>(2 + 3 * (size_t)d.max_routes),
+               o_vict = cv.take<int32_t>(vcap), o_los = cv.take<uint64_t>(vcap),
+               o_lol = cv.take<int32_t>(vcap), o_hb = cv.take<const uint8_t*>(K),
+               o_h = cv.take<float>((size_t)d.max_routes * std::max(I, 1)),
+               o_hs = cv.take<float>((size_t)d.max_rows * std::max(Is, 1)),
+               o_gate = cv.take<float>(d.max_rows),
+               o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1));
+  c->mem_bytes = align_up(cv.off, 256);
+  e = cudaMalloc(&c->mem, c->mem_bytes);
+  if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMalloc(state)"));
+  uint8_t* m = static_cast<uint8_t*>(c->mem);
+  DevState& st = c->st;
+  st.L = d.n_layers;
+  st.E = d.n_experts;
+  st.S = d.n_slots;
+  st.P = c->P;
+  st.per_layer = d.pool_mode == MOE_POOL_PER_LAYER;
+  st.map = reinterpret_cast<int32_t*>(m + o_map);
+  st.decode_freq = reinterpret_cast<uint32_t*>(m + o_dfq);
+  st.demand_freq = reinterpret_cast<uint32_t*>(m + o_dmq);
+  st.last_demand = reinterpret_cast<uint64_t*>(m + o_ld);
+  st.slot_key = reinterpret_cast<int32_t*>(m + o_sk);
+  st.stamp = reinterpret_cast<uint64_t*>(m + o_stamp);
+  st.pinned = m + o_pin;
+  st.clock = reinterpret_cast<uint64_t*>(m + o_clk);
+  st.stats = reinterpret_cast<moe_stats*>(m + o_stats);
+  st.plan_demand = reinterpret_cast<int32_t*>(m + o_pd);
+  st.plan_pf[0] = reinterpret_cast<int32_t*>(m + o_pp);
+  st.plan_pf[1] = reinterpret_cast<int32_t*>(m + o_pp2);
+  st.groups = reinterpret_cast<int32_t*>(m + o_grp);
+  st.vict = reinterpret_cast<int32_t*>(m + o_vict);
+  st.lo_stamp = reinterpret_cast<uint64_t*>(m + o_los);
+  st.lo_slot = reinterpret_cast<int32_t*>(m + o_lol);
+  st.vcap = vcap;
+  st.host_blob = reinterpret_cast<const uint8_t* const*>(m + o_hb);
+  st.slots = static_cast<uint8_t*>(d.slot_storage);
+  st.stride = c->d.slot_stride;
+  st.slot_bytes = d.slot_bytes;
+  st.max_routes = d.max_routes;
+  st.max_pred = d.max_pred;
+  c->sc.h = reinterpret_cast<float*>(m + o_h);
+  c->sc.hs = reinterpret_cast<float*>(m + o_hs);
+  c->sc.gate = reinterpret_cast<float*>(m + o_gate);
+  c->sc.ys = reinterpret_cast<float*>(m + o_ys);
+
+  // initial state: nothing resident, every clock at 1
+  e = cudaMemset(c->mem, 0, c->mem_bytes);
+  if (e == cudaSuccess) e = cudaMemset(st.map, 0xff, K * sizeof(int32_t));
+  if (e == cudaSuccess && PS) e = cudaMemset(st.slot_key, 0xff, PS * sizeof(int32_t));
+  if (e == cudaSuccess) {
+    std::vector<uint64_t> ones(c->P, 1ull);
+    e = cudaMemcpy(st.clock, ones.data(), c->P * sizeof(uint64_t), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) return fail(cuda_fail(e, "state init"));
+
+  if (d.slot_bytes > 0) {
+    std::vector<const uint8_t*> dev(K);
+    for (size_t k = 0; k < K; ++k) {
+      const void* hp = d.host_experts[k];
+      if (!hp || (reinterpret_cast<uintptr_t>(hp) & 15)) return fail(MOE_ERR_CONFIG);
+      void* dp = nullptr;
+      e = cudaHostGetDevicePointer(&dp, const_cast<void*>(hp), 0);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        std::snprintf(g_cuda_err, sizeof g_cuda_err,
+                      "host expert %zu is not pinned, mapped memory: %s", k, cudaGetErrorString(e));
+        return fail(MOE_ERR_CONFIG);
+      }
+      dev[k] = static_cast<const uint8_t*>(dp);
+    }
+    e = cudaMemcpy(const_cast<const uint8_t**>(st.host_blob), dev.data(), K * sizeof(void*),
+                   cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "host blob table"));
+  }
+
+  e = moe::admit_set_smem_limits(d.n_experts);
+  if (e != cudaSuccess) return fail(cuda_fail(e, "admission shared memory"));
+  if (compute) {
+    // the down kernel stages k routes' intermediates in shared memory
+    c->down_k_max = (int)std::min<size_t>(d.max_routes, (200 * 1024) / ((size_t)I * 4));
+    e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
+  }
+  e = cudaEventCreateWithFlags(&c->ev_ready, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(cuda_fail(e, "cudaEventCreate"));
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(cuda_fail(e, "create sync"));
+  *out = c;
+  return MOE_OK;
+}
+
+int moe_cache_destroy(moe_cache* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  int rc = MOE_OK;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) rc = cuda_fail(e, "destroy sync");
+  if (c->ev_ready) cudaEventDestroy(c->ev_ready);
+  if (c->ev_done) cudaEventDestroy(c->ev_done);
+  if (c->mem) cudaFree(c->mem);
+  delete c;
+  return rc;
+}
+
+int moe_cache_prefill(moe_cache* c, int layer, const int32_t* h_ids, int n, void* stream) {
+  if (check_layer(c, layer) != MOE_OK || n < 0 || (n > 0 && !h_ids)) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  const moe_cache_desc& d = c->d;
+  const int E = d.n_experts, S = d.n_slots;
+  const int p = c->P > 1 ? layer : 0;
+  CK(cudaDeviceSynchronize());
+  std::vector<int32_t> map(E), sk(S);
+  uint64_t clk = 0;
+  CK(cudaMemcpy(map.data(), c->st.map + (size_t)layer * E, E * 4, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(sk.data(), c->st.slot_key + (size_t)p * S, (size_t)S * 4, cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(&clk, c->st.clock + p, 8, cudaMemcpyDeviceToHost));
+  std::vector<int> slot_of(n);
+  int next = 0;
+  for (int i = 0; i < n; ++i) {
+    const int e = h_ids[i];
+    if (e < 0 || e >= E || map[e] >= 0) return MOE_ERR_INVALID_ARG;
+    while (next < S && sk[next] >= 0) ++next;
+    if (next >= S) return MOE_ERR_CAPACITY;
+    map[e] = next;
+    sk[next] = layer * E + e;
+    slot_of[i] = next;
+  }
+  // commit: map entries, slot keys, stamps = clock; then the bytes
+  CK(cudaMemcpy(c->st.map + (size_t)layer * E, map.data(), E * 4, cudaMemcpyHostToDevice));
+  CK(cudaMemcpy(c->st.slot_key + (size_t)p * S, sk.data(), (size_t)S * 4, cudaMemcpyHostToDevice));
+  for (int i = 0; i < n; ++i)
+    CK(cudaMemcpy(c->st.stamp + (size_t)p * S + slot_of[i], &clk, 8, cudaMemcpyHostToDevice));
+  if (d.slot_bytes > 0) {
+    for (int i = 0; i < n; ++i) {
+      uint8_t* dst = c->st.slots + ((size_t)p * S + slot_of[i]) * c->st.stride;
+      CK(cudaMemcpyAsync(dst, d.host_experts[(size_t)layer * E + h_ids[i]], d.slot_bytes,
+                         cudaMemcpyHostToDevice, as_stream(stream)));
+    }
+    CK(cudaStreamSynchronize(as_stream(stream)));
+  }
+  return MOE_OK;
+}
+
+int moe_cache_pin(moe_cache* c, int layer, int slot, int pinned, void* stream) {
+  if (check_layer(c, layer) != MOE_OK || slot < 0 || slot >= c->d.n_slots) return MOE_ERR_INVALID_ARG;
+  CK(moe::launch_pin(c->st, layer, slot, pinned ? 1 : 0, as_stream(stream)));
+  return MOE_OK;
+}
+
+int moe_admit(moe_cache* c, int layer, const int32_t* d_ids, int32_t* d_slot_ids, int n_routes,
+              int fetch_cap, void* stream) {
+  if (check_layer(c, layer) != MOE_OK || n_routes < 0) return MOE_ERR_INVALID_ARG;
+  if (n_routes > c->d.max_routes) return MOE_ERR_CAPACITY;
+  if (n_routes > 0 && (!d_ids || !d_slot_ids)) return MOE_ERR_INVALID_ARG;
+  CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, n_routes, fetch_cap, as_stream(stream)));
+  return MOE_OK;
+}
+
+int moe_prefetch(moe_cache* c, int layer, const int32_t* d_pred, int n, void* stream) {
+  if (check_layer(c, layer) != MOE_OK || n < 0 || (n > 0 && !d_pred)) return MOE_ERR_INVALID_ARG;
+  if (c->d.max_pred == 0) return MOE_ERR_STATE;
+  if (n > c->d.max_pred) return MOE_ERR_CAPACITY;
+  CK(moe::launch_prefetch(c->st, layer, d_pred, n, c->st.plan_pf[layer & 1], as_stream(stream)));
+  c->last_pf_layer = layer;
+  return MOE_OK;
+}
+
+int moe_gather_missing(moe_cache* c, int which, void* stream) {
+  if (!c || (which != MOE_PLAN_DEMAND && which != MOE_PLAN_PREFETCH)) return MOE_ERR_INVALID_ARG;
+  if (c->d.slot_bytes == 0) return MOE_ERR_STATE;
+  if (which == MOE_PLAN_PREFETCH && c->d.max_pred == 0) return MOE_ERR_STATE;
+  if (c->fail_gathers > 0) {
+    --c->fail_gathers;
+    return MOE_ERR_INJECTED;
+  }
+  const int32_t* plan =
+      which == MOE_PLAN_DEMAND ? c->st.plan_demand : c->st.plan_pf[c->last_pf_layer & 1];
+  CK(moe::launch_gather(c->st, plan, c->gather_grid, as_stream(stream)));
+  return MOE_OK;
+}
+
+int moe_rollback_plan(moe_cache* c, int which, void* stream) {
+  if (!c || (which != MOE_PLAN_DEMAND && which != MOE_PLAN_PREFETCH)) return MOE_ERR_INVALID_ARG;
+  const int32_t* plan =
+      which == MOE_PLAN_DEMAND ? c->st.plan_demand : c->st.plan_pf[c->last_pf_layer & 1];
+  CK(moe::launch_rollback(c->st, plan, as_stream(stream)));
+  return MOE_OK;
+}
+
+static int check_compute(moe_cache* c, int layer, int n_rows, int k, const void* shared_blob,
+                         const void* shared_gate) {
+  if (check_layer(c, layer) != MOE_OK || n_rows < 0 || k < 0) return MOE_ERR_INVALID_ARG;
+  if (c->d.hidden == 0 || c->d.slot_bytes == 0) return MOE_ERR_STATE;
+  if (n_rows > c->d.max_rows || (size_t)n_rows * k > (size_t)c->d.max_routes) return MOE_ERR_CAPACITY;
+  if (k > c->down_k_max) return MOE_ERR_UNSUPPORTED;
+  if (shared_blob && (c->d.shared_inter == 0 || !shared_gate)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+static int run_shared(moe_cache* c, const void* d_x, int n_rows, const void* blob, const void* gate,
+                      cudaStream_t s) {
+  if (n_rows == 0) return MOE_OK;
+  CK(moe::launch_shared_expert(c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows,
+                               static_cast<const uint8_t*>(blob), gate, c->sc, s));
+  return MOE_OK;
+}
+
+static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* slot_ids,
+                      const float* w, int n_rows, int k, bool with_shared, void* d_out,
+                      cudaStream_t s) {
+  const moe_cache_desc& d = c->d;
+  if (n_rows == 0) return MOE_OK;
+  if (k > 0)
+    CK(moe::launch_routed_up(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, n_rows, k,
+                           c->sc, s));
+  CK(moe::launch_routed_down_combine(c->st, d.wfmt, d.hidden, d.inter, layer, slot_ids, w,
+                                     n_rows, k, with_shared ? c->sc.ys : nullptr, d_out, c->sc, s));
+  return MOE_OK;
+}
+
+int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const int32_t* d_slot_ids,
+                       const float* d_w, int n_rows, int k, const void* d_shared_blob,
+                       const void* d_shared_gate, void* d_out, void* stream) {
+  int rc = check_compute(c, layer, n_rows, k, d_shared_blob, d_shared_gate);
+  if (rc != MOE_OK) return rc;
+  if (n_rows == 0) return MOE_OK;
+  if (!d_x || !d_out || (k > 0 && (!d_slot_ids || !d_w)) || d_out == d_x) return MOE_ERR_INVALID_ARG;
+  if (d_shared_blob && (rc = run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, as_stream(stream))))
+    return rc;
+  return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out,
+                    as_stream(stream));
+}
+
+int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,
+                     const float* d_w, int32_t* d_slot_ids, int n_rows, int k, int fetch_cap,
+                     const int32_t* d_pred, int n_pred, const void* d_shared_blob,
+                     const void* d_shared_gate, void* d_out, void* compute_stream,
+                     void* side_stream, unsigned flags) {
+  int rc = check_compute(c, layer, n_rows, k, d_shared_blob, d_shared_gate);
+  if (rc != MOE_OK) return rc;
+  const int R = n_rows * k;
+  if (R > 0 && (!d_ids || !d_slot_ids || !d_w)) return MOE_ERR_INVALID_ARG;
+  if (!d_x || !d_out || d_out == d_x) return MOE_ERR_INVALID_ARG;
+  const bool pf = d_pred && n_pred > 0;
+  if (pf && (layer + 1 >= c->d.n_layers || c->d.max_pred == 0)) return MOE_ERR_INVALID_ARG;
+  if (pf && n_pred > c->d.max_pred) return MOE_ERR_CAPACITY;
+  const bool overlap = (flags & MOE_OVERLAP) != 0;
+  if (overlap && !side_stream) return MOE_ERR_INVALID_ARG;
+  cudaStream_t cs = as_stream(compute_stream), ss = as_stream(side_stream);
+
+  CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
+  int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
+  if (pf) {
+    CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, cs));
+    c->last_pf_layer = layer + 1;
+  }
+  if (!overlap) {
+    CK(moe::launch_gather(c->st, c->st.plan_demand, c->gather_grid, cs));
+    if (d_shared_blob && (rc = run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, cs))) return rc;
+    if ((rc = run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out, cs)))
+      return rc;
+    if (pf) CK(moe::launch_gather(c->st, pf_plan, c->gather_grid, cs));
+    return MOE_OK;
+  }
+  // fork
+  CK(cudaEventRecord(c->ev_ready, cs));
+  CK(cudaStreamWaitEvent(ss, c->ev_ready, 0));
+  cudaError_t side_err = moe::launch_gather(c->st, c->st.plan_demand, c->gather_grid, ss);
+  cudaError_t rec = cudaEventRecord(c->ev_done, ss);
+  if (side_err == cudaSuccess && pf) side_err = moe::launch_gather(c->st, pf_plan, c->gather_grid, ss);
+  int shared_rc = MOE_OK;
+  if (side_err == cudaSuccess && rec == cudaSuccess && d_shared_blob)
+    shared_rc = run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, cs);
+  // join, on every path once forked
+  cudaError_t join = rec == cudaSuccess ? cudaStreamWaitEvent(cs, c->ev_done, 0) : rec;
+  if (side_err != cudaSuccess) return cuda_fail(side_err, "gather (side stream)");
+  if (join != cudaSuccess) return cuda_fail(join, "join");
+  if (shared_rc != MOE_OK) return shared_rc;
+  return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out, cs);
+}
+
+int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out) {
+  if (check_layer(c, layer) != MOE_OK || !h_out) return MOE_ERR_INVALID_ARG;
+  CK(cudaDeviceSynchronize());
+  CK(cudaMemcpy(h_out, c->st.stats + layer, sizeof(moe_stats), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+int moe_device_views(moe_cache* c, moe_views* v) {
+  if (!c || !v) return MOE_ERR_INVALID_ARG;
+  const DevState& st = c->st;
+  v->map = st.map;
+  v->slot_key = st.slot_key;
+  v->stamp = st.stamp;
+  v->pinned = st.pinned;
+  v->clock = st.clock;
+  v->decode_freq = st.decode_freq;
+  v->demand_freq = st.demand_freq;
+  v->last_demand = st.last_demand;
+  v->stats = st.stats;
+  v->plan_demand = st.plan_demand;
+  v->plan_prefetch = st.plan_pf[c->last_pf_layer & 1];
+  v->groups = st.groups;
+  v->n_pools = c->P;
+  return MOE_OK;
+}
+
+int moe_cache_fail_next_gather(moe_cache* c, int n) {
+  if (!c || n < 0) return MOE_ERR_INVALID_ARG;
+  c->fail_gathers = n;
+  return MOE_OK;
+}
+
+}  // extern "C"

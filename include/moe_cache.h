@@ -1,0 +1,301 @@
+/*
+ * moe_cache.h -- C ABI of the GB300 offloaded-MoE expert slot cache.
+ *
+ * One MoE decode layer whose expert weights live in pinned host memory: the
+ * GPU keeps the hot experts in a fixed pool of device "slots".  The library
+ * runs, all on one GPU (sm_103a) and without a host synchronisation:
+ *   1. admission (moe_admit): dedup the step's top-k ids, look them up in the
+ *      expert->slot map, refresh recency on hits, pick least-recently-used
+ *      victims for misses, write a device-side miss plan, rewrite ids to slot
+ *      ids (-1 for routes that get no slot);
+ *   2. the miss gather (moe_gather_missing): copy the planned experts' bytes
+ *      from pinned host memory into their slots;
+ *   3. the routed expert FFNs over the slots, the sigmoid-gated shared expert
+ *      and the weighted combine (moe_routed_experts, moe_decode_layer).
+ * Look-ahead prefetch with an LFRU eviction guard (moe_prefetch) fills slots
+ * for the next layer.
+ *
+ * Sources (page title, section):
+ *  [P1] FreeToken PR #491 "refactor(moe): extract hybrid decode orchestration"
+ *  [P2] FreeToken issue #753 "[Perf] Offloaded decode: overlap the expert-miss
+ *       gather with the same layer's shared expert, event-ordered inside the
+ *       CUDA graph"
+ *  [P3] FreeToken PR #680 "fix(moe): admit a wide offloaded decode step's
+ *       experts 128 at a time"
+ *  [P4] llama.cpp fork PR #126 "cuda : MoE look-ahead expert prefetch (PR-A
+ *       consumer) + LFRU eviction guard"
+ *
+ * ---------------------------------------------------------------- conventions
+ * Pointers named d_* are device pointers (or device-accessible), h_* host
+ * pointers.  Streams are cudaStream_t passed as void* (NULL = legacy default
+ * stream).  Expert ids, slot ids and route indices are int32; routing weights
+ * float32; hidden states and outputs bfloat16 (uint16 bit patterns).
+ *
+ * Ownership: the caller owns every tensor it passes (inputs, outputs, the slot
+ * storage, the pinned host blobs, the streams); pinned host blobs and slot
+ * storage must outlive the cache.  The cache owns its state (maps, stamps,
+ * frequencies, plans, statistics, scratch) and two CUDA events, all created in
+ * moe_cache_create, i.e. before any stream capture.
+ *
+ * Errors: every call returns MOE_OK (0) or a negative MOE_ERR_* code and never
+ * aborts or throws.  Argument errors are detected on the host before any work
+ * is enqueued.  Data-dependent anomalies never stop the stream: an id outside
+ * [0, n_experts) becomes route -1 and sets MOE_STATUS_INVALID_ID in the
+ * layer's statistics; a pool with too few evictable slots admits what it can
+ * (lowest expert ids first), the rest overflow (-1) and MOE_STATUS_CAPACITY is
+ * set.  Only moe_read_stats, moe_cache_prefill and moe_cache_destroy
+ * synchronise with the device; every other call only enqueues work and may be
+ * captured into a CUDA graph (fixed n_routes / n_rows / n_pred per capture).
+ *
+ * Single writer [P2 What we changed]: moe_admit, moe_prefetch and the layer's
+ * routed compute must be ordered on one (compute) stream; the gather only
+ * reads the plan and writes slot bytes.
+ *
+ * ---------------------------------------------------------------- layouts
+ * Keys: key = layer * n_experts + expert.  Pools: MOE_POOL_SHARED has one pool
+ * of n_slots used by every layer; MOE_POOL_PER_LAYER has n_layers pools of
+ * n_slots each.  A slot id is the index within its pool.  Slot s of pool p
+ * lives at slot_storage + (p * n_slots + s) * slot_stride.
+ *
+ * Expert blob (the copy unit, one contiguous block per expert, identical in
+ * host memory and in a slot) [P2 What we changed "fused copy layout",
+ * Correctness "six-bank NVFP4 row sizes"]:
+ *   MOE_W_BF16:  gate [I][H], up [I][H], down [H][I], bf16 row-major;
+ *                6*H*I bytes.
+ *   MOE_W_NVFP4: six banks then the global scales:
+ *                gate codes [I][H/2], up codes [I][H/2], down codes [H][I/2]
+ *                  (FP4 E2M1, two per byte, even element in the low nibble),
+ *                gate scales [I][H/16], up scales [I][H/16], down scales
+ *                  [H][I/16] (FP8 E4M3, one per 16 consecutive row elements),
+ *                float32 global scale of gate, up, down, 4 bytes of padding;
+ *                3*H*I/2 + 3*H*I/16 + 16 bytes.
+ *                element (n,k) = e2m1(code) * e4m3(scale[n][k/16]) * global.
+ *   H, I and shared_inter must be multiples of 32 (checked at create).
+ * Shared expert: a blob of the same format with I = shared_inter, plus a gate
+ *   vector w_g bf16 [H]: shared(x) = sigmoid(x . w_g) * FFN_shared(x).
+ * Expert FFN: g = W_g x, u = W_u x, h = silu(g) * u, y = W_d h.
+ * Layer output: out[b] = bf16( sum_j w[b,j] * y(slot[b,j], x[b])  +  shared(x[b]) )
+ *   routes with slot -1 contribute nothing; the sum runs over j ascending, then
+ *   adds the shared term; fp32 accumulation throughout.
+ *
+ * Miss plan (device, int32): [count, (slot, layer, expert) * count], entries
+ *   in ascending expert id; a plan holds at most max_routes (demand) or
+ *   max_pred (prefetch) entries.  There is one demand plan and two prefetch
+ *   plans: a prefetch for layer l writes plan l & 1, so the side-stream gather
+ *   of layer l's prefetch may still read its plan while layer l+1's prefetch
+ *   (for l+2) is admitted; moe_gather_missing / moe_rollback_plan with
+ *   MOE_PLAN_PREFETCH use the plan of the most recent prefetch call.
+ * Route groups (device, int32, written by moe_routed_experts when n_rows > 1):
+ *   [G, slot[max_routes], start[max_routes + 1], route[max_routes]]: group g
+ *   is the g-th distinct resident expert in ascending id, its slot, and its
+ *   routes route[start[g] .. start[g+1]) in ascending route index.
+ */
+#ifndef MOE_CACHE_H
+#define MOE_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_CACHE_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+enum moe_err {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,   /* a NULL, a size out of range, a bad enum */
+  MOE_ERR_CONFIG = -2,        /* inconsistent moe_cache_desc */
+  MOE_ERR_CUDA = -3,          /* a CUDA runtime call failed (see moe_last_cuda_error) */
+  MOE_ERR_CAPACITY = -4,      /* more routes / rows / predictions than the cache was sized for */
+  MOE_ERR_UNSUPPORTED = -5,   /* shape or format this build does not handle */
+  MOE_ERR_STATE = -6,         /* call not valid in the cache's current state */
+  MOE_ERR_INJECTED = -7       /* a test-requested failure (moe_cache_fail_next_gather) */
+};
+
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+typedef enum { MOE_POOL_SHARED = 0, MOE_POOL_PER_LAYER = 1 } moe_pool_mode;
+typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
+
+/* moe_decode_layer flags */
+#define MOE_OVERLAP 1u        /* gather on the side stream, joined by events [P2] */
+
+/* status_bits of moe_stats */
+#define MOE_STATUS_INVALID_ID 1ull
+#define MOE_STATUS_CAPACITY 2ull
+
+typedef struct moe_cache moe_cache; /* opaque */
+
+typedef struct {
+  int n_layers;                    /* > 0 */
+  int n_experts;                   /* per layer, 1 .. 16384 */
+  int n_slots;                     /* per pool, 0 .. 1,048,575 */
+  int pool_mode;                   /* moe_pool_mode */
+  int hidden, inter;               /* H, I of a routed expert (0, 0 = admission only) */
+  int wfmt;                        /* moe_wfmt */
+  int shared_inter;                /* I of the shared expert, 0 = none */
+  size_t slot_bytes;               /* bytes copied per expert: the blob size, 0 = no storage */
+  size_t slot_stride;              /* >= slot_bytes, multiple of 256; 0 = round up slot_bytes */
+  void* slot_storage;              /* device, caller-owned, n_pools*n_slots*slot_stride bytes */
+  const void* const* host_experts; /* host array [n_layers*n_experts] of pinned host blob
+                                      pointers (16-byte aligned; may alias); read at create */
+  int max_routes;                  /* routes per admission, 1 .. 16384 */
+  int max_rows;                    /* rows per layer call, 1 .. max_routes */
+  int max_pred;                    /* predictions per prefetch, 0 .. 4096 (0 = no prefetch) */
+  int gather_ctas;                 /* CTAs of the gather kernel, 0 = default (38) */
+} moe_cache_desc;
+
+/* Per-layer counters, device-resident, read with moe_read_stats.
+ * [P3 Solution]: a step counts once -- calls += 1, lookups += distinct valid
+ * ids ("met"), misses += distinct ids not resident -- while decode_freq
+ * counts every valid route.  fetched = misses admitted (copied);
+ * overflow_routes = valid routes left at -1.  pf_*: prefetch counters [P4
+ * Consumer, Eviction guard, Open item 3]: pf_requests = distinct valid
+ * predictions = pf_resident + pf_filled + pf_dropped_guard + pf_no_victim. */
+typedef struct {
+  uint64_t calls, lookups, hits, misses, fetched, overflow_routes, evictions, invalid_routes;
+  uint64_t pf_requests, pf_invalid, pf_resident, pf_filled, pf_dropped_guard, pf_no_victim,
+           pf_evictions, status_bits;
+} moe_stats;
+
+/* Device pointers into the cache's state, for inspection and tests.  Sizes:
+ * map, decode_freq, demand_freq, last_demand: n_layers*n_experts;
+ * slot_key, stamp, pinned: n_pools*n_slots; clock: n_pools; stats: n_layers;
+ * plans and groups as described above. */
+typedef struct {
+  const int32_t* map;            /* key -> slot in its pool, -1 = not resident */
+  const int32_t* slot_key;       /* slot -> key, -1 = empty */
+  const uint64_t* stamp;         /* slot -> clock of last touch, 0 = empty */
+  const uint8_t* pinned;
+  const uint64_t* clock;         /* per pool, starts at 1, +1 per admission */
+  const uint32_t* decode_freq;   /* valid routes per key */
+  const uint32_t* demand_freq;   /* admissions that demanded the key */
+  const uint64_t* last_demand;   /* clock of the last demand, 0 = never */
+  const moe_stats* stats;
+  const int32_t* plan_demand;
+  const int32_t* plan_prefetch;
+  const int32_t* groups;
+  int n_pools;
+} moe_views;
+
+/* Create a cache; every slot starts empty, every clock at 1.  Validates the
+ * descriptor (MOE_ERR_CONFIG), translates each host blob pointer to a device
+ * address (cudaHostGetDevicePointer; MOE_ERR_CONFIG if a pointer is not
+ * pinned, mapped memory), allocates state and scratch (MOE_ERR_CUDA on
+ * failure) and creates the events.  Uses the current CUDA device. */
+MOE_API int moe_cache_create(const moe_cache_desc* desc, moe_cache** out);
+
+/* Free all cache-owned memory and events after synchronising the device. */
+MOE_API int moe_cache_destroy(moe_cache* c);
+
+/* Set-up, synchronous: install n distinct, valid, non-resident experts of
+ * `layer` into the lowest empty slots of its pool, stamped with the pool's
+ * current clock, and copy their blobs into the slots.  No statistics change.
+ * MOE_ERR_INVALID_ARG for a bad / duplicate / resident id, MOE_ERR_CAPACITY
+ * when the pool has no empty slot left. */
+MOE_API int moe_cache_prefill(moe_cache* c, int layer, const int32_t* h_ids, int n, void* stream);
+
+/* Pin (never evict) or unpin slot `slot` of the pool of `layer` [P4
+ * Consumer: pinned slots are never chosen].  Enqueued on `stream`. */
+MOE_API int moe_cache_pin(moe_cache* c, int layer, int slot, int pinned, void* stream);
+
+/* Admission of one layer's step, "lru_ensure" [P3 Problem, Solution; P2 What
+ * we changed; P1 sections 4-5].  One CTA on `stream`:
+ *   clock += 1 for the layer's pool; ids outside [0, E) -> -1 (invalid);
+ *   distinct valid ids D (ascending); decode_freq += routes per id;
+ *   demand_freq += 1, last_demand = clock for each id of D;
+ *   hits: stamp = clock; misses M = D minus hits, ascending;
+ *   admitted A = the first min(fetch_cap, |M|) of M (all of M if fetch_cap < 0);
+ *   victims: unpinned slots with stamp < clock (never a slot touched by this
+ *     admission), ascending (stamp, slot) -- empty slots (stamp 0) first,
+ *     lowest index first; the i-th of A takes the i-th victim, evicting its
+ *     old expert; the plan lists (slot, layer, expert) in that order;
+ *   d_slot_ids[r] = slot of ids[r] if resident now, else -1.
+ * d_slot_ids may equal d_ids (in-place rewrite).  n_routes may be 0.
+ * MOE_ERR_CAPACITY if n_routes > max_routes. */
+MOE_API int moe_admit(moe_cache* c, int layer, const int32_t* d_ids, int32_t* d_slot_ids, int n_routes,
+              int fetch_cap, void* stream);
+
+/* Look-ahead prefetch for `layer` [P4 Consumer, Eviction guard].  One CTA on
+ * `stream`; the clock does not advance.  Ids outside [0, E) are ignored
+ * (pf_invalid), the rest deduplicated (pf_requests); resident ones are left
+ * alone (pf_resident).  Each other id, ascending, looks at the first
+ * evictable slot (unpinned, stamp < clock, ascending (stamp, slot)); if that
+ * slot holds an expert with demand_freq >= 2 and
+ *     4 * score(resident) > 5 * score(predicted) + 4 * (4 << 8),
+ *     score(key) = (min(demand_freq, 2^24-1) << 8) | recency,
+ *     recency = 255 - min(255, clock - last_demand), 0 if never demanded,
+ * the prediction is dropped (pf_dropped_guard), never forced into another
+ * slot; otherwise the slot is (evicted and) filled, stamped with the current
+ * clock, and listed in the prefetch plan.  No evictable slot: pf_no_victim.
+ * MOE_ERR_STATE if the cache was created with max_pred = 0. */
+MOE_API int moe_prefetch(moe_cache* c, int layer, const int32_t* d_pred, int n, void* stream);
+
+/* The gather, "copy_missing" [P2 Problem, What we changed]: copy every entry
+ * of the demand or prefetch plan from its pinned host blob into its slot.  The
+ * grid reads the device-side count, so the call needs no host sync and its
+ * launch does not depend on the miss count.  MOE_ERR_STATE if the cache has no
+ * slot storage. */
+MOE_API int moe_gather_missing(moe_cache* c, int which, void* stream);
+
+/* Undo the bookings of a plan whose copy failed or was abandoned: each of its
+ * slots that still holds the planned expert becomes empty and the expert
+ * non-resident.  Statistics are not rewound. */
+MOE_API int moe_rollback_plan(moe_cache* c, int which, void* stream);
+
+/* The routed expert FFNs over the slots plus the shared expert and the
+ * weighted combine [P2 Problem, What we changed; P1 section 5; P3 Tests]:
+ *   out[b] = bf16( sum_j w[b,j] * FFN_slot[b,j](x[b]) + shared(x[b]) ).
+ * d_x bf16 [n_rows][H]; d_slot_ids int32 [n_rows][k] (-1 = skip);
+ * d_w float32 [n_rows][k]; d_shared_blob / d_shared_gate: device shared
+ * expert (NULL = none; requires shared_inter > 0); d_out bf16 [n_rows][H]
+ * (must not alias d_x).  MOE_ERR_CAPACITY if n_rows > max_rows or
+ * n_rows*k > max_routes. */
+MOE_API int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const int32_t* d_slot_ids,
+                       const float* d_w, int n_rows, int k, const void* d_shared_blob,
+                       const void* d_shared_gate, void* d_out, void* stream);
+
+/* One whole offloaded decode layer [P2 What we changed, order inside one layer]:
+ *   compute: admit -> [prefetch layer+1] -> record(ready) -> shared expert + gate
+ *            -> wait(done) -> routed FFNs + combine
+ *   side:    wait(ready) -> gather (demand) -> record(done) -> gather (prefetch)
+ * With flags & MOE_OVERLAP the gather runs on side_stream and the two events
+ * fork and join it (capturable: both edges are recorded into the graph).
+ * Without it everything runs on compute_stream in the same order (serial
+ * mode, also the mode to profile with ncu).  d_slot_ids int32 [n_rows*k]
+ * receives the rewritten ids (may equal d_ids).  d_pred/n_pred (NULL/0 = none)
+ * are predicted ids of layer+1; their gather is queued on the side stream
+ * after this layer's demand gather and is joined by layer+1's own wait.  Must
+ * not be mixed with moe_gather_missing(MOE_PLAN_PREFETCH) calls of its own. */
+MOE_API int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,
+                     const float* d_w, int32_t* d_slot_ids, int n_rows, int k, int fetch_cap,
+                     const int32_t* d_pred, int n_pred, const void* d_shared_blob,
+                     const void* d_shared_gate, void* d_out, void* compute_stream,
+                     void* side_stream, unsigned flags);
+
+/* Copy one layer's counters to the host.  Synchronises the device. */
+MOE_API int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out);
+
+/* Device pointers into the state (valid until moe_cache_destroy). */
+MOE_API int moe_device_views(moe_cache* c, moe_views* out);
+
+/* Test hook: make the next moe_gather_missing call fail with MOE_ERR_INJECTED
+ * before it enqueues anything (the plan's bookings stay; the caller is
+ * expected to call moe_rollback_plan).  n = 0 clears the request. */
+MOE_API int moe_cache_fail_next_gather(moe_cache* c, int n);
+
+/* Text of an error code; last CUDA error text seen by this thread. */
+MOE_API const char* moe_strerror(int err);
+MOE_API const char* moe_last_cuda_error(void);
+MOE_API int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_CACHE_H */

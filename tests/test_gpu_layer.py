@@ -1,0 +1,243 @@
+"""Whole offloaded decode layers on the GPU against the fp64 oracle.
+
+Outputs must agree elementwise within |gpu - ref| <= atol + rtol*|ref|
+(NVFP4: atol 2e-2, rtol 1e-2; bf16: atol 5e-3, rtol 1e-2); slot ids, plans,
+statistics and the whole cache state must be bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests.gpu_util import Rig, assert_close, assert_state_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(a, dtype=None):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+class Stepper:
+    """Feeds one workload's steps through moe_decode_layer, mirroring every
+    admission/prefetch on the oracle."""
+
+    def __init__(self, rig: Rig, overlap: bool = True, n_pred: int = 0):
+        self.rig = rig
+        self.overlap = overlap
+        self.n_pred = n_pred
+        self.side = torch.cuda.Stream()
+        w = rig.w
+        self.out = torch.empty(w.n_layers, w.batch, w.hidden, dtype=torch.bfloat16, device="cuda")
+        self.slots = torch.empty(w.n_layers, w.batch * w.top_k, dtype=torch.int32, device="cuda")
+
+    def step(self, t: int, ids: np.ndarray, wts: np.ndarray, x: np.ndarray, check_state=True,
+             layers=None):
+        rig, w, m = self.rig, self.rig.w, self.rig.m
+        cs = torch.cuda.current_stream()
+        d_x = _dev(x)
+        d_ids = _dev(ids.reshape(w.n_layers, -1))
+        d_w = _dev(wts.reshape(w.n_layers, -1))
+        flags = m.MOE_OVERLAP if self.overlap else 0
+        refs = []
+        for layer in range(w.n_layers):
+            pred = None
+            if self.n_pred and layer + 1 < w.n_layers:
+                pred = synth.make_predictions(w, ids[layer + 1], t, layer)
+            m.moe_decode_layer(rig.sc.handle, layer, d_x[layer], d_ids[layer], d_w[layer],
+                               self.slots[layer], w.batch, w.top_k, w.fetch_cap,
+                               None if pred is None else _dev(pred), 0 if pred is None else len(pred),
+                               rig.shared_blob, rig.shared_gate, self.out[layer], cs, self.side,
+                               flags)
+            refs.append(rig.oc.admit(layer, ids[layer].ravel(), w.fetch_cap))
+            if pred is not None:
+                rig.oc.prefetch(layer + 1, pred)
+        torch.cuda.synchronize()
+        got = self.slots.cpu().numpy()
+        for layer in range(w.n_layers):
+            assert np.array_equal(got[layer], refs[layer]["slots"]), f"step {t} layer {layer}"
+        if check_state:
+            assert_state_equal(rig.sc, rig.oc, what=f"step {t}")
+        return refs
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+def test_tiny_all_steps(overlap):
+    w = synth.workloads()["tiny"]
+    rig = Rig(w)
+    st = Stepper(rig, overlap)
+    ids, wts = synth.make_routing(w)
+    worst = 0.0
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        st.step(t, ids[t], wts[t], x)
+        ref = rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0])
+        worst = max(worst, assert_close(st.out[0], ref, w.fmt, f"step {t}")["max_abs"])
+    s = rig.sc.stats(0)
+    assert s["misses"] > 0 and s["evictions"] > 0 and s["hits"] > 0
+
+
+def test_tiny_with_shared_expert_and_batch():
+    w = synth.scaled(synth.workloads()["tiny"], shared_inter=96, batch=5, steps=12, n_slots=9)
+    rig = Rig(w)
+    st = Stepper(rig)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        st.step(t, ids[t], wts[t], x)
+        assert_close(st.out[0], rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0]), w.fmt, f"step {t}")
+
+
+def test_overlap_bytes_equal_serial():
+    """[FreeToken issue #753, Correctness]: only where the gather runs differs,
+    so overlapped outputs are byte-equal to serial ones."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=6, steps=12)
+    blobs = synth.HostBlobs(w, pinned=True)
+    a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    sa, sb = Stepper(a, True), Stepper(b, False)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        sa.step(t, ids[t], wts[t], x)
+        sb.step(t, ids[t], wts[t], x)
+        assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16)), f"step {t}"
+
+
+def test_slot_placement_does_not_change_bits():
+    """[FreeToken PR #680, Tests]: the GEMV over the slots equals the GEMV over
+    the streamed layer exactly.  Here: the same experts placed in different
+    slots (a cold cache vs. one pre-filled in another order) give identical
+    output bytes."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=2, steps=4, n_slots=64)
+    blobs = synth.HostBlobs(w, pinned=True)
+    a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    b.prefill(0, np.arange(255, 215, -1, dtype=np.int32))
+    sa, sb = Stepper(a), Stepper(b)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        sa.step(t, ids[t], wts[t], x)
+        sb.step(t, ids[t], wts[t], x)
+        assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16))
+    assert not np.array_equal(sa.slots.cpu().numpy(), sb.slots.cpu().numpy())
+
+
+@pytest.mark.slow
+def test_qwen3moe_full_size():
+    """The decode benchmark's workload at full size (40 layers x 256 NVFP4
+    experts, 3,164 slots, shared expert), overlapped as benchmarked: state
+    exact every token, outputs of sampled tokens on every layer vs fp64."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], steps=20)
+    rig = Rig(w)
+    st = Stepper(rig)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        st.step(t, ids[t], wts[t], x)
+        if t in (0, w.steps - 1):
+            for layer in range(w.n_layers):
+                ref = rig.oracle_layer(layer, x[layer], ids[t, layer], wts[t, layer])
+                assert_close(st.out[layer], ref, w.fmt, f"token {t} layer {layer}")
+    misses = sum(rig.sc.stats(l)["misses"] for l in range(w.n_layers))
+    assert misses > 300
+
+
+@pytest.mark.slow
+def test_qwen3moe_graph_replay_equals_eager():
+    """One token (40 layers) captured as a CUDA graph and replayed with new
+    routes written into its input buffers equals the eager pipeline, byte for
+    byte, with identical cache state [FreeToken issue #753, What we changed:
+    fixed addresses, device-side miss counts, no host sync]."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=8, steps=10)
+    blobs = synth.HostBlobs(w, pinned=True)
+    eager, graphed = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    se = Stepper(eager)
+    m = graphed.m
+    ids, wts = synth.make_routing(w)
+    L, R = w.n_layers, w.routes
+    b_x = torch.empty(L, w.batch, w.hidden, dtype=torch.int16, device="cuda")
+    b_ids = torch.empty(L, R, dtype=torch.int32, device="cuda")
+    b_w = torch.empty(L, R, dtype=torch.float32, device="cuda")
+    b_slots = torch.empty(L, R, dtype=torch.int32, device="cuda")
+    b_out = torch.empty(L, w.batch, w.hidden, dtype=torch.bfloat16, device="cuda")
+    cs, side = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def enqueue():
+        for layer in range(L):
+            m.moe_decode_layer(graphed.sc.handle, layer, b_x[layer], b_ids[layer], b_w[layer],
+                               b_slots[layer], w.batch, w.top_k, -1, None, 0,
+                               graphed.shared_blob, graphed.shared_gate, b_out[layer], cs, side,
+                               m.MOE_OVERLAP)
+
+    def load(t):
+        b_x.copy_(_dev(synth.make_hidden(w, t)))
+        b_ids.copy_(_dev(ids[t].reshape(L, -1)))
+        b_w.copy_(_dev(wts[t].reshape(L, -1)))
+
+    load(0)
+    with torch.cuda.stream(cs):
+        enqueue()  # token 0 eagerly (also warms up)
+    torch.cuda.synchronize()
+    se.step(0, ids[0], wts[0], synth.make_hidden(w, 0))
+    assert torch.equal(b_out.view(torch.int16), se.out.view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        enqueue()
+    for t in range(1, w.steps):
+        load(t)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        se.step(t, ids[t], wts[t], synth.make_hidden(w, t))
+        assert torch.equal(b_out.view(torch.int16), se.out.view(torch.int16)), f"token {t}"
+        assert torch.equal(b_slots, se.slots)
+    for layer in range(L):
+        assert graphed.sc.stats(layer) == eager.sc.stats(layer)
+
+
+@pytest.mark.slow
+def test_wide_decode_step():
+    """600 rows x top-2 = 1,200 routes over 1,024 NVFP4 experts with 1,100
+    slots, 30% pre-resident: admission + gather + routed FFNs; every row's
+    slot ids exact, sampled rows' outputs vs fp64."""
+    w = synth.workloads()["wide_decode"]
+    rig = Rig(w)
+    rig.prefill(0, synth.prefill_ids(w))
+    st = Stepper(rig)
+    ids, wts = synth.make_routing(w, steps=1)
+    x = synth.make_hidden(w, 0)
+    st.step(0, ids[0], wts[0], x)
+    rows = np.random.default_rng(0).choice(w.batch, 12, replace=False)
+    ref = rig.oracle_layer(0, x[0][rows], ids[0, 0][rows], wts[0, 0][rows])
+    assert_close(st.out[0][torch.from_numpy(rows).cuda()], ref, w.fmt, "wide step rows")
+    s = rig.sc.stats(0)
+    assert s["fetched"] == s["misses"] > 400 and s["evictions"] == 0
+
+
+@pytest.mark.slow
+def test_hybrid_capped_prefetch_partial_plus_cpu():
+    """Capped fetch (4 per layer) + look-ahead prefetch over 48 bf16 layers:
+    the GPU computes the routes that got a slot, the oracle computes the -1
+    routes (the CPU side of [FreeToken PR #491, sections 4-5]); GPU partial +
+    CPU partial equals the full layer within the bf16 tolerance."""
+    w = synth.scaled(synth.workloads()["hybrid_prefetch"], steps=6)
+    rig = Rig(w)
+    st = Stepper(rig, n_pred=w.n_pred)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        refs = st.step(t, ids[t], wts[t], x)
+        if t in (0, w.steps - 1):
+            for layer in (0, 1, 23, 47):
+                slots = refs[layer]["slots"].reshape(w.batch, w.top_k)
+                cpu_mask = (slots < 0).astype(np.uint8)
+                full = rig.oracle_layer(layer, x[layer], ids[t, layer], wts[t, layer])
+                cpu = rig.oracle_layer(layer, x[layer], ids[t, layer], wts[t, layer], mask=cpu_mask)
+                got = st.out[layer].float().cpu().numpy().astype(np.float64) + cpu
+                atol, rtol = 5e-3, 1e-2
+                assert np.all(np.abs(got - full) <= atol + rtol * np.abs(full)), (t, layer)
+    tot = [rig.sc.stats(l) for l in range(w.n_layers)]
+    assert sum(s["overflow_routes"] for s in tot) > 0 and sum(s["pf_filled"] for s in tot) > 0
