@@ -39,6 +39,7 @@ struct DevState {
   size_t stride;           // bytes between slots
   size_t slot_bytes;       // bytes copied per expert
   int max_routes, max_pred;
+  unsigned long long* status;  // device status word (MOE_STATUS_* bits not tied to a layer)
 };
 
 __host__ __device__ inline int pool_of(const DevState& st, int layer) {
@@ -158,5 +159,16 @@ cudaError_t launch_routed_down_combine(const DevState& st, int wfmt, int H, int 
                                        const int32_t* slot_ids, const float* w, int n_rows,
                                        int k, const float* shared_y, void* out, FfnScratch sc,
                                        cudaStream_t s);
+
+// Streaming expert FFNs for decode-sized steps (ffn_stream.cu).
+bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks);
+cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int max_tasks);
+cudaError_t launch_shared_stream(const DevState& st, int wfmt, int H, int Is, const void* x,
+                                 int n_rows, const uint8_t* blob, const void* gate_w,
+                                 FfnScratch sc, unsigned long long* status, cudaStream_t s);
+cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int layer,
+                                 const void* x, const int32_t* slot_ids, const float* w,
+                                 int n_rows, int k, const float* shared_y, void* out,
+                                 FfnScratch sc, unsigned long long* status, cudaStream_t s);
 
 }  // namespace moe

@@ -38,6 +38,7 @@ struct moe_cache {
   int gather_grid = 38;
   int down_k_max = 0;        // largest k the down kernel's shared memory was sized for
   int last_pf_layer = 0;     // target layer of the last prefetch enqueued (selects its plan)
+  bool stream_ffn = true;    // decode-sized steps use the streaming FFN kernels
 };
 
 namespace {
@@ -161,7 +162,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_h = cv.take<float>((size_t)d.max_routes * std::max(I, 1)),
                o_hs = cv.take<float>((size_t)d.max_rows * std::max(Is, 1)),
                o_gate = cv.take<float>(d.max_rows),
-               o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1));
+               o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1)),
+               o_status = cv.take<unsigned long long>(1);
   c->mem_bytes = align_up(cv.off, 256);
   e = cudaMalloc(&c->mem, c->mem_bytes);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMalloc(state)"));
@@ -195,6 +197,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   st.slot_bytes = d.slot_bytes;
   st.max_routes = d.max_routes;
   st.max_pred = d.max_pred;
+  st.status = reinterpret_cast<unsigned long long*>(m + o_status);
   c->sc.h = reinterpret_cast<float*>(m + o_h);
   c->sc.hs = reinterpret_cast<float*>(m + o_hs);
   c->sc.gate = reinterpret_cast<float*>(m + o_gate);
@@ -236,6 +239,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     // the down kernel stages k routes' intermediates in shared memory
     c->down_k_max = (int)std::min<size_t>(d.max_routes, (200 * 1024) / ((size_t)I * 4));
     e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
+    if (e == cudaSuccess) e = moe::ffn_stream_init(d.wfmt, H, I, Is, d.max_rows, d.max_routes);
     if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
   }
   e = cudaEventCreateWithFlags(&c->ev_ready, cudaEventDisableTiming);
@@ -357,6 +361,12 @@ static int check_compute(moe_cache* c, int layer, int n_rows, int k, const void*
 static int run_shared(moe_cache* c, const void* d_x, int n_rows, const void* blob, const void* gate,
                       cudaStream_t s) {
   if (n_rows == 0) return MOE_OK;
+  if (c->stream_ffn &&
+      moe::ffn_stream_supported(c->d.wfmt, c->d.hidden, c->d.shared_inter, n_rows, n_rows)) {
+    CK(moe::launch_shared_stream(c->st, c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows,
+                                 static_cast<const uint8_t*>(blob), gate, c->sc, c->st.status, s));
+    return MOE_OK;
+  }
   CK(moe::launch_shared_expert(c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows,
                                static_cast<const uint8_t*>(blob), gate, c->sc, s));
   return MOE_OK;
@@ -367,6 +377,11 @@ static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* s
                       cudaStream_t s) {
   const moe_cache_desc& d = c->d;
   if (n_rows == 0) return MOE_OK;
+  if (c->stream_ffn && moe::ffn_stream_supported(d.wfmt, d.hidden, d.inter, n_rows, n_rows * k)) {
+    CK(moe::launch_routed_stream(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w, n_rows,
+                                 k, with_shared ? c->sc.ys : nullptr, d_out, c->sc, c->st.status, s));
+    return MOE_OK;
+  }
   if (k > 0)
     CK(moe::launch_routed_up(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, n_rows, k,
                            c->sc, s));
@@ -440,6 +455,9 @@ int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out) {
   if (check_layer(c, layer) != MOE_OK || !h_out) return MOE_ERR_INVALID_ARG;
   CK(cudaDeviceSynchronize());
   CK(cudaMemcpy(h_out, c->st.stats + layer, sizeof(moe_stats), cudaMemcpyDeviceToHost));
+  unsigned long long dev_status = 0;
+  CK(cudaMemcpy(&dev_status, c->st.status, sizeof dev_status, cudaMemcpyDeviceToHost));
+  h_out->status_bits |= dev_status;
   return MOE_OK;
 }
 

@@ -129,6 +129,7 @@ typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 /* status_bits of moe_stats */
 #define MOE_STATUS_INVALID_ID 1ull
 #define MOE_STATUS_CAPACITY 2ull
+#define MOE_STATUS_TIMEOUT 4ull   /* a bounded device wait gave up (reported in every layer) */
 
 typedef struct moe_cache moe_cache; /* opaque */
 

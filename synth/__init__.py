@@ -252,13 +252,13 @@ class HostBlobs:
         return [self.blob(layer * E + e) for e in range(E)]
 
 
-def make_shared(w: Workload):
-    """Shared expert blob (uint8) and its sigmoid-gate vector (bf16 bits [H])."""
+def make_shared(w: Workload, layer: int = 0):
+    """Layer's shared expert blob (uint8) and its sigmoid-gate vector (bf16 bits [H])."""
     if not w.shared_inter:
         return None, None
     blob = np.empty(blob_bytes(w.fmt, w.hidden, w.shared_inter), np.uint8)
-    fill_blob(blob, w.fmt, w.hidden, w.shared_inter, Rng(w.seed, S_SHARED, 0))
-    gate = to_bf16_bits(Rng(w.seed, S_SHARED, 1).normal(w.hidden) * 0.02)
+    fill_blob(blob, w.fmt, w.hidden, w.shared_inter, Rng(w.seed, S_SHARED, layer, 0))
+    gate = to_bf16_bits(Rng(w.seed, S_SHARED, layer, 1).normal(w.hidden) * 0.02)
     return blob, gate
 
 

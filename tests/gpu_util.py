@@ -110,13 +110,13 @@ class Rig:
             max_routes=mr, max_rows=max_rows or max(w.batch, 1),
             max_pred=w.n_pred if max_pred is None else max_pred, gather_ctas=gather_ctas)
         self.oc = oracle.OracleCache(w.n_layers, w.n_experts, w.n_slots, w.per_layer_pools)
-        self.shared_blob = self.shared_gate = None
-        self.h_shared_blob = self.h_shared_gate = None
+        # one shared expert per layer (host copy for the oracle, device copy for the GPU)
+        self.h_shared = [(None, None)] * w.n_layers
+        self.d_shared = [(None, None)] * w.n_layers
         if compute and w.shared_inter:
-            sb, sg = synth.make_shared(w)
-            self.h_shared_blob, self.h_shared_gate = sb, sg
-            self.shared_blob = torch.from_numpy(sb).cuda()
-            self.shared_gate = torch.from_numpy(sg.view(np.int16)).cuda()
+            self.h_shared = [synth.make_shared(w, l) for l in range(w.n_layers)]
+            self.d_shared = [(torch.from_numpy(b).cuda(), torch.from_numpy(g.view(np.int16)).cuda())
+                             for b, g in self.h_shared]
 
     def prefill(self, layer: int, ids) -> None:
         ids = np.ascontiguousarray(ids, dtype=np.int32)
@@ -133,5 +133,5 @@ class Rig:
         w = self.w
         return oracle.layer(w.fmt, [self.blobs.addr(layer * w.n_experts + e) for e in range(w.n_experts)],
                             w.n_experts, w.hidden, w.inter, x, ids, wts, mask=mask,
-                            shared_blob=self.h_shared_blob, shared_inter=w.shared_inter,
-                            shared_gate_w=self.h_shared_gate)
+                            shared_blob=self.h_shared[layer][0], shared_inter=w.shared_inter,
+                            shared_gate_w=self.h_shared[layer][1])

@@ -50,7 +50,7 @@ class Stepper:
             m.moe_decode_layer(rig.sc.handle, layer, d_x[layer], d_ids[layer], d_w[layer],
                                self.slots[layer], w.batch, w.top_k, w.fetch_cap,
                                None if pred is None else _dev(pred), 0 if pred is None else len(pred),
-                               rig.shared_blob, rig.shared_gate, self.out[layer], cs, self.side,
+                               *rig.d_shared[layer], self.out[layer], cs, self.side,
                                flags)
             refs.append(rig.oc.admit(layer, ids[layer].ravel(), w.fetch_cap))
             if pred is not None:
@@ -169,7 +169,7 @@ def test_qwen3moe_graph_replay_equals_eager():
         for layer in range(L):
             m.moe_decode_layer(graphed.sc.handle, layer, b_x[layer], b_ids[layer], b_w[layer],
                                b_slots[layer], w.batch, w.top_k, -1, None, 0,
-                               graphed.shared_blob, graphed.shared_gate, b_out[layer], cs, side,
+                               *graphed.d_shared[layer], b_out[layer], cs, side,
                                m.MOE_OVERLAP)
 
     def load(t):
