@@ -147,6 +147,7 @@ struct FfnScratch {
   float* hs;        // [max_rows * Is] shared intermediate
   float* gate;      // [max_rows] sigmoid gate of the shared expert
   float* ys;        // [max_rows * H] shared expert output (gated)
+  unsigned long long* bar;  // grid-barrier counter of the fused FFN kernel (only grows)
 };
 
 cudaError_t launch_shared_expert(int wfmt, int H, int Is, const void* x, int n_rows,

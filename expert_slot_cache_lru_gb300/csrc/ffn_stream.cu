@@ -8,17 +8,17 @@
 // fast path when every (route, row) of the step fits a small task list.
 //
 // A decode step moves ~14 MB of weights per layer, which the HBM delivers in
-// ~2 us, so the kernel must have megabytes in flight almost at once.  Each
-// warp owns a list of weight rows and keeps a ring of up to 8 of them in
-// flight: lane 0 issues cp.async.bulk copies (global -> shared, completion on
-// a per-stage mbarrier) and the warp decodes stages as they land.  One CTA
-// per SM.  The down-projection kernel is launched as a programmatic
-// dependent of the gate/up kernel: it starts while gate/up still runs, loads
-// its weights, and waits (griddepcontrol.wait) only before it reads h.
+// ~2 us, so the kernel must have megabytes in flight almost at once.  One
+// cooperative launch of one CTA per SM computes a whole group of expert FFNs:
+// gate/up rows (phase A), a grid-wide barrier, then down rows and the combine
+// (phase B).  A producer warp streams the weight rows of both phases through
+// a ring of shared-memory stages with cp.async.bulk (completion on per-stage
+// mbarriers), so phase-B weights land while phase A computes; sixteen
+// consumer warps decode the stages as they land.
 //
-// Every wait on an mbarrier is bounded (%globaltimer); on a timeout the kernel
-// sets MOE_STATUS_TIMEOUT in the cache's device status word, drains its own
-// copies (again bounded) and returns.
+// Every wait (mbarrier, grid barrier) is bounded (%globaltimer); on a timeout
+// the kernel sets MOE_STATUS_TIMEOUT in the cache's device status word, skips
+// the remaining work, drains its own copies (again bounded) and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -33,6 +33,7 @@ constexpr int kST = 32 * kSW;      // threads per CTA
 constexpr int kMaxStages = 8;      // ring depth
 constexpr int kMaxTasks = 64;      // routes per call on this path
 constexpr int kXW = 4;             // x words (8 bf16 each) held per consumer thread
+constexpr int kYsPre = 2;          // shared-expert outputs prefetched per consumer thread
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
 
 // ------------------------------------------------------------ PTX wrappers
@@ -71,6 +72,27 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most n of this thread's most recent groups are still pending (n <= 7)
+__device__ __forceinline__ void cp_async_wait(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
+}
+// cooperative copy of `bytes` (multiple of 16) by kST threads, 16 bytes each
+__device__ __forceinline__ void copy_async(uint8_t* dst, const uint8_t* src, uint32_t bytes) {
+  for (uint32_t o = threadIdx.x * 16; o < bytes; o += kST * 16) cp_async16(dst + o, src + o);
+}
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -90,10 +112,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
   return true;
 }
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------ decode helpers
 // NVFP4 decode uses the hardware conversions: cvt.rn.f16x2.e2m1x2 (two FP4
@@ -168,6 +186,20 @@ __device__ __forceinline__ float dot8_fp4_f(uint32_t w, const float* h) {
   a = fmaf(f.x, h[4], fmaf(f.y, h[5], a));
   f = h2_f32(e2m1x2_h2<3>(w));
   return fmaf(f.x, h[6], fmaf(f.y, h[7], a));
+}
+// sum_{i<8} e2m1(nibble i of w) * h[i] with h given as f16 hi + lo parts
+// (h = hi + lo to ~22 bits); products exact, fp32 accumulate
+__device__ __forceinline__ float dot8_fp4_hl(uint32_t w, const uint32_t* hi, const uint32_t* lo) {
+  const uint32_t c0 = e2m1x2_h2<0>(w), c1 = e2m1x2_h2<1>(w), c2 = e2m1x2_h2<2>(w),
+                 c3 = e2m1x2_h2<3>(w);
+  float a = fma2_h(c0, hi[0], 0.f), b = fma2_h(c0, lo[0], 0.f);
+  a = fma2_h(c1, hi[1], a);
+  b = fma2_h(c1, lo[1], b);
+  a = fma2_h(c2, hi[2], a);
+  b = fma2_h(c2, lo[2], b);
+  a = fma2_h(c3, hi[3], a);
+  b = fma2_h(c3, lo[3], b);
+  return a + b;
 }
 // sum_{i<8} bf16 weights (uint4) * bf16 x (uint4), fp32
 __device__ __forceinline__ float dot8_bf16_bf(uint4 w, uint4 x, float a) {
@@ -258,23 +290,6 @@ __device__ void tasks_compact(Tasks& tk, int R) {
     tk.n = n;
   }
 }
-template <int FMT>
-__device__ void tasks_consts(Tasks& tk, int H, int I, const float* w) {
-  const int t = threadIdx.x;
-  if (t < tk.n) {
-    tk.wt[t] = w ? w[tk.route[t]] : 1.f;
-    if (FMT == MOE_W_NVFP4) {
-      const size_t ih = (size_t)I * H;
-      const float* g = reinterpret_cast<const float*>(tk.blob[t] + 3 * ih / 2 + 3 * (ih / 16));
-      tk.gs[t][0] = g[0];
-      tk.gs[t][1] = g[1];
-      tk.gs[t][2] = g[2];
-    } else {
-      tk.gs[t][0] = tk.gs[t][1] = tk.gs[t][2] = 1.f;
-    }
-  }
-}
-
 __device__ void flag_timeout(unsigned long long* status) {
   if (status) atomicOr(status, (unsigned long long)MOE_STATUS_TIMEOUT);
 }
@@ -312,49 +327,105 @@ __host__ __device__ inline int rows_per_chunk(int row_bytes, int cap) {
   return rc;
 }
 
-// ---------------------------------------------------------------- gate / up
-// Rows u of the flattened (task, n) list -> h[route][n] = silu(g) * u.
+// ---------------------------------------------------------------- grid barrier
+// One CTA per SM, launched cooperatively, so every CTA of the grid is resident.
+// `ctr` only grows: each launch adds gridDim.x, and a CTA waits until the count
+// reaches the next multiple of gridDim.x.  Release/acquire at GPU scope orders
+// the h written before the barrier with the reads after it.  Bounded spin.
+__device__ bool grid_barrier(unsigned long long* ctr, unsigned long long* status) {
+  __shared__ int s_ok;
+  consumers_sync();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    unsigned long long old;
+    asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
+    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+    unsigned long long v = 0;
+    const unsigned long long t0 = now_ns();
+    int ok = 1;
+    for (;;) {
+      asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+      if (v >= target) break;
+      if (now_ns() - t0 > kWaitNs) {
+        flag_timeout(status);
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    s_ok = ok;
+  }
+  consumers_sync();
+  return s_ok != 0;
+}
+
+// ---------------------------------------------------------------- fused FFN
+// One launch computes a group of expert FFNs for a decode-sized step:
+//   phase A (gate/up): rows u of the flattened (task, n) list,
+//       h[route][n] = silu(W_g x_b)[n] * (W_u x_b)[n];
+//   grid barrier;
+//   phase B (down + combine): output rows (b, n),
+//       SHARED: ys[b][n] = sigmoid(x_b . w_g) * (W_d h_b)[n]
+//       ROUTED: out[b][n] = bf16( sum_j w[b,j] (W_d[slot] h_bj)[n] + ys[b][n] ).
+// The producer warp streams the chunks of both phases through one ring of
+// stages with cp.async.bulk: phase-B weights arrive during phase A and the
+// barrier; after the barrier only h (a few KB, from L2) is read.
 //
-// x is staged in shared memory once per CTA: as f16 for NVFP4 experts (so the
-// products e2m1 * x are exact halves-times-halves), scaled per row by a power
-// of two so the largest |x| is below 2^15 -- a bf16 value converts to f16
-// exactly in that range, and the scale is undone on the fp32 sums -- or as
-// bf16 for bf16 experts.
-template <int FMT>
-__global__ void __launch_bounds__(kST + 32, 2)
-stream_up_kernel(DevState st, int H, int I, int layer, const uint16_t* __restrict__ x, int k,
-                 const int32_t* __restrict__ slot_ids, int R, const uint8_t* fixed_blob,
-                 float* __restrict__ h, int n_rows, int nstage, int stage_bytes,
-                 unsigned long long* status, const uint16_t* __restrict__ gate_w,
-                 float* __restrict__ gate_out) {
+// Phase A chunk: rcA consecutive rows of one task, gate and up banks.
+// Phase B chunk: rcB rows of one batch row b for a group of up to tpc of b's
+// tasks.  Consumer warps split a chunk into (task, K slice, row) items, keep
+// their slice of x (A) or h (B) in registers, read weights with lane-contiguous
+// loads, and combine slice partials through shared memory in a fixed order.
+//
+// x is staged once per CTA: as f16 for NVFP4 experts (products e2m1 * x exact
+// halves-times-halves), scaled per row by a power of two so that max |x| < 2^15
+// -- a bf16 value converts to f16 exactly in that range, and the scale is undone
+// on the fp32 sums -- or as bf16 for bf16 experts.
+struct FusedArgs {
+  int H, I, layer, k, R, n_rows;
+  const uint16_t* x;
+  const int32_t* slot_ids;
+  const uint8_t* fixed_blob;   // shared expert blob (SHARED) or null
+  const float* w;              // routing weights (ROUTED)
+  float* h;                    // [R][I] intermediate
+  const uint16_t* gate_w;      // SHARED: gate vector
+  float* gate;                 // SHARED: sigmoid gate per row (scratch)
+  float* ys;                   // SHARED: output [n_rows][H]; ROUTED: input (may be null)
+  __nv_bfloat16* out;          // ROUTED output
+  int nstage, stage_bytes, rcA, rcB, tpc;
+  unsigned long long* status;
+  unsigned long long* bar_ctr;
+};
+
+template <int FMT, bool SHARED>
+__global__ void __launch_bounds__(kST + 32, 1)
+ffn_fused_kernel(DevState st, FusedArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ Tasks tk;
   __shared__ Ring rg;
   __shared__ unsigned int xmax[16];  // per row max |x| (float bits, only when > 2^14)
   __shared__ float xscale[16];       // per row power-of-two scale applied to x
   __shared__ float xinv[16];         // per row 1 / scale
-  __shared__ float red[16][16][2];   // [row of chunk][K slice]: partials of gate and up
-  pdl_launch_dependents();  // the down kernel may start loading its weights now
+  __shared__ float gate_s[16];
+  __shared__ int ts[17];             // tasks of batch row b: [ts[b], ts[b+1])
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_bytes = FMT == MOE_W_NVFP4 ? 2 * (H / 2 + H / 16) : 2 * H * 2;
-  const int rc = rows_per_chunk(row_bytes, stage_bytes);
-  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);  // [n_rows][H]
-  uint8_t* ring = sm + ((size_t)n_rows * H * 2 + 127) / 128 * 128;
+  const int H = a.H, I = a.I, k = a.k, n_rows = a.n_rows;
 
-  // One global round trip for the routes' slots and all of x (8 bf16 per
-  // thread per uint4, kept in registers); then the compaction; then the
-  // producer starts copying while the consumers finish their set-up.
-  // (the consumer threads hold x: kXW uint4 each, so n_rows * H <= kXW * 8 * kST)
-  const int nx8 = n_rows * H / 8;          // uint4 words of x (H % 256 == 0)
+  const int rowB = FMT == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;            // down row bytes
+  const int nslA = H / 1024, nslB = I / 512;
+  const int rcA = a.rcA, rcB = a.rcB, tpc = a.tpc, nstage = a.nstage;
+
+  // ---- prologue: one global round trip for the routes' slots and all of x
+  const int nx8 = n_rows * H / 8;
   uint4 xw[kXW];
   if (threadIdx.x < 16) xmax[threadIdx.x] = 0u;
-  tasks_load(tk, st, layer, slot_ids, R, fixed_blob);
+  tasks_load(tk, st, a.layer, a.slot_ids, a.R, a.fixed_blob);
 #pragma unroll
   for (int j = 0; j < kXW; ++j) {
     const int i = threadIdx.x + j * kST;
-    if (threadIdx.x < kST && i < nx8) xw[j] = reinterpret_cast<const uint4*>(x)[i];
+    if (threadIdx.x < kST && i < nx8) xw[j] = reinterpret_cast<const uint4*>(a.x)[i];
   }
-  __syncthreads();  // xmax zeroed, task loads done
+  __syncthreads();
   if (FMT == MOE_W_NVFP4) {
 #pragma unroll
     for (int j = 0; j < kXW; ++j) {
@@ -369,7 +440,7 @@ stream_up_kernel(DevState st, int H, int I, int layer, const uint16_t* __restric
       if (mx > 16384.f) atomicMax(&xmax[(i * 8) / H], __float_as_uint(mx));
     }
   }
-  tasks_compact(tk, R);
+  tasks_compact(tk, a.R);
   if (threadIdx.x == 0) {
     for (int q = 0; q < nstage; ++q) {
       mbar_init(&rg.full[q], 1);
@@ -377,52 +448,145 @@ stream_up_kernel(DevState st, int H, int I, int layer, const uint16_t* __restric
     }
     fence_barrier_init();
   }
-  __syncthreads();  // tasks, barriers and every row's max |x| ready
+  __syncthreads();
   const int T = tk.n;
-  const int U = T * I;
-  const int per = (U + gridDim.x - 1) / gridDim.x;
-  const int u0 = min(U, per * blockIdx.x), u1 = min(U, u0 + per);
-  // chunks: rc rows each, never crossing a task boundary
+  if (threadIdx.x <= n_rows) {  // first task of each batch row (tasks are b-major)
+    int t = 0;
+    while (t < T && tk.route[t] / k < (int)threadIdx.x) ++t;
+    ts[threadIdx.x] = t;
+  }
+  __syncthreads();
+
+  // phase A rows of this CTA
+  const int UA = T * I;
+  const int perA = (UA + gridDim.x - 1) / gridDim.x;
+  const int u0 = min(UA, perA * blockIdx.x), u1 = min(UA, u0 + perA);
+  // phase B output rows of this CTA
+  const int UB = n_rows * H;
+  const int perB = (UB + gridDim.x - 1) / gridDim.x;
+  const int ru0 = min(UB, perB * blockIdx.x), ru1 = min(UB, ru0 + perB);
+
+  // shared memory: x | h [T][I] | y [T][perB] | redA [2][2][nslA*rcA] | redB [2][tpc*nslB*rcB] | ring
+  uint16_t* xs = reinterpret_cast<uint16_t*>(sm);
+  float* hsm = reinterpret_cast<float*>(sm + ((size_t)n_rows * H * 2 + 127) / 128 * 128);
+  float* ysm = hsm + (size_t)T * I;
+  float* redA = ysm + (size_t)T * perB;
+  const int redA_n = nslA * rcA;
+  float* redB = redA + 4 * redA_n;
+  const int redB_n = tpc * nslB * rcB;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(redB + 2 * redB_n) + 127) / 128 * 128);
   const BlobOff o(H, I);
 
-  if (warp == kSW) {  // ------------------------------------------ producer
+  // phase B chunk cursor: (b, row block n, task group t0); rows without tasks skipped
+  struct Cur {
+    int b, n, t0;
+  };
+  auto b_lo = [&](int b) { return max(ru0 - b * H, 0); };
+  auto b_hi = [&](int b) { return min(ru1 - b * H, H); };
+  auto settle = [&](Cur& c) -> bool {
+    while (c.b * H < ru1) {
+      if (ts[c.b] < ts[c.b + 1] && c.n < b_hi(c.b)) {
+        if (c.t0 < ts[c.b]) c.t0 = ts[c.b];
+        if (c.t0 < ts[c.b + 1]) return true;
+        c.t0 = ts[c.b];
+        c.n += rcB;
+        continue;
+      }
+      ++c.b;
+      if (c.b * H >= ru1) return false;
+      c.n = b_lo(c.b);
+      c.t0 = ts[c.b];
+    }
+    return false;
+  };
+  auto advance = [&](Cur& c) -> bool {
+    c.t0 += tpc;
+    return settle(c);
+  };
+  auto start = [&](Cur& c) -> bool {
+    if (ru0 >= ru1) return false;
+    c.b = ru0 / H;
+    c.n = b_lo(c.b);
+    c.t0 = ts[c.b];
+    return settle(c);
+  };
+
+  if (warp == kSW) {  // ================================================ producer
     if (lane == 0) {
       int q = 0;
-      for (int u = u0; u < u1;) {
-        const int t = u / I, n = u - t * I;
-        const int nr = min(rc, min(u1 - u, I - n));
-        const int s = q % nstage;
+      bool ok = true;
+      auto acquire = [&](int& s) -> bool {  // next stage, free
+        s = q % nstage;
         if (q >= nstage && !mbar_wait(&rg.empty[s], (uint32_t)(((q / nstage) - 1) & 1))) {
-          flag_timeout(status);
-          break;
+          flag_timeout(a.status);
+          return false;
         }
-        uint8_t* dst = ring + (size_t)s * stage_bytes;
-        const uint8_t* blob = tk.blob[t];
         fence_proxy_async();
+        return true;
+      };
+      for (int u = u0; u < u1 && ok;) {  // phase A
+        const int t = u / I, n = u - t * I;
+        const int nr = min(rcA, min(u1 - u, I - n));
+        int s;
+        if (!(ok = acquire(s))) break;
+        uint8_t* dst = ring + (size_t)s * a.stage_bytes;
+        const uint8_t* blob = tk.blob[t];
         if (FMT == MOE_W_NVFP4) {
           const uint32_t cb = nr * (H / 2), sb = nr * (H / 16);
           mbar_expect_tx(&rg.full[s], 2 * (cb + sb));
           bulk_g2s(dst, blob + o.code[0] + (size_t)n * (H / 2), cb, &rg.full[s]);
-          bulk_g2s(dst + rc * (H / 2), blob + o.code[1] + (size_t)n * (H / 2), cb, &rg.full[s]);
-          bulk_g2s(dst + 2 * rc * (H / 2), blob + o.scale[0] + (size_t)n * (H / 16), sb,
+          bulk_g2s(dst + rcA * (H / 2), blob + o.code[1] + (size_t)n * (H / 2), cb, &rg.full[s]);
+          bulk_g2s(dst + 2 * rcA * (H / 2), blob + o.scale[0] + (size_t)n * (H / 16), sb, &rg.full[s]);
+          bulk_g2s(dst + 2 * rcA * (H / 2) + rcA * (H / 16), blob + o.scale[1] + (size_t)n * (H / 16), sb,
                    &rg.full[s]);
-          bulk_g2s(dst + 2 * rc * (H / 2) + rc * (H / 16), blob + o.scale[1] + (size_t)n * (H / 16),
-                   sb, &rg.full[s]);
         } else {
           const uint32_t rb = nr * H * 2;
           mbar_expect_tx(&rg.full[s], 2 * rb);
           bulk_g2s(dst, blob + o.mat[0] + (size_t)n * H * 2, rb, &rg.full[s]);
-          bulk_g2s(dst + (size_t)rc * H * 2, blob + o.mat[1] + (size_t)n * H * 2, rb, &rg.full[s]);
+          bulk_g2s(dst + (size_t)rcA * H * 2, blob + o.mat[1] + (size_t)n * H * 2, rb, &rg.full[s]);
         }
         ++q;
         u += nr;
+      }
+      Cur c;
+      for (bool more = ok && start(c); more; more = advance(c)) {  // phase B
+        const int nr = min(rcB, b_hi(c.b) - c.n);
+        const int t1 = min(c.t0 + tpc, ts[c.b + 1]);
+        int s;
+        if (!acquire(s)) break;
+        uint8_t* dst = ring + (size_t)s * a.stage_bytes;
+        mbar_expect_tx(&rg.full[s], (t1 - c.t0) * nr * rowB);
+        for (int t = c.t0; t < t1; ++t) {  // stage: task-major, each task rcB rows
+          uint8_t* d = dst + (size_t)(t - c.t0) * rcB * rowB;
+          const uint8_t* blob = tk.blob[t];
+          if (FMT == MOE_W_NVFP4) {
+            bulk_g2s(d, blob + o.code[2] + (size_t)c.n * (I / 2), nr * (I / 2), &rg.full[s]);
+            bulk_g2s(d + rcB * (I / 2), blob + o.scale[2] + (size_t)c.n * (I / 16), nr * (I / 16),
+                     &rg.full[s]);
+          } else {
+            bulk_g2s(d, blob + o.mat[2] + (size_t)c.n * I * 2, nr * I * 2, &rg.full[s]);
+          }
+        }
+        ++q;
       }
       producer_drain(rg, nstage, q);
     }
     return;
   }
 
-  // ------------------------------------------------------------ consumers
+  // ================================================================ consumers
+  // per-task constants: loads issued now, stored to shared memory before use
+  float cg0 = 1.f, cg1 = 1.f, cg2 = 1.f, cw = 1.f;
+  if (threadIdx.x < T) {
+    if (!SHARED) cw = a.w[tk.route[threadIdx.x]];
+    if (FMT == MOE_W_NVFP4) {
+      const float* gp = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob);
+      cg0 = gp[0];
+      cg1 = gp[1];
+      cg2 = gp[2];
+    }
+  }
   if (threadIdx.x < n_rows) {
     float sc = 1.f;  // power of two bringing max |x| below 2^15
     const float mx = __uint_as_float(xmax[threadIdx.x]);
@@ -430,7 +594,6 @@ stream_up_kernel(DevState st, int H, int I, int layer, const uint16_t* __restric
     xscale[threadIdx.x] = sc;
     xinv[threadIdx.x] = 1.f / sc;
   }
-  tasks_consts<FMT>(tk, H, I, nullptr);
   consumers_sync();
 #pragma unroll
   for (int j = 0; j < kXW; ++j) {  // x into shared memory (f16 for NVFP4, bf16 otherwise)
@@ -451,370 +614,280 @@ stream_up_kernel(DevState st, int H, int I, int layer, const uint16_t* __restric
       reinterpret_cast<uint4*>(xs)[i] = xw[j];
     }
   }
+  if (threadIdx.x < T) {
+    tk.gs[threadIdx.x][0] = cg0;
+    tk.gs[threadIdx.x][1] = cg1;
+    tk.gs[threadIdx.x][2] = cg2;
+    tk.wt[threadIdx.x] = cw;
+  }
   consumers_sync();
   // the shared expert's sigmoid gate, sigmoid(x_b . w_g), in fp32
-  if (gate_w && blockIdx.x == 0 && warp < n_rows) {
+  if (SHARED && blockIdx.x == 0 && warp < n_rows) {
     float z = 0.f;
     for (int i0 = lane * 8; i0 < H; i0 += 256) {
-      const uint4 gv = *reinterpret_cast<const uint4*>(gate_w + i0);
-      const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)warp * H + i0);
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.gate_w + i0);
+      const uint4 xv = *reinterpret_cast<const uint4*>(a.x + (size_t)warp * H + i0);
       z = dot8_bf16_bf(gv, xv, z);
     }
     z = wsum(z);
-    if (lane == 0) gate_out[warp] = 1.f / (1.f + expf(-z));
+    if (lane == 0) a.gate[warp] = 1.f / (1.f + expf(-z));
   }
-  // Warp = (K slice of 1024 elements, row group).  The warp's slice of x stays
-  // in registers for every row it processes; the weights of a row slice are
-  // read with lane-contiguous 16-byte loads (no bank conflicts).
-  //   NVFP4: lane L takes elements [32L, 32L+32) of the slice (16 code bytes)
-  //   bf16:  lane L takes elements 8L + 256j + [0, 8), j = 0..3 (4 x 16 bytes)
-  const int nsl = H / 1024;
-  const int ngr = kSW / nsl;
-  const int my_sl = warp % nsl, my_g = warp / nsl;
-  uint4 xv[4];
-  int xb = -1;
+
   bool failed = false;  // a timed-out wait: keep taking part in the barriers, skip the work
   int q = 0;
-  for (int u = u0; u < u1; ++q) {
-    const int t = u / I, n = u - t * I;
-    const int nr = min(rc, min(u1 - u, I - n));
-    const int s = q % nstage;
-    if (!failed && !mbar_wait(&rg.full[s], (uint32_t)((q / nstage) & 1))) {
-      flag_timeout(status);
-      failed = true;
-    }
-    const int b = tk.route[t] / k;
-    if (b != xb) {  // this batch row's x slice into registers
-      const uint16_t* xr = xs + (size_t)b * H + my_sl * 1024;
+  // ---------------------------------------------------------------- phase A
+  // items (slice sl of 1024, row r), row fastest, contiguous per warp
+  //   NVFP4: lane L takes elements [32L, 32L+32) of the slice (16 code bytes)
+  //   bf16:  lane L takes elements 8L + 256m + [0, 8), m = 0..3 (4 x 16 bytes)
+  {
+    uint4 xv[4];
+    int xkey = -1;
+    for (int u = u0; u < u1; ++q) {
+      const int t = u / I, n = u - t * I;
+      const int nr = min(rcA, min(u1 - u, I - n));
+      const int s = q % nstage;
+      if (!failed && !mbar_wait(&rg.full[s], (uint32_t)((q / nstage) & 1))) {
+        flag_timeout(a.status);
+        failed = true;
+      }
+      const int b = tk.route[t] / k;
+      const uint8_t* stg = ring + (size_t)s * a.stage_bytes;
+      float* rd = redA + (size_t)(q & 1) * 2 * redA_n;
+      const int items = nslA * nr;
+      const int ipw = (items + kSW - 1) / kSW;
+      const int i0 = min(items, warp * ipw), i1 = min(items, i0 + ipw);
+      int sl = i0 / nr, r = i0 - sl * nr;
+      for (int it = i0; it < i1 && !failed; ++it, (++r == nr ? (r = 0, ++sl) : 0)) {
+        if (sl * 16 + b != xkey) {  // this batch row's x slice into registers
+          const uint16_t* xr = xs + (size_t)b * H + sl * 1024;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        xv[j] = FMT == MOE_W_NVFP4 ? reinterpret_cast<const uint4*>(xr + lane * 32)[j]
-                                   : *reinterpret_cast<const uint4*>(xr + lane * 8 + 256 * j);
-      xb = b;
-    }
-    const uint8_t* stg = ring + (size_t)s * stage_bytes;
-    for (int r = my_g; r < nr && !failed; r += ngr) {
-      float g = 0.f, up = 0.f;
-      if (FMT == MOE_W_NVFP4) {
-        const int e0 = my_sl * 1024 + lane * 32;
-        const uint4 cg = *reinterpret_cast<const uint4*>(stg + (size_t)r * (H / 2) + e0 / 2);
-        const uint4 cu = *reinterpret_cast<const uint4*>(stg + (size_t)(rc + r) * (H / 2) + e0 / 2);
-        const uint8_t* sc = stg + (size_t)2 * rc * (H / 2);
-        const float2 sg = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(sc + (size_t)r * (H / 16) + e0 / 16));
-        const float2 su =
-            e4m3x2_f32(*reinterpret_cast<const uint16_t*>(sc + (size_t)(rc + r) * (H / 16) + e0 / 16));
-        g = fmaf(dot8_fp4_h(cg.x, xv[0]) + dot8_fp4_h(cg.y, xv[1]), sg.x, 0.f);
-        g = fmaf(dot8_fp4_h(cg.z, xv[2]) + dot8_fp4_h(cg.w, xv[3]), sg.y, g);
-        up = fmaf(dot8_fp4_h(cu.x, xv[0]) + dot8_fp4_h(cu.y, xv[1]), su.x, 0.f);
-        up = fmaf(dot8_fp4_h(cu.z, xv[2]) + dot8_fp4_h(cu.w, xv[3]), su.y, up);
-      } else {
-        const uint8_t* rowg = stg + (size_t)r * H * 2 + (size_t)my_sl * 2048;
-        const uint8_t* rowu = stg + (size_t)(rc + r) * H * 2 + (size_t)my_sl * 2048;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          g = dot8_bf16_bf(*reinterpret_cast<const uint4*>(rowg + lane * 16 + 512 * j), xv[j], g);
-          up = dot8_bf16_bf(*reinterpret_cast<const uint4*>(rowu + lane * 16 + 512 * j), xv[j], up);
+          for (int m = 0; m < 4; ++m)
+            xv[m] = FMT == MOE_W_NVFP4 ? reinterpret_cast<const uint4*>(xr + lane * 32)[m]
+                                       : *reinterpret_cast<const uint4*>(xr + lane * 8 + 256 * m);
+          xkey = sl * 16 + b;
         }
-      }
-      g = wsum(g);
-      up = wsum(up);
-      if (lane == 0) {
-        red[r][my_sl][0] = g;
-        red[r][my_sl][1] = up;
-      }
-    }
-    consumers_sync();  // every slice of every row done, stage no longer read
-    if (threadIdx.x == 0) mbar_arrive_one(&rg.empty[s]);
-    if (threadIdx.x < nr && !failed) {  // one thread per row: slices in a fixed order
-      const int r = threadIdx.x;
-      float gs = 0.f, us = 0.f;
-      for (int sl = 0; sl < nsl; ++sl) {
-        gs += red[r][sl][0];
-        us += red[r][sl][1];
-      }
-      const float xi = FMT == MOE_W_NVFP4 ? xinv[b] : 1.f;
-      const float gg = gs * xi * tk.gs[t][0], uu = us * xi * tk.gs[t][1];
-      h[(size_t)tk.route[t] * I + n + r] = gg / (1.f + expf(-gg)) * uu;
-    }
-    consumers_sync();  // red[] reusable
-    u += nr;
-  }
-}
-
-// ---------------------------------------------------------------- down
-// SHARED: ys[b][n] = gate[b] * (W_d h_b)[n]  (one task per row b)
-// ROUTED: out[b][n] = bf16( sum_j w[b,j] * (W_d[slot] h_bj)[n] + ys[b][n] )
-// The CTA's output rows are a range of (b, n); for each batch row b in it the
-// chunks are (task of b, rc rows), tasks in route order; the per-task row
-// results are kept in shared memory and combined at the end in route order.
-template <int FMT, bool SHARED>
-__global__ void __launch_bounds__(kST + 32, 2)
-stream_down_kernel(DevState st, int H, int I, int layer, int k,
-                   const int32_t* __restrict__ slot_ids, int R, const uint8_t* fixed_blob,
-                   const float* __restrict__ w, const float* h, const float* gate_in,
-                   float* ys, __nv_bfloat16* out, int n_rows, int nstage, int stage_bytes,
-                   unsigned long long* status) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  __shared__ Tasks tk;
-  __shared__ Ring rg;
-  __shared__ float gate_s[16];
-  __shared__ int ts[17];  // tasks of batch row b: [ts[b], ts[b+1])
-  __shared__ float red[16][16];  // [row of chunk][K slice]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row_bytes = FMT == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
-  const int rc = rows_per_chunk(row_bytes, stage_bytes);
-  tasks_load(tk, st, layer, slot_ids, R, fixed_blob);
-  __syncthreads();
-  tasks_compact(tk, R);
-  __syncthreads();
-  const int T = tk.n;
-  if (threadIdx.x <= n_rows) {  // first task of each batch row (tasks are b-major)
-    int a = 0;
-    while (a < T && tk.route[a] / k < (int)threadIdx.x) ++a;
-    ts[threadIdx.x] = a;
-  }
-  if (threadIdx.x == 0) {
-    for (int q = 0; q < nstage; ++q) {
-      mbar_init(&rg.full[q], 1);
-      mbar_init(&rg.empty[q], 1);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  const int U = n_rows * H;
-  const int per = (U + gridDim.x - 1) / gridDim.x;
-  const int ru0 = min(U, per * blockIdx.x), ru1 = min(U, ru0 + per);
-  // shared memory: h of every task [T][I], then y[T][per] (per-task row results), then the ring
-  float* hsm = reinterpret_cast<float*>(sm);
-  float* ysm = hsm + (size_t)T * I;
-  uint8_t* ring = sm + (((size_t)T * I + (size_t)T * per) * 4 + 127) / 128 * 128;
-  const BlobOff o(H, I);
-
-  // chunk sequence: for b, for task t of b, for rows [n, n+nr) of b's range
-  auto first_chunk = [&](int* b, int* t, int* n) {
-    *b = ru0 / H;
-    *t = ts[*b];
-    *n = ru0 - *b * H;
-  };
-  // advance to the next chunk; false when done
-  auto next_chunk = [&](int* b, int* t, int* n, int nr) -> bool {
-    const int nb_end = min(ru1 - *b * H, H);
-    *n += nr;
-    if (*n < nb_end) return true;
-    ++*t;
-    *n = max(ru0 - *b * H, 0);
-    if (*t < ts[*b + 1]) return true;
-    ++*b;
-    if (*b * H >= ru1) return false;
-    *t = ts[*b];
-    *n = 0;
-    return true;
-  };
-  auto valid_chunk = [&](int* b, int* t, int* n) -> bool {  // skip rows without tasks
-    while (*b * H < ru1 && *t >= ts[*b + 1]) {
-      ++*b;
-      if (*b * H >= ru1) return false;
-      *t = ts[*b];
-      *n = 0;
-    }
-    return *b * H < ru1 && ru0 < ru1;
-  };
-  auto rows_of = [&](int b, int n) { return min(rc, min(ru1 - b * H, H) - n); };
-
-  if (warp == kSW) {  // ------------------------------------------ producer
-    if (lane == 0) {
-      int b, t, n, q = 0;
-      first_chunk(&b, &t, &n);
-      bool more = valid_chunk(&b, &t, &n);
-      while (more) {
-        const int nr = rows_of(b, n);
-        const int s = q % nstage;
-        if (q >= nstage && !mbar_wait(&rg.empty[s], (uint32_t)(((q / nstage) - 1) & 1))) {
-          flag_timeout(status);
-          break;
-        }
-        uint8_t* dst = ring + (size_t)s * stage_bytes;
-        const uint8_t* blob = tk.blob[t];
-        fence_proxy_async();
+        float g = 0.f, up = 0.f;
         if (FMT == MOE_W_NVFP4) {
-          const uint32_t cb = nr * (I / 2), sb = nr * (I / 16);
-          mbar_expect_tx(&rg.full[s], cb + sb);
-          bulk_g2s(dst, blob + o.code[2] + (size_t)n * (I / 2), cb, &rg.full[s]);
-          bulk_g2s(dst + rc * (I / 2), blob + o.scale[2] + (size_t)n * (I / 16), sb, &rg.full[s]);
+          const int e0 = sl * 1024 + lane * 32;
+          const uint4 cgw = *reinterpret_cast<const uint4*>(stg + (size_t)r * (H / 2) + e0 / 2);
+          const uint4 cuw = *reinterpret_cast<const uint4*>(stg + (size_t)(rcA + r) * (H / 2) + e0 / 2);
+          const uint8_t* sc = stg + (size_t)2 * rcA * (H / 2);
+          const float2 sg = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(sc + (size_t)r * (H / 16) + e0 / 16));
+          const float2 su =
+              e4m3x2_f32(*reinterpret_cast<const uint16_t*>(sc + (size_t)(rcA + r) * (H / 16) + e0 / 16));
+          g = fmaf(dot8_fp4_h(cgw.x, xv[0]) + dot8_fp4_h(cgw.y, xv[1]), sg.x, 0.f);
+          g = fmaf(dot8_fp4_h(cgw.z, xv[2]) + dot8_fp4_h(cgw.w, xv[3]), sg.y, g);
+          up = fmaf(dot8_fp4_h(cuw.x, xv[0]) + dot8_fp4_h(cuw.y, xv[1]), su.x, 0.f);
+          up = fmaf(dot8_fp4_h(cuw.z, xv[2]) + dot8_fp4_h(cuw.w, xv[3]), su.y, up);
         } else {
-          const uint32_t rb = nr * I * 2;
-          mbar_expect_tx(&rg.full[s], rb);
-          bulk_g2s(dst, blob + o.mat[2] + (size_t)n * I * 2, rb, &rg.full[s]);
+          const uint8_t* rowg = stg + (size_t)r * H * 2 + (size_t)sl * 2048;
+          const uint8_t* rowu = stg + (size_t)(rcA + r) * H * 2 + (size_t)sl * 2048;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            g = dot8_bf16_bf(*reinterpret_cast<const uint4*>(rowg + lane * 16 + 512 * m), xv[m], g);
+            up = dot8_bf16_bf(*reinterpret_cast<const uint4*>(rowu + lane * 16 + 512 * m), xv[m], up);
+          }
         }
-        ++q;
-        more = next_chunk(&b, &t, &n, nr) && valid_chunk(&b, &t, &n);
+        g = wsum(g);
+        up = wsum(up);
+        if (lane == 0) {
+          rd[it] = g;
+          rd[redA_n + it] = up;
+        }
       }
-      producer_drain(rg, nstage, q);
+      consumers_sync();  // every item of the chunk done, stage no longer read
+      if (threadIdx.x == 0) mbar_arrive_one(&rg.empty[s]);
+      if (threadIdx.x < nr && !failed) {  // one thread per row: slices in a fixed order
+        const int rr = threadIdx.x;
+        float gs = 0.f, us = 0.f;
+        for (int z = 0; z < nslA; ++z) {
+          gs += rd[z * nr + rr];
+          us += rd[redA_n + z * nr + rr];
+        }
+        const float xi = FMT == MOE_W_NVFP4 ? xinv[b] : 1.f;
+        const float gg = gs * xi * tk.gs[t][0], uu = us * xi * tk.gs[t][1];
+        a.h[(size_t)tk.route[t] * I + n + rr] = gg / (1.f + expf(-gg)) * uu;
+      }
+      u += nr;  // rd is double-buffered: the next chunk writes the other half
     }
-    return;
   }
 
-  // ------------------------------------------------------------ consumers
-  tasks_consts<FMT>(tk, H, I, SHARED ? nullptr : w);
-  // everything above overlaps the gate/up kernel; its outputs are read only
-  // after it has completed
-  pdl_wait();
+  // ---------------------------------------------------------------- barrier
+  if (!grid_barrier(a.bar_ctr, a.status)) failed = true;
   {  // every task's h into shared memory: float4 loads, four in flight per thread
     const int n4 = T * I / 4, i4 = I / 4;
     float4* hs4 = reinterpret_cast<float4*>(hsm);
-    const float4* h4 = reinterpret_cast<const float4*>(h);
+    const float4* h4 = reinterpret_cast<const float4*>(a.h);
     for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kST) {
       float4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int i = i0 + j * kST;
-        if (i < n4) v[j] = h4[(size_t)tk.route[i / i4] * i4 + (i % i4)];
+        if (i < n4) v[j] = __ldcg(&h4[(size_t)tk.route[i / i4] * i4 + (i % i4)]);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         if (i0 + j * kST < n4) hs4[i0 + j * kST] = v[j];
     }
   }
-  if (SHARED && threadIdx.x < n_rows) gate_s[threadIdx.x] = gate_in[threadIdx.x];
+  if (SHARED && threadIdx.x < n_rows) gate_s[threadIdx.x] = __ldcg(&a.gate[threadIdx.x]);
+  float ysv[kYsPre];  // the shared expert's output for this thread's combine rows
+#pragma unroll
+  for (int m = 0; m < kYsPre; ++m) {
+    const int ru = ru0 + threadIdx.x + m * kST;
+    ysv[m] = (!SHARED && a.ys && ru < ru1) ? a.ys[ru] : 0.f;
+  }
   consumers_sync();
 
-  // Warp = (K slice of 512 elements, row group); the warp's slice of h_t stays
-  // in registers while it walks the rows of task t.
+  // ---------------------------------------------------------------- phase B
+  // items (task j, slice sl of 512, row r), row fastest, contiguous per warp
   //   NVFP4: lane L takes elements [16L, 16L+16) of the slice (8 code bytes)
-  //   bf16:  lane L takes elements 8L + 256j + [0, 8), j = 0, 1 (2 x 16 bytes)
-  const int nsl = I / 512;
-  const int ngr = kSW / nsl;
-  const int my_sl = warp % nsl, my_g = warp / nsl;
+  //   bf16:  lane L takes elements 8L + 256m + [0, 8), m = 0, 1 (2 x 16 bytes)
   {
-    bool failed = false;  // a timed-out wait: keep taking part in the barriers, skip the work
     float hv[16];
-    int ht = -1;
-    int b, t, n, q = 0;
-    first_chunk(&b, &t, &n);
-    bool more = valid_chunk(&b, &t, &n);
-    while (more) {
-      const int nr = rows_of(b, n);
+    int hkey = -1;
+    Cur c;
+    for (bool more = start(c); more; more = advance(c), ++q) {
+      const int nr = min(rcB, b_hi(c.b) - c.n);
+      const int t1 = min(c.t0 + tpc, ts[c.b + 1]);
+      const int nt = t1 - c.t0;
       const int s = q % nstage;
       if (!failed && !mbar_wait(&rg.full[s], (uint32_t)((q / nstage) & 1))) {
-        flag_timeout(status);
+        flag_timeout(a.status);
         failed = true;
       }
-      if (t != ht) {  // task t's h slice into registers
-        const float* hp = hsm + (size_t)t * I + my_sl * 512;
+      const uint8_t* stg = ring + (size_t)s * a.stage_bytes;
+      float* rd = redB + (size_t)(q & 1) * redB_n;
+      const int items = nt * nslB * nr;
+      const int ipw = (items + kSW - 1) / kSW;
+      const int i0 = min(items, warp * ipw), i1 = min(items, i0 + ipw);
+      int r = i0 % nr, sl = (i0 / nr) % nslB, j = (i0 / nr) / nslB;
+      for (int it = i0; it < i1 && !failed;
+           ++it, (++r == nr ? (r = 0, (++sl == nslB ? (sl = 0, ++j) : 0)) : 0)) {
+        const int key = (c.t0 + j) * nslB + sl;
+        if (key != hkey) {  // task's h slice into registers
+          const float* hp = hsm + (size_t)(c.t0 + j) * I + sl * 512;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 v = FMT == MOE_W_NVFP4
-                               ? reinterpret_cast<const float4*>(hp + lane * 16)[j]
-                               : *reinterpret_cast<const float4*>(hp + lane * 8 + 256 * (j >> 1) + 4 * (j & 1));
-          hv[4 * j] = v.x;
-          hv[4 * j + 1] = v.y;
-          hv[4 * j + 2] = v.z;
-          hv[4 * j + 3] = v.w;
+          for (int m = 0; m < 4; ++m) {
+            const float4 v = FMT == MOE_W_NVFP4
+                                 ? reinterpret_cast<const float4*>(hp + lane * 16)[m]
+                                 : *reinterpret_cast<const float4*>(hp + lane * 8 + 256 * (m >> 1) + 4 * (m & 1));
+            hv[4 * m] = v.x;
+            hv[4 * m + 1] = v.y;
+            hv[4 * m + 2] = v.z;
+            hv[4 * m + 3] = v.w;
+          }
+          hkey = key;
         }
-        ht = t;
-      }
-      const uint8_t* stg = ring + (size_t)s * stage_bytes;
-      for (int r = my_g; r < nr && !failed; r += ngr) {
+        const uint8_t* tb = stg + (size_t)j * rcB * rowB;
         float p;
         if (FMT == MOE_W_NVFP4) {
-          const int e0 = my_sl * 512 + lane * 16;
-          const uint2 c = *reinterpret_cast<const uint2*>(stg + (size_t)r * (I / 2) + e0 / 2);
-          const float qd = dot8_fp4_f(c.x, hv) + dot8_fp4_f(c.y, hv + 8);
-          p = qd * e4m3x2_f32(stg[(size_t)rc * (I / 2) + (size_t)r * (I / 16) + e0 / 16]).x;
+          const int e0 = sl * 512 + lane * 16;
+          const uint2 cw2 = *reinterpret_cast<const uint2*>(tb + (size_t)r * (I / 2) + e0 / 2);
+          const float qd = dot8_fp4_f(cw2.x, hv) + dot8_fp4_f(cw2.y, hv + 8);
+          p = qd * e4m3x2_f32(tb[(size_t)rcB * (I / 2) + (size_t)r * (I / 16) + e0 / 16]).x;
         } else {
-          const uint8_t* row = stg + (size_t)r * I * 2 + (size_t)my_sl * 1024;
+          const uint8_t* row = tb + (size_t)r * I * 2 + (size_t)sl * 1024;
           p = dot8_bf16_f(*reinterpret_cast<const uint4*>(row + lane * 16), hv, 0.f);
           p = dot8_bf16_f(*reinterpret_cast<const uint4*>(row + lane * 16 + 512), hv + 8, p);
         }
         p = wsum(p);
-        if (lane == 0) red[r][my_sl] = p;
+        if (lane == 0) rd[it] = p;
       }
-      consumers_sync();
+      consumers_sync();  // stage no longer read; rd complete
       if (threadIdx.x == 0) mbar_arrive_one(&rg.empty[s]);
-      if (threadIdx.x < nr && !failed) {  // one thread per row: slices in a fixed order
-        const int r = threadIdx.x;
+      if (threadIdx.x < nt * nr && !failed) {  // one thread per (task, row): slices in order
+        const int jj = threadIdx.x / nr, rr = threadIdx.x % nr;
         float y = 0.f;
-        for (int sl = 0; sl < nsl; ++sl) y += red[r][sl];
-        ysm[(size_t)t * per + (b * H + n + r - ru0)] = y;
+        for (int z = 0; z < nslB; ++z) y += rd[(jj * nslB + z) * nr + rr];
+        ysm[(size_t)(c.t0 + jj) * perB + (c.b * H + c.n + rr - ru0)] = y;
       }
-      consumers_sync();
-      ++q;
-      more = next_chunk(&b, &t, &n, nr) && valid_chunk(&b, &t, &n);
     }
   }
+  consumers_sync();  // every per-task row result in ysm
   // combine: each output row, its tasks in route order (j ascending), then + ys
-  for (int ru = ru0 + threadIdx.x; ru < ru1; ru += kST) {
+  int m = 0;
+  for (int ru = ru0 + threadIdx.x; ru < ru1; ru += kST, ++m) {
     const int b = ru / H, n = ru - b * H;
     float acc = 0.f;
     for (int t = ts[b]; t < ts[b + 1]; ++t)
-      acc = fmaf(tk.wt[t] * tk.gs[t][2], ysm[(size_t)t * per + (ru - ru0)], acc);
+      acc = fmaf(tk.wt[t] * tk.gs[t][2], ysm[(size_t)t * perB + (ru - ru0)], acc);
     if (SHARED) {
-      ys[(size_t)b * H + n] = gate_s[b] * acc;
+      a.ys[(size_t)b * H + n] = gate_s[b] * acc;
     } else {
-      const float yy = ys ? acc + ys[(size_t)b * H + n] : acc;
-      out[(size_t)b * H + n] = __float2bfloat16_rn(yy);
+      const float yv = m < kYsPre ? ysv[m] : (a.ys ? a.ys[ru] : 0.f);
+      a.out[(size_t)b * H + n] = __float2bfloat16_rn(a.ys ? acc + yv : acc);
     }
   }
 }
 
 int g_num_sms = 0;
+constexpr size_t kBudget = 200 * 1024;
+constexpr int kStageCapA = 36 * 1024;
+constexpr int kStageCapB = 24 * 1024;
 
-// Shared-memory budgets: the gate/up kernel and its dependent down kernel are
-// sized to fit one SM together (228 KB), so the down kernel can load while
-// gate/up still runs.
-constexpr size_t kUpBudget = 150 * 1024;
-constexpr size_t kDownBudget = 72 * 1024;
-constexpr int kUpStageCap = 36 * 1024;
-constexpr int kDownStageCap = 16 * 1024;
+size_t round128(size_t v) { return (v + 127) / 128 * 128; }
 
-template <typename K, typename... Args>
-cudaError_t launch_ex(K kernel, int grid, size_t smem, cudaStream_t s, bool pdl, Args... args) {
+struct Plan {
+  size_t smem;
+  int nstage, stage_bytes, rcA, rcB, tpc;
+  bool ok;
+};
+
+Plan fused_plan(int wfmt, int H, int I, int n_rows, int T) {
+  Plan p{};
+  const int rowA = wfmt == MOE_W_NVFP4 ? 2 * (H / 2 + H / 16) : 2 * H * 2;
+  const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
+  p.rcA = rows_per_chunk(rowA, kStageCapA);
+  p.rcB = rows_per_chunk(rowB, kStageCapB);
+  p.tpc = kStageCapB / (p.rcB * rowB);
+  p.tpc = p.tpc < 1 ? 1 : (p.tpc > 16 ? 16 : p.tpc);
+  const size_t sA = (size_t)p.rcA * rowA, sB = (size_t)p.tpc * p.rcB * rowB;
+  p.stage_bytes = (int)round128(sA > sB ? sA : sB);
+  const int G = g_num_sms > 0 ? g_num_sms : 1;
+  const int perB = (n_rows * H + G - 1) / G;
+  const size_t fixed = round128((size_t)n_rows * H * 2) +
+                       round128(((size_t)T * I + (size_t)T * perB + 4 * (size_t)(H / 1024) * p.rcA +
+                                 2 * (size_t)p.tpc * (I / 512) * p.rcB) * 4);
+  p.nstage = fixed < kBudget ? (int)((kBudget - fixed) / p.stage_bytes) : 0;
+  p.nstage = p.nstage > kMaxStages ? kMaxStages : p.nstage;
+  p.smem = fixed + (size_t)p.nstage * p.stage_bytes;
+  p.ok = p.nstage >= 1 && H % 1024 == 0 && H / 1024 <= kSW && I % 512 == 0 && I / 512 <= kSW &&
+         n_rows * H <= kXW * 8 * kST && p.tpc * p.rcB <= kST && (size_t)p.rcA * rowA <= (size_t)kStageCapA &&
+         (size_t)p.rcB * rowB <= (size_t)kStageCapB;
+  return p;
+}
+
+template <typename K>
+cudaError_t launch_coop(K kernel, size_t smem, cudaStream_t s, const DevState& st,
+                        const FusedArgs& a) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(g_num_sms);
   cfg.blockDim = dim3(kST + 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, st, a);
 }
 
-struct Plan {
-  size_t smem;
-  int nstage, stage_bytes, rc;
-  bool ok;
-};
-
-Plan up_plan(int wfmt, int H, int n_rows) {
-  Plan p{};
-  const int row = wfmt == MOE_W_NVFP4 ? 2 * (H / 2 + H / 16) : 2 * H * 2;
-  p.rc = rows_per_chunk(row, kUpStageCap);
-  p.stage_bytes = (p.rc * row + 127) / 128 * 128;
-  const size_t fixed = ((size_t)n_rows * H * 2 + 127) / 128 * 128;
-  p.nstage = fixed < kUpBudget ? (int)((kUpBudget - fixed) / p.stage_bytes) : 0;
-  p.nstage = p.nstage > kMaxStages ? kMaxStages : p.nstage;
-  p.smem = fixed + (size_t)p.nstage * p.stage_bytes;
-  p.ok = p.rc * row <= kUpStageCap && p.nstage >= 2 && H % 1024 == 0 && H / 1024 <= kSW &&
-         n_rows * H <= kXW * 8 * kST;
-  return p;
-}
-
-Plan down_plan(int wfmt, int H, int I, int n_rows, int T) {
-  Plan p{};
-  const int row = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
-  p.rc = rows_per_chunk(row, kDownStageCap);
-  p.stage_bytes = (p.rc * row + 127) / 128 * 128;
-  const int per = (n_rows * H + g_num_sms - 1) / (g_num_sms > 0 ? g_num_sms : 1);
-  const size_t fixed = (((size_t)T * I + (size_t)T * per) * 4 + 127) / 128 * 128;
-  p.nstage = fixed < kDownBudget ? (int)((kDownBudget - fixed) / p.stage_bytes) : 0;
-  p.nstage = p.nstage > kMaxStages ? kMaxStages : p.nstage;
-  p.smem = fixed + (size_t)p.nstage * p.stage_bytes;
-  p.ok = p.rc * row <= kDownStageCap && p.nstage >= 2 && I % 512 == 0 && I / 512 <= kSW;
-  return p;
+cudaError_t launch_fused(const DevState& st, int wfmt, bool shared, const FusedArgs& a0,
+                         cudaStream_t s) {
+  FusedArgs a = a0;
+  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, a.R);
+  a.nstage = p.nstage;
+  a.stage_bytes = p.stage_bytes;
+  a.rcA = p.rcA;
+  a.rcB = p.rcB;
+  a.tpc = p.tpc;
+  if (wfmt == MOE_W_NVFP4)
+    return shared ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, true>, p.smem, s, st, a)
+                  : launch_coop(ffn_fused_kernel<MOE_W_NVFP4, false>, p.smem, s, st, a);
+  return shared ? launch_coop(ffn_fused_kernel<MOE_W_BF16, true>, p.smem, s, st, a)
+                : launch_coop(ffn_fused_kernel<MOE_W_BF16, false>, p.smem, s, st, a);
 }
 
 }  // namespace
@@ -822,88 +895,72 @@ Plan down_plan(int wfmt, int H, int I, int n_rows, int T) {
 bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks) {
   if (g_num_sms <= 0 || n_tasks > kMaxTasks || n_rows > 16 || n_rows < 1) return false;
   if (H % 256 || I % 256) return false;  // every bulk copy 16-byte aligned and sized
-  return up_plan(wfmt, H, n_rows).ok && down_plan(wfmt, H, I, n_rows, n_tasks).ok;
+  return fused_plan(wfmt, H, I, n_rows, n_tasks).ok;
 }
 
 cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int max_tasks) {
   int dev;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-  auto set = [&](auto kern, size_t bytes) {
+  auto set = [&](auto kern) {
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBudget);
   };
-  set(stream_up_kernel<MOE_W_BF16>, kUpBudget);
-  set(stream_up_kernel<MOE_W_NVFP4>, kUpBudget);
-  set(stream_down_kernel<MOE_W_BF16, true>, kDownBudget);
-  set(stream_down_kernel<MOE_W_NVFP4, true>, kDownBudget);
-  set(stream_down_kernel<MOE_W_BF16, false>, kDownBudget);
-  set(stream_down_kernel<MOE_W_NVFP4, false>, kDownBudget);
+  set(ffn_fused_kernel<MOE_W_BF16, true>);
+  set(ffn_fused_kernel<MOE_W_NVFP4, true>);
+  set(ffn_fused_kernel<MOE_W_BF16, false>);
+  set(ffn_fused_kernel<MOE_W_NVFP4, false>);
   (void)wfmt, (void)H, (void)I, (void)Is, (void)max_rows, (void)max_tasks;
   return e;
 }
 
-// Shared expert: h_s and the gate via the up kernel, then ys = gate * W_d h_s.
 cudaError_t launch_shared_stream(const DevState& st, int wfmt, int H, int Is, const void* x,
                                  int n_rows, const uint8_t* blob, const void* gate_w,
                                  FfnScratch sc, unsigned long long* status, cudaStream_t s) {
-  const uint16_t* xx = static_cast<const uint16_t*>(x);
-  const uint16_t* gw = static_cast<const uint16_t*>(gate_w);
-  const Plan pu = up_plan(wfmt, H, n_rows), pd = down_plan(wfmt, H, Is, n_rows, n_rows);
-  const int grid = g_num_sms;
-  const int32_t* none = nullptr;
-  cudaError_t e;
-  if (wfmt == MOE_W_NVFP4) {
-    e = launch_ex(stream_up_kernel<MOE_W_NVFP4>, grid, pu.smem, s, false, st, H, Is, 0, xx, 1,
-                  none, n_rows, blob, sc.hs, n_rows, pu.nstage, pu.stage_bytes, status, gw,
-                  sc.gate);
-    if (e == cudaSuccess)
-      e = launch_ex(stream_down_kernel<MOE_W_NVFP4, true>, grid, pd.smem, s, true, st, H, Is, 0, 1,
-                    none, n_rows, blob, (const float*)nullptr, (const float*)sc.hs,
-                    (const float*)sc.gate, sc.ys, (__nv_bfloat16*)nullptr, n_rows, pd.nstage,
-                    pd.stage_bytes, status);
-  } else {
-    e = launch_ex(stream_up_kernel<MOE_W_BF16>, grid, pu.smem, s, false, st, H, Is, 0, xx, 1,
-                  none, n_rows, blob, sc.hs, n_rows, pu.nstage, pu.stage_bytes, status, gw,
-                  sc.gate);
-    if (e == cudaSuccess)
-      e = launch_ex(stream_down_kernel<MOE_W_BF16, true>, grid, pd.smem, s, true, st, H, Is, 0, 1,
-                    none, n_rows, blob, (const float*)nullptr, (const float*)sc.hs,
-                    (const float*)sc.gate, sc.ys, (__nv_bfloat16*)nullptr, n_rows, pd.nstage,
-                    pd.stage_bytes, status);
-  }
-  return e;
+  FusedArgs a{};
+  a.H = H;
+  a.I = Is;
+  a.layer = 0;
+  a.k = 1;
+  a.R = n_rows;
+  a.n_rows = n_rows;
+  a.x = static_cast<const uint16_t*>(x);
+  a.slot_ids = nullptr;
+  a.fixed_blob = blob;
+  a.w = nullptr;
+  a.h = sc.hs;
+  a.gate_w = static_cast<const uint16_t*>(gate_w);
+  a.gate = sc.gate;
+  a.ys = sc.ys;
+  a.out = nullptr;
+  a.status = status;
+  a.bar_ctr = sc.bar;
+  return launch_fused(st, wfmt, true, a, s);
 }
 
 cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int layer,
                                  const void* x, const int32_t* slot_ids, const float* w,
                                  int n_rows, int k, const float* shared_y, void* out,
                                  FfnScratch sc, unsigned long long* status, cudaStream_t s) {
-  const uint16_t* xx = static_cast<const uint16_t*>(x);
-  const int R = n_rows * k;
-  const Plan pu = up_plan(wfmt, H, n_rows), pd = down_plan(wfmt, H, I, n_rows, R);
-  const int grid = g_num_sms;
-  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-  const uint8_t* nob = nullptr;
-  const uint16_t* nogw = nullptr;
-  float* nogate = nullptr;
-  cudaError_t e;
-  if (wfmt == MOE_W_NVFP4) {
-    e = launch_ex(stream_up_kernel<MOE_W_NVFP4>, grid, pu.smem, s, false, st, H, I, layer, xx, k,
-                  slot_ids, R, nob, sc.h, n_rows, pu.nstage, pu.stage_bytes, status, nogw, nogate);
-    if (e == cudaSuccess)
-      e = launch_ex(stream_down_kernel<MOE_W_NVFP4, false>, grid, pd.smem, s, true, st, H, I,
-                    layer, k, slot_ids, R, nob, w, (const float*)sc.h, (const float*)nullptr,
-                    const_cast<float*>(shared_y), o, n_rows, pd.nstage, pd.stage_bytes, status);
-  } else {
-    e = launch_ex(stream_up_kernel<MOE_W_BF16>, grid, pu.smem, s, false, st, H, I, layer, xx, k,
-                  slot_ids, R, nob, sc.h, n_rows, pu.nstage, pu.stage_bytes, status, nogw, nogate);
-    if (e == cudaSuccess)
-      e = launch_ex(stream_down_kernel<MOE_W_BF16, false>, grid, pd.smem, s, true, st, H, I,
-                    layer, k, slot_ids, R, nob, w, (const float*)sc.h, (const float*)nullptr,
-                    const_cast<float*>(shared_y), o, n_rows, pd.nstage, pd.stage_bytes, status);
-  }
-  return e;
+  FusedArgs a{};
+  a.H = H;
+  a.I = I;
+  a.layer = layer;
+  a.k = k;
+  a.R = n_rows * k;
+  a.n_rows = n_rows;
+  a.x = static_cast<const uint16_t*>(x);
+  a.slot_ids = slot_ids;
+  a.fixed_blob = nullptr;
+  a.w = w;
+  a.h = sc.h;
+  a.gate_w = nullptr;
+  a.gate = nullptr;
+  a.ys = const_cast<float*>(shared_y);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = status;
+  a.bar_ctr = sc.bar;
+  return launch_fused(st, wfmt, false, a, s);
 }
 
 }  // namespace moe

@@ -14,7 +14,7 @@
 namespace moe {
 namespace {
 
-constexpr int kGatherThreads = 512;
+constexpr int kGatherThreads = 256;
 constexpr size_t kChunk = 64 * 1024;
 constexpr int kUnroll = 4;
 

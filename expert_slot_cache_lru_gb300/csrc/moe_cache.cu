@@ -35,7 +35,7 @@ struct moe_cache {
   size_t mem_bytes = 0;
   cudaEvent_t ev_ready = nullptr, ev_done = nullptr;
   int fail_gathers = 0;
-  int gather_grid = 38;
+  int gather_grid = 76;
   int down_k_max = 0;        // largest k the down kernel's shared memory was sized for
   int last_pf_layer = 0;     // target layer of the last prefetch enqueued (selects its plan)
   bool stream_ffn = true;    // decode-sized steps use the streaming FFN kernels
@@ -135,7 +135,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->d = d;
   if (d.slot_bytes > 0 && !d.slot_stride) c->d.slot_stride = align_up(d.slot_bytes, 256);
   c->P = d.pool_mode == MOE_POOL_PER_LAYER ? d.n_layers : 1;
-  c->gather_grid = d.gather_ctas ? d.gather_ctas : 38;
+  c->gather_grid = d.gather_ctas ? d.gather_ctas : 76;
   auto fail = [&](int r) {
     moe_cache_destroy(c);
     return r;
@@ -163,7 +163,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_hs = cv.take<float>((size_t)d.max_rows * std::max(Is, 1)),
                o_gate = cv.take<float>(d.max_rows),
                o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1)),
-               o_status = cv.take<unsigned long long>(1);
+               o_status = cv.take<unsigned long long>(1),
+               o_bar = cv.take<unsigned long long>(1);
   c->mem_bytes = align_up(cv.off, 256);
   e = cudaMalloc(&c->mem, c->mem_bytes);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMalloc(state)"));
@@ -202,6 +203,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.hs = reinterpret_cast<float*>(m + o_hs);
   c->sc.gate = reinterpret_cast<float*>(m + o_gate);
   c->sc.ys = reinterpret_cast<float*>(m + o_ys);
+  c->sc.bar = reinterpret_cast<unsigned long long*>(m + o_bar);
 
   // initial state: nothing resident, every clock at 1
   e = cudaMemset(c->mem, 0, c->mem_bytes);

@@ -149,7 +149,7 @@ typedef struct {
   int max_routes;                  /* routes per admission, 1 .. 16384 */
   int max_rows;                    /* rows per layer call, 1 .. max_routes */
   int max_pred;                    /* predictions per prefetch, 0 .. 4096 (0 = no prefetch) */
-  int gather_ctas;                 /* CTAs of the gather kernel, 0 = default (38) */
+  int gather_ctas;                 /* CTAs of the gather kernel, 0 = default (76) */
 } moe_cache_desc;
 
 /* Per-layer counters, device-resident, read with moe_read_stats.
