@@ -30,6 +30,8 @@ MOE_ERR_CAPACITY = -4
 MOE_ERR_UNSUPPORTED = -5
 MOE_ERR_STATE = -6
 MOE_ERR_INJECTED = -7
+MOE_ERR_SCRATCH = -8
+MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 MOE_W_BF16 = 0
 MOE_W_NVFP4 = 1
 MOE_POOL_SHARED = 0
@@ -82,6 +84,8 @@ _SIGS = {
     "moe_gather_missing": [_vp, _i, _vp],
     "moe_rollback_plan": [_vp, _i, _vp],
     "moe_routed_experts": [_vp, _i, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp],
+    "moe_routed_experts_noalloc": [_i, _i, _i, _vp, C.c_size_t, _i, _vp, _vp, _vp, _i, _i, _vp,
+                                   _vp, _vp],
     "moe_decode_layer": [_vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp,
                          _vp, _u],
     "moe_read_stats": [_vp, _i, C.POINTER(moe_stats)],
@@ -185,6 +189,16 @@ def moe_routed_experts(cache: int, layer: int, d_x, d_slot_ids, d_w, n_rows: int
     _check("moe_routed_experts", _lib.moe_routed_experts(
         cache, layer, _ptr(d_x), _ptr(d_slot_ids), _ptr(d_w), n_rows, k, _ptr(d_shared_blob),
         _ptr(d_shared_gate), _ptr(d_out), _stream(stream)))
+
+
+def moe_routed_experts_noalloc(wfmt: int, hidden: int, inter: int, d_slots, slot_stride: int,
+                               n_slots: int, d_x, d_slot_ids, d_w, n_rows: int, k: int, d_out,
+                               d_status=None, stream=None) -> None:
+    """Routed FFNs + combine over a caller-owned slot pool; allocates nothing
+    (scratch is a fixed 1 MiB device array, see include/moe_cache.h)."""
+    _check("moe_routed_experts_noalloc", _lib.moe_routed_experts_noalloc(
+        wfmt, hidden, inter, _ptr(d_slots), slot_stride, n_slots, _ptr(d_x), _ptr(d_slot_ids),
+        _ptr(d_w), n_rows, k, _ptr(d_out), _ptr(d_status), _stream(stream)))
 
 
 def moe_decode_layer(cache: int, layer: int, d_x, d_ids, d_w, d_slot_ids, n_rows: int, k: int,

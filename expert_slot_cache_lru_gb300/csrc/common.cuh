@@ -172,4 +172,12 @@ cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int
                                  int n_rows, int k, const float* shared_y, void* out,
                                  FfnScratch sc, unsigned long long* status, cudaStream_t s);
 
+// Allocation-free routed FFN (ffn_stream.cu): the scratch is a file-scope
+// device array whose address noalloc_scratch looks up once per device.
+cudaError_t noalloc_scratch(void** out);
+cudaError_t launch_routed_noalloc(int wfmt, int H, int I, const uint8_t* slots, size_t stride,
+                                  int n_slots, const void* x, const int32_t* slot_ids,
+                                  const float* w, int n_rows, int k, void* out,
+                                  unsigned long long* status, void* scratch, cudaStream_t s);
+
 }  // namespace moe

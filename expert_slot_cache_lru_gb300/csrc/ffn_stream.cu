@@ -23,6 +23,8 @@
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -961,6 +963,54 @@ cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int
   a.status = status;
   a.bar_ctr = sc.bar;
   return launch_fused(st, wfmt, false, a, s);
+}
+
+// ---------------------------------------------------------------- allocation-free variant
+// moe_routed_experts_noalloc runs ffn_fused_kernel with its scratch in this
+// file-scope array instead of memory a cache allocated: bytes [0, 256) hold
+// the grid-barrier counter, bytes [256, end) the fp32 intermediate h.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t noalloc_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {  // once per device, with that device current
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e == cudaSuccess) e = ffn_stream_init(0, 0, 0, 0, 0, 0);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+cudaError_t launch_routed_noalloc(int wfmt, int H, int I, const uint8_t* slots, size_t stride,
+                                  int n_slots, const void* x, const int32_t* slot_ids,
+                                  const float* w, int n_rows, int k, void* out,
+                                  unsigned long long* status, void* scratch, cudaStream_t s) {
+  DevState st{};  // just enough state to resolve a slot id to its blob
+  st.L = 1;
+  st.P = 1;
+  st.S = n_slots;
+  st.per_layer = 0;
+  st.slots = const_cast<uint8_t*>(slots);
+  st.stride = stride;
+  FfnScratch sc{};
+  sc.bar = static_cast<unsigned long long*>(scratch);
+  sc.h = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + 256);
+  // the barrier waits for the counter's next multiple of the grid size; a launch
+  // that gave up after a timeout can leave it elsewhere, so start from zero
+  cudaError_t e = cudaMemsetAsync(sc.bar, 0, sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return e;
+  return launch_routed_stream(st, wfmt, H, I, 0, x, slot_ids, w, n_rows, k, nullptr, out, sc,
+                              status, s);
 }
 
 }  // namespace moe

@@ -98,6 +98,8 @@ const char* moe_strerror(int err) {
     case MOE_ERR_UNSUPPORTED: return "unsupported shape or format";
     case MOE_ERR_STATE: return "call not valid in the cache's state";
     case MOE_ERR_INJECTED: return "injected failure";
+    case MOE_ERR_SCRATCH:
+      return "request larger than the 1 MiB scratch of moe_routed_experts_noalloc";
     default: return "unknown error";
   }
 }
@@ -403,6 +405,31 @@ int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const int32_t* 
     return rc;
   return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out,
                     as_stream(stream));
+}
+
+int moe_routed_experts_noalloc(int wfmt, int hidden, int inter, const void* d_slots,
+                               size_t slot_stride, int n_slots, const void* d_x,
+                               const int32_t* d_slot_ids, const float* d_w, int n_rows, int k,
+                               void* d_out, unsigned long long* d_status, void* stream) {
+  if ((wfmt != MOE_W_BF16 && wfmt != MOE_W_NVFP4) || hidden <= 0 || inter <= 0 || hidden % 32 ||
+      inter % 32 || n_slots <= 0 || n_rows < 0 || k < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!d_slots || (reinterpret_cast<uintptr_t>(d_slots) & 255) || slot_stride % 256 ||
+      slot_stride < blob_bytes(wfmt, hidden, inter))
+    return MOE_ERR_INVALID_ARG;
+  if (n_rows == 0) return MOE_OK;
+  if (!d_x || !d_out || d_out == d_x || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
+      (k > 0 && (!d_slot_ids || !d_w)))
+    return MOE_ERR_INVALID_ARG;
+  if (256 + (size_t)n_rows * (size_t)k * (size_t)inter * sizeof(float) > MOE_NOALLOC_SCRATCH_BYTES)
+    return MOE_ERR_SCRATCH;
+  void* scratch = nullptr;
+  CK(moe::noalloc_scratch(&scratch));
+  if (!moe::ffn_stream_supported(wfmt, hidden, inter, n_rows, n_rows * k)) return MOE_ERR_UNSUPPORTED;
+  CK(moe::launch_routed_noalloc(wfmt, hidden, inter, static_cast<const uint8_t*>(d_slots),
+                                slot_stride, n_slots, d_x, d_slot_ids, d_w, n_rows, k, d_out,
+                                d_status, scratch, as_stream(stream)));
+  return MOE_OK;
 }
 
 int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,

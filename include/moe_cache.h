@@ -116,7 +116,8 @@ enum moe_err {
   MOE_ERR_CAPACITY = -4,      /* more routes / rows / predictions than the cache was sized for */
   MOE_ERR_UNSUPPORTED = -5,   /* shape or format this build does not handle */
   MOE_ERR_STATE = -6,         /* call not valid in the cache's current state */
-  MOE_ERR_INJECTED = -7       /* a test-requested failure (moe_cache_fail_next_gather) */
+  MOE_ERR_INJECTED = -7,      /* a test-requested failure (moe_cache_fail_next_gather) */
+  MOE_ERR_SCRATCH = -8        /* request larger than MOE_NOALLOC_SCRATCH_BYTES allows */
 };
 
 typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
@@ -290,6 +291,54 @@ MOE_API int moe_device_views(moe_cache* c, moe_views* out);
  * before it enqueues anything (the plan's bookings stay; the caller is
  * expected to call moe_rollback_plan).  n = 0 clears the request. */
 MOE_API int moe_cache_fail_next_gather(moe_cache* c, int n);
+
+/* ---------------------------------------------------------------- no allocation
+ * The pages have no counterpart of this call.  It runs the routed expert FFNs
+ * and the weighted combine of moe_routed_experts (without the shared expert)
+ * over a slot pool the caller owns, and it allocates nothing: no cache handle,
+ * no cudaMalloc / cudaFree, no allocator of any library (torch's included).
+ *
+ * Who needs it: a caller that cannot allocate device memory where it runs the
+ * experts.  Examples are a serving engine that reserved its whole memory
+ * budget (slot pool, KV cache) at start-up and must not allocate during
+ * decode, and code that keeps experts resident by itself and so has no
+ * moe_cache whose scratch it could borrow.  Creating a cache allocates state
+ * and scratch, and a cudaFree synchronises the device, so neither fits there.
+ *
+ * Scratch: a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES (1 MiB).
+ * Bytes [0, 256) hold the kernel's grid-barrier counter and bytes [256, 1 MiB)
+ * hold the fp32 intermediate h [n_rows*k][inter].  A request needs
+ * 256 + 4*n_rows*k*inter bytes; a larger one returns MOE_ERR_SCRATCH before
+ * anything is enqueued.  Each call clears the counter with a cudaMemsetAsync
+ * on `stream` before the kernel; h needs no clearing (every element read is
+ * written first in the same launch).
+ *
+ * Set-up: the first call on each device (that device current) looks up the
+ * array's address with cudaGetSymbolAddress and sets the kernel's shared
+ * memory limit; a failure returns MOE_ERR_CUDA.  If the first call is the
+ * one doing this set-up, make it before any stream capture.
+ *
+ * Races: there is one scratch array per device, so calls whose executions
+ * overlap on a device (different streams, or threads without ordering) race
+ * on it.  Order them on one stream or with events.
+ *
+ * Arguments: wfmt / hidden / inter as in moe_cache_desc; d_slots the pool
+ * base (256-byte aligned), slot s at d_slots + s*slot_stride (multiple of 256,
+ * at least the blob size), n_slots > 0; d_x bf16 [n_rows][hidden], 16-byte
+ * aligned; d_slot_ids int32 [n_rows][k] (outside [0, n_slots) = skip);
+ * d_w float32 [n_rows][k]; d_out bf16 [n_rows][hidden] (not aliasing d_x):
+ *   out[b] = bf16( sum_j w[b,j] * FFN_slot[b,j](x[b]) ).
+ * d_status: device word that receives MOE_STATUS_TIMEOUT if a bounded wait in
+ * the kernel gives up (NULL = not reported).  Only shapes the streaming
+ * kernel handles are accepted (among its conditions: hidden % 1024 == 0,
+ * inter % 512 == 0, n_rows <= 16, n_rows*k <= 64); others return
+ * MOE_ERR_UNSUPPORTED.  Enqueues work only. */
+#define MOE_NOALLOC_SCRATCH_BYTES (1u << 20)
+MOE_API int moe_routed_experts_noalloc(int wfmt, int hidden, int inter, const void* d_slots,
+                                       size_t slot_stride, int n_slots, const void* d_x,
+                                       const int32_t* d_slot_ids, const float* d_w, int n_rows,
+                                       int k, void* d_out, unsigned long long* d_status,
+                                       void* stream);
 
 /* Text of an error code; last CUDA error text seen by this thread. */
 MOE_API const char* moe_strerror(int err);
