@@ -125,7 +125,7 @@ class Decode:
     """The benchmark workload on one GPU: cache, inputs, one-token graph."""
 
     def __init__(self, dev: int, overlap: bool = True, warm_tokens: int = WARM_TOKENS,
-                 total_tokens: int = 512):
+                 total_tokens: int = 512, n_layers: int | None = None, n_slots: int | None = None):
         import torch
 
         import expert_slot_cache_lru_gb300 as m
@@ -133,6 +133,8 @@ class Decode:
         self.torch, self.m, self.synth = torch, m, synth
         torch.cuda.set_device(dev)
         w = synth.workloads()[WORKLOAD]
+        if n_layers or n_slots:  # a smaller case of the same layer, for profiler captures
+            w = synth.scaled(w, n_layers=n_layers or w.n_layers, n_slots=n_slots or w.n_slots)
         self.w = w
         self.overlap = overlap
         t0 = time.time()
@@ -274,7 +276,8 @@ class Decode:
         launches = reps * steps * L
         per_launch_s = ms * 1e-3 / launches
         per_launch_bytes = nbytes / (steps * L)
-        return {"kernel": "routed expert GEMV (moe_routed_experts: stream_up_kernel + stream_down_kernel)",
+        return {"kernel": "ffn_fused_kernel<NVFP4, routed> (moe_routed_experts: gate/up, "
+                          "grid barrier, down + combine in one cooperative launch)",
                 "launches": launches, "avg_launch_us": per_launch_s * 1e6,
                 "bytes_per_launch": per_launch_bytes,
                 "achieved_gbs": per_launch_bytes / per_launch_s / 1e9}
@@ -446,7 +449,9 @@ def run_native(args) -> None:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
                                 device_id=torch.device("cuda", local))
     peaks = measured_peaks()
-    dec = Decode(local, overlap=not args.serial)
+    dec = Decode(local, overlap=not args.serial, warm_tokens=args.warm_tokens,
+                 n_layers=args.layers, n_slots=args.slots)
+    L = dec.w.n_layers
     props = torch.cuda.get_device_properties(local)
     for _ in range(args.warmup):
         dec.step()
@@ -477,6 +482,12 @@ def run_native(args) -> None:
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     tok_s = ws * args.steps / (ms * 1e-3)
+    if args.decode_only:  # profiler runs: the timed decode only, no sub-measurements
+        if rank == 0:
+            print(json.dumps({"decode_only": True, "layers": L, "slots": dec.w.n_slots,
+                              "tok_s": round(tok_s, 2), "ms_per_step": round(ms / args.steps, 4)}),
+                  flush=True)
+        return
 
     # end to end through the public API: pinned host inputs in, output back, per token
     barrier()
@@ -515,8 +526,9 @@ def run_native(args) -> None:
                    "global_batch": ws, "graph": "one CUDA graph per token (40 layers)",
                    "overlap": not args.serial, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2: each token streams ~637 MB of expert weights",
-                   "cache_warmup_tokens": WARM_TOKENS},
-        "gpu_launches": args.steps * (6 * 40),
+                   "cache_warmup_tokens": args.warm_tokens},
+        # per layer: admission, demand gather, shared-expert FFN, routed FFN + combine
+        "gpu_launches": args.steps * 4 * L,
         "e2e": e2e,
         "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1),
                      "peak": hbm, "unit": "GB/s",
@@ -597,6 +609,12 @@ def main():
     ap.add_argument("--serial", action="store_true", help="gather on the compute stream (ncu mode)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--warm-tokens", type=int, default=WARM_TOKENS,
+                    help="eager tokens that warm the cache before the graph is captured")
+    ap.add_argument("--layers", type=int, default=None, help="profiler case: fewer layers")
+    ap.add_argument("--slots", type=int, default=None, help="profiler case: fewer slots")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time the decode only and print a short line (profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
