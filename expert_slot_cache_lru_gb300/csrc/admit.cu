@@ -27,29 +27,130 @@
 namespace moe {
 namespace {
 
+constexpr int kLoSmem = 512;  // victims ordered in shared memory up to this many
+constexpr int kTopMax = 16;   // warp-minimum selection up to this many victims
+constexpr int kTopSpt = 8;    // ... over at most this many slots per thread
+
 struct SelSmem {
   int bins[kAdmitThreads];
   int digit;
   int krem;
+  int nvict;
+  uint32_t wk[kAdmitThreads / 32][kTopMax];
+  unsigned long long lo_t[kLoSmem];
+  int lo_s[kLoSmem];
+  int vict[kLoSmem];
 };
 
+// The victim key of slot s: its stamp when the slot may be evicted, ~0 when it
+// is pinned or was touched by this admission (stamp >= clk).  A real stamp is
+// a clock value and never ~0.  CACHED reads a copy of the pool held in shared
+// memory (filled at kernel entry and patched on hits); otherwise the key is
+// derived from the global stamp and pin arrays.
+template <bool CACHED>
+struct PoolKeys {
+  const unsigned long long* sm;  // CACHED: [S]
+  const DevState* st;
+  size_t base;
+  unsigned long long clk;
+  __device__ __forceinline__ unsigned long long operator()(int s) const {
+    if (CACHED) return sm[s];
+    const unsigned long long t = st->stamp[base + s];
+    return (st->pinned[base + s] || t >= clk) ? ~0ull : t;
+  }
+};
+
+// The `want` (<= kTopMax) smallest (stamp, slot) pairs among the evictable
+// slots when the evictable stamps span fewer than 2^16 clock values: keys are
+// 32-bit, (stamp - oldest) << 16 | slot, unique and ordered like (stamp,
+// slot).  Each thread sorts its (at most kTopSpt) keys; each warp takes its
+// `want` smallest by repeated warp minimum (redux.sync) and popping the
+// winner; warp 0 does the same over the warps' lists.  Returns -1 (in every
+// thread) when the stamps span too much for 32-bit keys.
+template <bool CACHED>
+__device__ int select_victims_small(const DevState& st, const PoolKeys<CACHED>& key, int want,
+                                    int* vict, SelSmem& sm, BlockScratch& bs) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int S = st.S;
+  const int spt = (S + kAdmitThreads - 1) / kAdmitThreads;
+  const int s0 = min(S, tid * spt), s1 = min(S, s0 + spt);
+  unsigned long long mn = ~0ull, mx = 0;
+  for (int s = s0; s < s1; ++s) {
+    const unsigned long long t = key(s);
+    if (t == ~0ull) continue;
+    mn = t < mn ? t : mn;
+    mx = t > mx ? t : mx;
+  }
+  unsigned long long smin, smax;
+  block_minmax_u64(mn, mx, bs, &smin, &smax);
+  if (smin == ~0ull) return 0;               // nothing evictable
+  if (smax - smin >= 0xffffull) return -1;   // too wide for 32-bit keys
+  uint32_t k[kTopSpt];
+#pragma unroll
+  for (int j = 0; j < kTopSpt; ++j) k[j] = 0xffffffffu;
+  for (int s = s0; s < s1; ++s) {  // insertion into the sorted k
+    const unsigned long long t = key(s);
+    if (t == ~0ull) continue;
+    uint32_t v = ((uint32_t)(t - smin) << 16) | (uint32_t)s;
+#pragma unroll
+    for (int j = 0; j < kTopSpt; ++j)
+      if (v < k[j]) {
+        const uint32_t x = k[j];
+        k[j] = v;
+        v = x;
+      }
+  }
+  for (int i = 0; i < want; ++i) {  // this warp's `want` smallest
+    const uint32_t m = __reduce_min_sync(0xffffffffu, k[0]);
+    if (k[0] == m && m != 0xffffffffu) {  // keys are unique: one lane pops its head
+#pragma unroll
+      for (int j = 0; j < kTopSpt - 1; ++j) k[j] = k[j + 1];
+      k[kTopSpt - 1] = 0xffffffffu;
+    }
+    if (lane == 0) sm.wk[w][i] = m;
+  }
+  __syncthreads();
+  if (w == 0) {
+    int h = 0, n = 0;
+    uint32_t cur = sm.wk[lane][0];
+    for (int i = 0; i < want; ++i) {
+      const uint32_t m = __reduce_min_sync(0xffffffffu, cur);
+      if (m == 0xffffffffu) break;  // fewer evictable slots than wanted (uniform)
+      if (cur == m) {
+        ++h;
+        cur = h < want ? sm.wk[lane][h] : 0xffffffffu;
+      }
+      if (lane == 0) vict[i] = (int)(m & 0xffffu);
+      n = i + 1;
+    }
+    if (lane == 0) sm.nvict = n;
+  }
+  __syncthreads();
+  return sm.nvict;
+}
+
 // Chooses up to `want` victims in pool p and writes them, ascending
-// (stamp, slot), to st.vict[0..n).  Returns n (the same in every thread).
-__device__ int select_victims(const DevState& st, int p, unsigned long long clk, int want,
-                              SelSmem& sm, BlockScratch& bs) {
+// (stamp, slot), to vict[0..n) (shared memory when want <= kLoSmem, else the
+// global scratch).  Returns n (the same in every thread).
+template <bool CACHED>
+__device__ int select_victims(const DevState& st, const PoolKeys<CACHED>& key, int want,
+                              int* vict, SelSmem& sm, BlockScratch& bs) {
   if (want <= 0) return 0;
   const int tid = threadIdx.x;
   const int S = st.S;
-  const size_t base = (size_t)p * S;
   const int spt = (S + kAdmitThreads - 1) / kAdmitThreads;
+  if (want <= kTopMax && spt <= kTopSpt && S <= 65536) {
+    const int n = select_victims_small<CACHED>(st, key, want, vict, sm, bs);
+    if (n >= 0) return n;
+  }
   const int s0 = min(S, tid * spt), s1 = min(S, s0 + spt);
 
   // pass 0: how many slots may be evicted, and their stamp range
   int ne = 0;
   unsigned long long mn = ~0ull, mx = 0;
   for (int s = s0; s < s1; ++s) {
-    const unsigned long long t = st.stamp[base + s];
-    if (!st.pinned[base + s] && t < clk) {
+    const unsigned long long t = key(s);
+    if (t != ~0ull) {
       ++ne;
       mn = t < mn ? t : mn;
       mx = t > mx ? t : mx;
@@ -71,8 +172,8 @@ __device__ int select_victims(const DevState& st, int p, unsigned long long clk,
       sm.bins[tid] = 0;
       __syncthreads();
       for (int s = s0; s < s1; ++s) {
-        const unsigned long long t = st.stamp[base + s];
-        if (st.pinned[base + s] || t >= clk) continue;
+        const unsigned long long t = key(s);
+        if (t == ~0ull) continue;
         const unsigned long long rel = t - smin;
         const bool match = (shift + 10 >= 64) || ((rel >> (shift + 10)) == (prefix >> (shift + 10)));
         if (match) atomicAdd(&sm.bins[(rel >> shift) & 1023], 1);
@@ -96,12 +197,15 @@ __device__ int select_victims(const DevState& st, int p, unsigned long long clk,
   k = k < 1 ? 1 : (k > n ? n : k);
   const unsigned long long T = smin + prefix;
   const int below = n - k;  // every evictable slot with stamp < T is a victim
+  unsigned long long* lo_t =
+      below <= kLoSmem ? sm.lo_t : reinterpret_cast<unsigned long long*>(st.lo_stamp);
+  int* lo_s = below <= kLoSmem ? sm.lo_s : st.lo_slot;
 
   // the k lowest-index evictable slots with stamp == T, in slot order
   int eq = 0, lt = 0;
   for (int s = s0; s < s1; ++s) {
-    const unsigned long long t = st.stamp[base + s];
-    if (st.pinned[base + s] || t >= clk) continue;
+    const unsigned long long t = key(s);
+    if (t == ~0ull) continue;
     eq += (t == T);
     lt += (t < T);
   }
@@ -109,15 +213,15 @@ __device__ int select_victims(const DevState& st, int p, unsigned long long clk,
   int r = block_excl_scan(eq, bs, &tot);
   int q = below > 0 ? block_excl_scan(lt, bs, &tot) : 0;
   for (int s = s0; s < s1; ++s) {
-    const unsigned long long t = st.stamp[base + s];
-    if (st.pinned[base + s] || t >= clk) continue;
+    const unsigned long long t = key(s);
+    if (t == ~0ull) continue;
     if (t == T) {
-      if (r < k) st.vict[below + r] = s;
+      if (r < k) vict[below + r] = s;
       ++r;
     } else if (t < T) {
       if (q < below) {
-        st.lo_stamp[q] = t;
-        st.lo_slot[q] = s;
+        lo_t[q] = t;
+        lo_s[q] = s;
       }
       ++q;
     }
@@ -125,42 +229,86 @@ __device__ int select_victims(const DevState& st, int p, unsigned long long clk,
   __syncthreads();
   // order the (few) older victims by (stamp, slot)
   for (int i = tid; i < below; i += kAdmitThreads) {
-    const unsigned long long ti = st.lo_stamp[i];
-    const int si = st.lo_slot[i];
+    const unsigned long long ti = lo_t[i];
+    const int si = lo_s[i];
     int rank = 0;
     for (int j = 0; j < below; ++j) {
-      const unsigned long long tj = st.lo_stamp[j];
-      rank += (tj < ti) || (tj == ti && st.lo_slot[j] < si);
+      const unsigned long long tj = lo_t[j];
+      rank += (tj < ti) || (tj == ti && lo_s[j] < si);
     }
-    st.vict[rank] = si;
+    vict[rank] = si;
   }
   __syncthreads();
   return n;
 }
 
+// Admission.  CACHED keeps the pool's victim keys and slot keys in shared
+// memory for the whole call: they are loaded at entry together with the ids
+// and the clock, so the victim search and the install read no global memory.
+template <bool CACHED>
 __global__ void __launch_bounds__(kAdmitThreads, 1)
 admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, int cap) {
-  extern __shared__ int smem_i[];
-  const int E = st.E;
-  int* cnt = smem_i;      // [E] routes per expert
-  int* aux = smem_i + E;  // [E] miss rank, -1 otherwise
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int E = st.E, S = st.S;
+  unsigned long long* pkey = reinterpret_cast<unsigned long long*>(smem_raw);  // [S] CACHED
+  int* pslot = reinterpret_cast<int*>(smem_raw + (CACHED ? (size_t)S * 8 : 0));  // [S] CACHED
+  int* cnt = pslot + (CACHED ? S : 0);  // [E] routes per expert
+  int* aux = cnt + E;                    // [E] miss rank, -1 otherwise
+  int* slot_of = aux + E;                // [E] slot of each requested expert after the call
   __shared__ BlockScratch bs;
   __shared__ SelSmem sel;
-  __shared__ unsigned long long s_clk;
   __shared__ int s_acc[6];  // invalid, distinct, hits, evictions, overflow routes
+  __shared__ unsigned long long s_st[sizeof(moe_stats) / 8];  // the layer's counters
   const int tid = threadIdx.x;
   const int p = pool_of(st, layer);
-  const size_t pbase = (size_t)p * st.S;
+  const size_t pbase = (size_t)p * S;
+  const int ept = (E + kAdmitThreads - 1) / kAdmitThreads;
+  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
 
-  if (tid == 0) s_clk = st.clock[p] + 1;  // one recency stamp per admission
+  // independent loads first: the first ids, the clock, the layer's counters,
+  // this thread's expert state (one expert per thread when E <= 1024), the pool
+  uint32_t pf_df = 0, pf_dm = 0;
+  int pf_map = -1;
+  if (ept == 1 && e0 < e1) {
+    const int key = layer * E + e0;
+    pf_df = st.decode_freq[key];
+    pf_dm = st.demand_freq[key];
+    pf_map = st.map[key];
+  }
+  if (tid < (int)(sizeof(moe_stats) / 8))
+    s_st[tid] = reinterpret_cast<const unsigned long long*>(&st.stats[layer])[tid];
+  int idv[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int r = tid + j * kAdmitThreads;
+    idv[j] = r < R ? ids[r] : 0;
+  }
+  const unsigned long long clk = st.clock[p] + 1;  // one recency stamp per admission
+  if (CACHED) {
+#pragma unroll 4
+    for (int s = tid; s < S; s += kAdmitThreads) {
+      const unsigned long long t = st.stamp[pbase + s];
+      const uint8_t pin = st.pinned[pbase + s];
+      const int sk = st.slot_key[pbase + s];
+      pkey[s] = pin ? ~0ull : t;  // every stored stamp is below clk
+      pslot[s] = sk;
+    }
+  }
   if (tid < 6) s_acc[tid] = 0;
   for (int e = tid; e < E; e += kAdmitThreads) cnt[e] = 0;
   __syncthreads();
-  const unsigned long long clk = s_clk;
 
   // histogram of the valid ids; ids outside [0, E) are counted and dropped
   int inv = 0;
-  for (int r = tid; r < R; r += kAdmitThreads) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int r = tid + j * kAdmitThreads;
+    if (r >= R) continue;
+    const int e = idv[j];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    else ++inv;
+  }
+  for (int r = tid + 2 * kAdmitThreads; r < R; r += kAdmitThreads) {
     const int e = ids[r];
     if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
     else ++inv;
@@ -168,22 +316,24 @@ admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, in
   __syncthreads();
 
   // distinct experts (contiguous chunk per thread): counters, lookup, hits
-  const int ept = (E + kAdmitThreads - 1) / kAdmitThreads;
-  const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
   int nd = 0, nh = 0, nm = 0;
   for (int e = e0; e < e1; ++e) {
     const int c = cnt[e];
     aux[e] = -1;
+    slot_of[e] = -1;
     if (c == 0) continue;
     ++nd;
     const int key = layer * E + e;
-    st.decode_freq[key] += (uint32_t)c;
-    const uint32_t df = st.demand_freq[key];
+    const bool pre = ept == 1;  // state loaded at entry
+    st.decode_freq[key] = (pre ? pf_df : st.decode_freq[key]) + (uint32_t)c;
+    const uint32_t df = pre ? pf_dm : st.demand_freq[key];
     if (df != 0xffffffffu) st.demand_freq[key] = df + 1;
     st.last_demand[key] = clk;
-    const int s = st.map[key];
+    const int s = pre ? pf_map : st.map[key];
     if (s >= 0) {
       st.stamp[pbase + s] = clk;  // hit: refresh recency; protected from this admission
+      if (CACHED) pkey[s] = ~0ull;
+      slot_of[e] = s;
       ++nh;
     } else {
       aux[e] = 1;
@@ -195,7 +345,9 @@ admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, in
   for (int e = e0; e < e1; ++e)
     if (aux[e] >= 0) aux[e] = rank++;
   int nA = (cap >= 0 && cap < nM) ? cap : nM;  // the fetch cap admits the lowest ids
-  const int nV = select_victims(st, p, clk, nA, sel, bs);
+  int* vict = nA <= kLoSmem ? sel.vict : st.vict;
+  const PoolKeys<CACHED> keys{pkey, &st, pbase, clk};
+  const int nV = select_victims<CACHED>(st, keys, nA, vict, sel, bs);
   const bool short_of_slots = nV < nA;
   nA = nV;
 
@@ -204,9 +356,9 @@ admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, in
   for (int e = e0; e < e1; ++e) {
     const int i = aux[e];
     if (i < 0 || i >= nA) continue;
-    const int s = st.vict[i];
+    const int s = vict[i];
     const size_t g = pbase + s;
-    const int old = st.slot_key[g];
+    const int old = CACHED ? pslot[s] : st.slot_key[g];
     if (old >= 0) {
       st.map[old] = -1;
       ++nev;
@@ -215,6 +367,7 @@ admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, in
     st.slot_key[g] = key;
     st.map[key] = s;
     st.stamp[g] = clk;
+    slot_of[e] = s;
     st.plan_demand[1 + 3 * i + 0] = s;
     st.plan_demand[1 + 3 * i + 1] = layer;
     st.plan_demand[1 + 3 * i + 2] = e;
@@ -223,11 +376,23 @@ admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, in
 
   // rewrite routes to slots (in place allowed: each thread reads then writes its own r)
   int ov = 0;
-  for (int r = tid; r < R; r += kAdmitThreads) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int r = tid + j * kAdmitThreads;
+    if (r >= R) continue;
+    const int e = idv[j];
+    int o = -1;
+    if ((unsigned)e < (unsigned)E) {
+      o = slot_of[e];
+      ov += (o < 0);
+    }
+    out[r] = o;
+  }
+  for (int r = tid + 2 * kAdmitThreads; r < R; r += kAdmitThreads) {
     const int e = ids[r];
     int o = -1;
     if ((unsigned)e < (unsigned)E) {
-      o = st.map[layer * E + e];
+      o = slot_of[e];
       ov += (o < 0);
     }
     out[r] = o;
@@ -238,18 +403,20 @@ admit_kernel(DevState st, int layer, const int32_t* ids, int32_t* out, int R, in
   if (nev) atomicAdd(&s_acc[3], nev);
   if (ov) atomicAdd(&s_acc[4], ov);
   __syncthreads();
-  if (tid == 0) {
-    moe_stats* S = &st.stats[layer];
-    S->calls += 1;
-    S->lookups += s_acc[1];
-    S->hits += s_acc[2];
-    S->misses += nM;
-    S->fetched += nA;
-    S->overflow_routes += s_acc[4];
-    S->evictions += s_acc[3];
-    S->invalid_routes += s_acc[0];
-    if (s_acc[0]) S->status_bits |= MOE_STATUS_INVALID_ID;
-    if (short_of_slots) S->status_bits |= MOE_STATUS_CAPACITY;
+  if (tid == 0) {  // the counters as loaded at entry, plus this call
+    moe_stats v;
+    memcpy(&v, s_st, sizeof v);
+    v.calls += 1;
+    v.lookups += s_acc[1];
+    v.hits += s_acc[2];
+    v.misses += nM;
+    v.fetched += nA;
+    v.overflow_routes += s_acc[4];
+    v.evictions += s_acc[3];
+    v.invalid_routes += s_acc[0];
+    if (s_acc[0]) v.status_bits |= MOE_STATUS_INVALID_ID;
+    if (short_of_slots) v.status_bits |= MOE_STATUS_CAPACITY;
+    st.stats[layer] = v;
     st.plan_demand[0] = nA;
     st.clock[p] = clk;
   }
@@ -317,7 +484,8 @@ prefetch_kernel(DevState st, int layer, const int32_t* pred, int n, int32_t* pla
   if (inv) atomicAdd(&s_acc[0], inv);
   if (nreq) atomicAdd(&s_acc[1], nreq);
   if (nres) atomicAdd(&s_acc[2], nres);
-  const int nV = select_victims(st, p, clk, nQ, sel, bs);
+  const PoolKeys<false> keys{nullptr, &st, pbase, clk};
+  const int nV = select_victims<false>(st, keys, nQ, st.vict, sel, bs);
 
   if (tid == 0) {
     // Each candidate, ascending, looks at the current first evictable slot.
@@ -393,17 +561,27 @@ __global__ void pin_kernel(DevState st, size_t g, int v) { st.pinned[g] = (uint8
 
 }  // namespace
 
-size_t admit_smem_bytes(int E) { return 2ull * E * sizeof(int); }
+// Dynamic shared memory of an admission: [E] x 3 counters, plus the pool's
+// victim keys and slot keys when the pool is small enough to keep.
+constexpr size_t kAdmitCacheMax = 200 * 1024;
+bool admit_cached(int E, int S) { return (size_t)S * 12 + 3ull * E * 4 <= kAdmitCacheMax; }
+size_t admit_smem_bytes(int E, int S) {
+  return 3ull * E * sizeof(int) + (admit_cached(E, S) ? (size_t)S * 12 : 0);
+}
 
 cudaError_t launch_admit(const DevState& st, int layer, const int32_t* ids, int32_t* out, int R,
                          int cap, cudaStream_t s) {
-  admit_kernel<<<1, kAdmitThreads, admit_smem_bytes(st.E), s>>>(st, layer, ids, out, R, cap);
+  const size_t smem = admit_smem_bytes(st.E, st.S);
+  if (admit_cached(st.E, st.S))
+    admit_kernel<true><<<1, kAdmitThreads, smem, s>>>(st, layer, ids, out, R, cap);
+  else
+    admit_kernel<false><<<1, kAdmitThreads, smem, s>>>(st, layer, ids, out, R, cap);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefetch(const DevState& st, int layer, const int32_t* pred, int n,
                             int32_t* plan, cudaStream_t s) {
-  prefetch_kernel<<<1, kAdmitThreads, admit_smem_bytes(st.E), s>>>(st, layer, pred, n, plan);
+  prefetch_kernel<<<1, kAdmitThreads, 2ull * st.E * sizeof(int), s>>>(st, layer, pred, n, plan);
   return cudaGetLastError();
 }
 
@@ -417,13 +595,16 @@ cudaError_t launch_pin(const DevState& st, int layer, int slot, int pinned, cuda
   return cudaGetLastError();
 }
 
-cudaError_t admit_set_smem_limits(int E) {
-  const size_t bytes = admit_smem_bytes(E);
-  cudaError_t e = cudaFuncSetAttribute(admit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)bytes);
+cudaError_t admit_set_smem_limits(int E, int S) {
+  cudaError_t e = cudaFuncSetAttribute(admit_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)admit_smem_bytes(E, S));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(admit_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)admit_smem_bytes(E, S));
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(prefetch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)bytes);
+                              (int)(2ull * E * sizeof(int)));
 }
 
 }  // namespace moe

@@ -132,7 +132,7 @@ __device__ __forceinline__ void block_minmax_u64(unsigned long long mn, unsigned
 // ---------------------------------------------------------------- launchers
 // Each returns the cudaError_t of the launch.
 
-size_t admit_smem_bytes(int E);
+size_t admit_smem_bytes(int E, int S);
 cudaError_t launch_admit(const DevState& st, int layer, const int32_t* ids, int32_t* out, int R,
                          int cap, cudaStream_t s);
 cudaError_t launch_prefetch(const DevState& st, int layer, const int32_t* pred, int n,

@@ -1,5 +1,5 @@
-// ffn_stream.cu -- expert FFNs for decode-sized steps, streamed through
-// shared memory with bulk asynchronous copies.
+// ffn_stream.cu -- expert FFNs for decode-sized steps: one cooperative launch
+// per group of experts.
 //
 // What is computed is the same as gemv.cu (FreeToken issue #753 "[Perf]
 // Offloaded decode: overlap the expert-miss gather with the same layer's
@@ -8,21 +8,28 @@
 // fast path when every (route, row) of the step fits a small task list.
 //
 // A decode step moves ~14 MB of weights per layer, which the HBM delivers in
-// ~2 us, so the kernel must have megabytes in flight almost at once.  One
-// cooperative launch of one CTA per SM computes a whole group of expert FFNs:
-// gate/up rows (phase A), a grid-wide barrier, then down rows and the combine
-// (phase B).  A producer warp streams the weight rows of both phases through
-// a ring of shared-memory stages with cp.async.bulk (completion on per-stage
-// mbarriers), so phase-B weights land while phase A computes; sixteen
-// consumer warps decode the stages as they land.
+// ~2 us after ~1 us of latency, and the arithmetic per weight is a handful of
+// instructions, so the kernel is built to have every byte requested within a
+// microsecond of entry and to spend few instructions per weight:
+//   * one CTA per SM (cooperative launch), 16 warps;
+//   * phase A (gate/up): each warp owns whole weight rows, loads them straight
+//     into registers (16-byte loads, next row in flight while the current one
+//     is decoded) and reduces each row in-warp -- no shared-memory staging, no
+//     block-wide synchronisation per row;
+//   * the down-projection rows this CTA needs in phase B are requested with
+//     cp.async into shared memory at entry, so they land during phase A;
+//   * a grid-wide barrier (h of every task is needed by every CTA);
+//   * phase B (down + combine): each warp takes runs of (task, output row)
+//     items, reduces four at a time with one butterfly, and the CTA combines
+//     its output rows over the tasks in route order.
 //
-// Every wait (mbarrier, grid barrier) is bounded (%globaltimer); on a timeout
-// the kernel sets MOE_STATUS_TIMEOUT in the cache's device status word, skips
-// the remaining work, drains its own copies (again bounded) and returns.
+// The only wait that depends on other CTAs is the grid barrier; it is bounded
+// (%globaltimer): on a timeout the kernel sets MOE_STATUS_TIMEOUT in the
+// cache's device status word and skips the remaining work.
 #include <cuda_bf16.h>
-#include <cuda_fp4.h>
-#include <cuda_fp8.h>
+#include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -30,12 +37,15 @@
 namespace moe {
 namespace {
 
-constexpr int kSW = 16;            // warps per CTA
-constexpr int kST = 32 * kSW;      // threads per CTA
-constexpr int kMaxStages = 8;      // ring depth
+constexpr int kW = 16;             // warps per CTA
+constexpr int kT = 32 * kW;        // threads per CTA
 constexpr int kMaxTasks = 64;      // routes per call on this path
-constexpr int kXW = 4;             // x words (8 bf16 each) held per consumer thread
-constexpr int kYsPre = 2;          // shared-expert outputs prefetched per consumer thread
+constexpr int kMaxRows = 16;       // batch rows per call on this path
+constexpr int kXW = 4;             // x words (8 elements each) loaded per thread
+constexpr int kYsPre = 1;          // shared-expert outputs prefetched per thread
+// Registers per thread: 512 x 104 leaves room on the SM for a gather CTA
+// (256 threads x 32 registers), which runs beside this kernel on the side stream.
+constexpr int kMaxReg = 104;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
 
 // ------------------------------------------------------------ PTX wrappers
@@ -48,71 +58,29 @@ __device__ __forceinline__ unsigned long long now_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_one(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
+// 16 bytes global -> shared, asynchronous (completion by cp.async.wait_group)
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+               : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// wait until at most n of this thread's most recent groups are still pending (n <= 7)
-__device__ __forceinline__ void cp_async_wait(int n) {
-  switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
-    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
-  }
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
 }
-// cooperative copy of `bytes` (multiple of 16) by kST threads, 16 bytes each
-__device__ __forceinline__ void copy_async(uint8_t* dst, const uint8_t* src, uint32_t bytes) {
-  for (uint32_t o = threadIdx.x * 16; o < bytes; o += kST * 16) cp_async16(dst + o, src + o);
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
+// read-only weight loads that should not displace anything in L1
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
 }
-// Bounded wait; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
-  const unsigned long long t0 = now_ns();
-  while (!mbar_test(bar, parity)) {
-    if (now_ns() - t0 > kWaitNs) return false;
-  }
-  return true;
+__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
 }
 
 // ------------------------------------------------------------ decode helpers
@@ -189,20 +157,6 @@ __device__ __forceinline__ float dot8_fp4_f(uint32_t w, const float* h) {
   f = h2_f32(e2m1x2_h2<3>(w));
   return fmaf(f.x, h[6], fmaf(f.y, h[7], a));
 }
-// sum_{i<8} e2m1(nibble i of w) * h[i] with h given as f16 hi + lo parts
-// (h = hi + lo to ~22 bits); products exact, fp32 accumulate
-__device__ __forceinline__ float dot8_fp4_hl(uint32_t w, const uint32_t* hi, const uint32_t* lo) {
-  const uint32_t c0 = e2m1x2_h2<0>(w), c1 = e2m1x2_h2<1>(w), c2 = e2m1x2_h2<2>(w),
-                 c3 = e2m1x2_h2<3>(w);
-  float a = fma2_h(c0, hi[0], 0.f), b = fma2_h(c0, lo[0], 0.f);
-  a = fma2_h(c1, hi[1], a);
-  b = fma2_h(c1, lo[1], b);
-  a = fma2_h(c2, hi[2], a);
-  b = fma2_h(c2, lo[2], b);
-  a = fma2_h(c3, hi[3], a);
-  b = fma2_h(c3, lo[3], b);
-  return a + b;
-}
 // sum_{i<8} bf16 weights (uint4) * bf16 x (uint4), fp32
 __device__ __forceinline__ float dot8_bf16_bf(uint4 w, uint4 x, float a) {
   a = fma2_bf(w.x, x.x, a);
@@ -226,6 +180,7 @@ __device__ __forceinline__ float wsum(float v) {
   return v;
 }
 
+
 // Offsets inside a blob (layout of moe_cache.h).
 struct BlobOff {
   size_t code[3], scale[3], glob;  // NVFP4
@@ -245,88 +200,172 @@ struct BlobOff {
   }
 };
 
-// Per-call task list, identical in every CTA: the valid routes in route order,
-// with each task's blob, routing weight and fp32 global scales staged in
-// shared memory so the compute loops never wait on a global load.
+// Per-call task list, identical in every CTA: the valid routes in route order.
 struct Tasks {
   int n;
-  int route[kMaxTasks];  // route index r = b*k + j
+  int route[kMaxTasks];            // route index r = b*k + j
   const uint8_t* blob[kMaxTasks];
-  float wt[kMaxTasks];   // routing weight (1 for the shared expert)
-  float gs[kMaxTasks][3];  // NVFP4 global scales of gate, up, down (1 for bf16)
-  int valid[kMaxTasks];
+  float wt[kMaxTasks];             // routing weight x down global scale
 };
 
-// Step 1 (threads r < R, one global round trip): which routes have a slot.
-// Step 2 (after a __syncthreads): compaction by a prefix count.
-// Step 3 (after a __syncthreads): weights and global scales, in parallel.
-__device__ void tasks_load(Tasks& tk, const DevState& st, int layer, const int32_t* slot_ids,
-                           int R, const uint8_t* fixed_blob) {
-  const int r = threadIdx.x;
-  if (r < R) {
-    const uint8_t* b = fixed_blob;
-    if (!b) {
-      const int s = slot_ids[r];
-      b = (unsigned)s < (unsigned)st.S
-              ? st.slots + ((size_t)pool_of(st, layer) * st.S + s) * st.stride
-              : nullptr;
-    }
-    tk.valid[r] = b != nullptr;
-    tk.blob[r] = b;  // temporarily indexed by route
-  }
-}
-__device__ void tasks_compact(Tasks& tk, int R) {
-  const int r = threadIdx.x;
-  const uint8_t* b = r < R ? tk.blob[r] : nullptr;
-  int pos = 0;
-  if (r < R && tk.valid[r])
-    for (int q = 0; q < r; ++q) pos += tk.valid[q];
-  __syncthreads();
-  if (r < R && tk.valid[r]) {
-    tk.route[pos] = r;
-    tk.blob[pos] = b;
-  }
-  if (r == 0) {
-    int n = 0;
-    for (int q = 0; q < R; ++q) n += tk.valid[q];
-    tk.n = n;
-  }
-}
 __device__ void flag_timeout(unsigned long long* status) {
   if (status) atomicOr(status, (unsigned long long)MOE_STATUS_TIMEOUT);
 }
 
-// ---------------------------------------------------------------- pipeline
-// A CTA walks a list of chunks; a chunk is `rc` consecutive rows of one
-// task's matrix (gate+up for the gate/up kernel, down for the down kernel),
-// copied with one cp.async.bulk per bank (codes, scales) into a ring stage.
-// Warp kSW (the producer) issues the copies; the kSW consumer warps split the
-// chunk into rc rows x (kSW / rc) slices of the reduction dimension, combine
-// the slices of each row through shared memory in a fixed order, and release
-// the stage.  full[s] completes on the copies' bytes, empty[s] on release.
+// x lives in shared memory as 16-byte units, row-major per batch row, with
+// unit u of a row stored at u ^ ((u >> 3) & 7): the eight lanes of a quarter
+// warp that read units 8L + j (NVFP4, 64 contiguous elements per lane) or
+// 32s + L (bf16) then hit eight different bank groups.
+__device__ __forceinline__ int xswz(int u) { return u ^ ((u >> 3) & 7); }
 
-struct Ring {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+// Power of two that brings max |x| of a row below 2^15 (1 when it already is).
+// At most 140 halvings, so an infinite input cannot keep the loop going.
+__device__ __forceinline__ float x_scale(float mx) {
+  float sc = 1.f;
+  for (int i = 0; i < 140 && mx * sc >= 32768.f; ++i) sc *= 0.5f;
+  return sc;
+}
+
+// Two per-lane partial sums -> lane 0 holds both totals (6 shuffles).
+__device__ __forceinline__ float2 reduce2(float g, float u, int lane) {
+  const bool hi = lane & 16;
+  float v = hi ? u : g;
+  v += __shfl_xor_sync(0xffffffffu, hi ? g : u, 16);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return make_float2(v, __shfl_sync(0xffffffffu, v, 16));
+}
+// Four per-lane partial sums -> lane 8j holds the total of p[j] (6 shuffles).
+__device__ __forceinline__ float reduce4(const float p[4], int lane) {
+  const bool hi = lane & 16, h8 = lane & 8;
+  float k0 = hi ? p[2] : p[0], k1 = hi ? p[3] : p[1];
+  k0 += __shfl_xor_sync(0xffffffffu, hi ? p[0] : p[2], 16);
+  k1 += __shfl_xor_sync(0xffffffffu, hi ? p[1] : p[3], 16);
+  float v = h8 ? k1 : k0;
+  v += __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------ phase A rows
+// One gate row and one up row (a chunk of CW elements of each), in registers.
+//   NVFP4 (CW = 2048): lane L holds elements [64L, 64L+64) of the chunk:
+//     32 code bytes and 4 e4m3 block scales per matrix.
+//   bf16  (CW = 512):  lane L holds elements 256s + 8L + [0, 8), s = 0..1.
+template <int FMT>
+struct RowA;
+template <>
+struct RowA<MOE_W_NVFP4> {
+  static constexpr int CW = 2048;
+  uint4 g0, g1, u0, u1;
+  uint32_t sg, su;
+  float gs0, gs1;  // the row's gate / up global scales (lane 0 only)
+  __device__ __forceinline__ void load(const uint8_t* blob, const BlobOff& o, int H, int i, int c,
+                                       int lane) {
+    if (lane == 0) {
+      gs0 = *reinterpret_cast<const float*>(blob + o.glob);
+      gs1 = *reinterpret_cast<const float*>(blob + o.glob + 4);
+    }
+    const size_t cr = (size_t)i * (H / 2) + c * 1024 + lane * 32;
+    const size_t sr = (size_t)i * (H / 16) + c * 128 + lane * 4;
+    g0 = ldg_stream16(blob + o.code[0] + cr);
+    g1 = ldg_stream16(blob + o.code[0] + cr + 16);
+    u0 = ldg_stream16(blob + o.code[1] + cr);
+    u1 = ldg_stream16(blob + o.code[1] + cr + 16);
+    sg = ldg_stream4(blob + o.scale[0] + sr);
+    su = ldg_stream4(blob + o.scale[1] + sr);
+  }
+  // x row (16-byte units, swizzled) -> per-lane partial gate / up sums
+  __device__ __forceinline__ void dot(const uint4* xr, int c, int lane, float& g, float& u) const {
+    const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    const float2 sg01 = e4m3x2_f32(sg & 0xffffu), sg23 = e4m3x2_f32(sg >> 16);
+    const float2 su01 = e4m3x2_f32(su & 0xffffu), su23 = e4m3x2_f32(su >> 16);
+    const float sgv[4] = {sg01.x, sg01.y, sg23.x, sg23.y};
+    const float suv[4] = {su01.x, su01.y, su23.x, su23.y};
+    const int u0i = c * 256 + lane * 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 xa = xr[xswz(u0i + 2 * j)], xb = xr[xswz(u0i + 2 * j + 1)];
+      g = fmaf(dot8_fp4_h(gw[2 * j], xa) + dot8_fp4_h(gw[2 * j + 1], xb), sgv[j], g);
+      u = fmaf(dot8_fp4_h(uw[2 * j], xa) + dot8_fp4_h(uw[2 * j + 1], xb), suv[j], u);
+    }
+  }
+};
+template <>
+struct RowA<MOE_W_BF16> {
+  static constexpr int CW = 512;
+  static constexpr float gs0 = 1.f, gs1 = 1.f;
+  uint4 g[2], u[2];
+  __device__ __forceinline__ void load(const uint8_t* blob, const BlobOff& o, int H, int i, int c,
+                                       int lane) {
+    const size_t e = (size_t)i * H + c * 512 + lane * 8;
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      g[s] = ldg_stream16(blob + o.mat[0] + (e + 256 * s) * 2);
+      u[s] = ldg_stream16(blob + o.mat[1] + (e + 256 * s) * 2);
+    }
+  }
+  __device__ __forceinline__ void dot(const uint4* xr, int c, int lane, float& gs, float& us) const {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const uint4 xv = xr[xswz(c * 64 + 32 * s + lane)];
+      gs = dot8_bf16_bf(g[s], xv, gs);
+      us = dot8_bf16_bf(u[s], xv, us);
+    }
+  }
 };
 
-// The producer's last act: wait (bounded) until every chunk it issued has
-// landed, so no copy is still writing shared memory when the CTA exits.
-__device__ void producer_drain(Ring& rg, int nstage, int issued) {
-  for (int c = issued - nstage < 0 ? 0 : issued - nstage; c < issued; ++c)
-    mbar_wait(&rg.full[c % nstage], (uint32_t)((c / nstage) & 1));
-}
+// ------------------------------------------------------------ phase B items
+// One down row of one task: I = 512 m elements.
+//   NVFP4: lane L holds elements [16mL, 16mL + 16m): 8m code bytes, m scales.
+//   bf16:  lane L holds elements 256s + 8L + [0, 8), s = 0..2m-1.
+// h (fp32) for the same elements sits in registers, 16m values per lane.
+template <int FMT>
+struct ItemB {
+  uint4 w[2];   // NVFP4: w[0] = codes (8m bytes), w[1].x = scales; bf16: 2m of these
+  uint4 w2[2];  // bf16, m = 2 only
+};
 
-// Named barrier among the consumer warps only (the producer does not take part).
-__device__ __forceinline__ void consumers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kSW * 32) : "memory");
+// loads one item's lane data from `row` (shared or global, generic address)
+template <int FMT>
+__device__ __forceinline__ void itemb_load(ItemB<FMT>& it, const uint8_t* codes,
+                                           const uint8_t* scales, int m, int lane) {
+  if (FMT == MOE_W_NVFP4) {
+    if (m == 1) {
+      const uint2 cw = *reinterpret_cast<const uint2*>(codes + lane * 8);
+      it.w[0] = make_uint4(cw.x, cw.y, 0u, 0u);
+      it.w[1].x = scales[lane];
+    } else {
+      it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
+      it.w[1].x = *reinterpret_cast<const uint16_t*>(scales + lane * 2);
+    }
+  } else {
+    it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
+    it.w[1] = *reinterpret_cast<const uint4*>(codes + 512 + lane * 16);
+    if (m == 2) {
+      it.w2[0] = *reinterpret_cast<const uint4*>(codes + 1024 + lane * 16);
+      it.w2[1] = *reinterpret_cast<const uint4*>(codes + 1536 + lane * 16);
+    }
+  }
 }
-
-// rows per chunk: the largest power of two <= 16 whose stage fits `cap` bytes
-__host__ __device__ inline int rows_per_chunk(int row_bytes, int cap) {
-  int rc = 16;
-  while (rc > 1 && rc * row_bytes > cap) rc >>= 1;
-  return rc;
+template <int FMT>
+__device__ __forceinline__ float itemb_dot(const ItemB<FMT>& it, const float* hv, int m) {
+  if (FMT == MOE_W_NVFP4) {
+    const float2 sc = e4m3x2_f32(it.w[1].x & 0xffffu);
+    float p = (dot8_fp4_f(it.w[0].x, hv) + dot8_fp4_f(it.w[0].y, hv + 8)) * sc.x;
+    if (m == 2) p = fmaf(dot8_fp4_f(it.w[0].z, hv + 16) + dot8_fp4_f(it.w[0].w, hv + 24), sc.y, p);
+    return p;
+  } else {
+    float p = dot8_bf16_f(it.w[0], hv, 0.f);
+    p = dot8_bf16_f(it.w[1], hv + 8, p);
+    if (m == 2) {
+      p = dot8_bf16_f(it.w2[0], hv + 16, p);
+      p = dot8_bf16_f(it.w2[1], hv + 24, p);
+    }
+    return p;
+  }
 }
 
 // ---------------------------------------------------------------- grid barrier
@@ -336,7 +375,7 @@ __host__ __device__ inline int rows_per_chunk(int row_bytes, int cap) {
 // the h written before the barrier with the reads after it.  Bounded spin.
 __device__ bool grid_barrier(unsigned long long* ctr, unsigned long long* status) {
   __shared__ int s_ok;
-  consumers_sync();
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     unsigned long long old;
@@ -353,31 +392,24 @@ __device__ bool grid_barrier(unsigned long long* ctr, unsigned long long* status
         ok = 0;
         break;
       }
-      __nanosleep(32);
     }
     s_ok = ok;
   }
-  consumers_sync();
+  __syncthreads();
   return s_ok != 0;
 }
 
 // ---------------------------------------------------------------- fused FFN
 // One launch computes a group of expert FFNs for a decode-sized step:
-//   phase A (gate/up): rows u of the flattened (task, n) list,
-//       h[route][n] = silu(W_g x_b)[n] * (W_u x_b)[n];
+//   phase A (gate/up): rows (task t, i) of the flattened list,
+//       h[route_t][i] = silu(W_g x_b)[i] * (W_u x_b)[i];
 //   grid barrier;
-//   phase B (down + combine): output rows (b, n),
+//   phase B (down + combine) over this CTA's output rows (b, n):
 //       SHARED: ys[b][n] = sigmoid(x_b . w_g) * (W_d h_b)[n]
 //       ROUTED: out[b][n] = bf16( sum_j w[b,j] (W_d[slot] h_bj)[n] + ys[b][n] ).
-// The producer warp streams the chunks of both phases through one ring of
-// stages with cp.async.bulk: phase-B weights arrive during phase A and the
-// barrier; after the barrier only h (a few KB, from L2) is read.
-//
-// Phase A chunk: rcA consecutive rows of one task, gate and up banks.
-// Phase B chunk: rcB rows of one batch row b for a group of up to tpc of b's
-// tasks.  Consumer warps split a chunk into (task, K slice, row) items, keep
-// their slice of x (A) or h (B) in registers, read weights with lane-contiguous
-// loads, and combine slice partials through shared memory in a fixed order.
+// Phase-B items are (task, output row) pairs, b-major then task then row; the
+// first `qs` of them are staged in shared memory at entry (cp.async), the rest
+// are read from global memory when they are reached.
 //
 // x is staged once per CTA: as f16 for NVFP4 experts (products e2m1 * x exact
 // halves-times-halves), scaled per row by a power of two so that max |x| < 2^15
@@ -394,45 +426,86 @@ struct FusedArgs {
   float* gate;                 // SHARED: sigmoid gate per row (scratch)
   float* ys;                   // SHARED: output [n_rows][H]; ROUTED: input (may be null)
   __nv_bfloat16* out;          // ROUTED output
-  int nstage, stage_bytes, rcA, rcB, tpc;
+  int qs;                      // phase-B items staged in shared memory
+  int htasks;                  // tasks whose h fits the CTA's h buffer (>= its tasks)
   unsigned long long* status;
   unsigned long long* bar_ctr;
 };
 
 template <int FMT, bool SHARED>
-__global__ void __launch_bounds__(kST + 32, 1)
-ffn_fused_kernel(DevState st, FusedArgs a) {
+__global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) {
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ Tasks tk;
-  __shared__ Ring rg;
-  __shared__ unsigned int xmax[16];  // per row max |x| (float bits, only when > 2^14)
-  __shared__ float xscale[16];       // per row power-of-two scale applied to x
-  __shared__ float xinv[16];         // per row 1 / scale
-  __shared__ float gate_s[16];
-  __shared__ int ts[17];             // tasks of batch row b: [ts[b], ts[b+1])
+  __shared__ int ts[kMaxRows + 1];         // tasks of batch row b: [ts[b], ts[b+1])
+  __shared__ unsigned int xmax[kMaxRows];  // per row max |x| (float bits, only when > 2^14)
+  __shared__ float xinv[kMaxRows];         // per row 1 / (power-of-two scale applied to x)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, I = a.I, k = a.k, n_rows = a.n_rows;
+  const int m = I / 512;                                   // 16-element groups per lane (B)
+  const int CB = FMT == MOE_W_NVFP4 ? I / 2 : I * 2;       // down row: code bytes
+  const int SB = FMT == MOE_W_NVFP4 ? I / 16 : 0;          // down row: scale bytes
+  constexpr int CW = RowA<FMT>::CW;
+  const int KC = H / CW;                                   // phase-A chunks per row
+  const BlobOff o(H, I);
 
-  const int rowB = FMT == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;            // down row bytes
-  const int nslA = H / 1024, nslB = I / 512;
-  const int rcA = a.rcA, rcB = a.rcB, tpc = a.tpc, nstage = a.nstage;
+  // this CTA's output rows (phase B): at most two batch rows (perB <= H)
+  const int UB = n_rows * H;
+  const int perB = (UB + gridDim.x - 1) / gridDim.x;
+  const int ru0 = min(UB, perB * (int)blockIdx.x), ru1 = min(UB, ru0 + perB);
 
-  // ---- prologue: one global round trip for the routes' slots and all of x
+  // ---- entry: the slot ids (warp 0) and x (everyone) in flight at once
   const int nx8 = n_rows * H / 8;
   uint4 xw[kXW];
-  if (threadIdx.x < 16) xmax[threadIdx.x] = 0u;
-  tasks_load(tk, st, a.layer, a.slot_ids, a.R, a.fixed_blob);
 #pragma unroll
   for (int j = 0; j < kXW; ++j) {
-    const int i = threadIdx.x + j * kST;
-    if (threadIdx.x < kST && i < nx8) xw[j] = reinterpret_cast<const uint4*>(a.x)[i];
+    const int i = threadIdx.x + j * kT;
+    if (i < nx8) xw[j] = reinterpret_cast<const uint4*>(a.x)[i];
   }
-  __syncthreads();
-  if (FMT == MOE_W_NVFP4) {
+  float ysv[kYsPre];
+#pragma unroll
+  for (int j = 0; j < kYsPre; ++j) {
+    const int ru = ru0 + threadIdx.x + j * kT;
+    ysv[j] = (!SHARED && a.ys && ru < ru1) ? a.ys[ru] : 0.f;
+  }
+  if (threadIdx.x < kMaxRows) xmax[threadIdx.x] = 0u;
+  if (warp == 0) {
+    const uint8_t* b0 = nullptr;
+    const uint8_t* b1 = nullptr;
+    auto resolve = [&](int r) -> const uint8_t* {
+      if (a.fixed_blob) return a.fixed_blob;
+      const int s = a.slot_ids[r];
+      return (unsigned)s < (unsigned)st.S
+                 ? st.slots + ((size_t)pool_of(st, a.layer) * st.S + s) * st.stride
+                 : nullptr;
+    };
+    if (lane < a.R) b0 = resolve(lane);
+    if (lane + 32 < a.R) b1 = resolve(lane + 32);
+    const unsigned m0 = __ballot_sync(0xffffffffu, b0 != nullptr);
+    const unsigned m1 = __ballot_sync(0xffffffffu, b1 != nullptr);
+    const unsigned lt = (1u << lane) - 1u;
+    if (b0) {
+      const int p = __popc(m0 & lt);
+      tk.route[p] = lane;
+      tk.blob[p] = b0;
+    }
+    if (b1) {
+      const int p = __popc(m0) + __popc(m1 & lt);
+      tk.route[p] = lane + 32;
+      tk.blob[p] = b1;
+    }
+    if (lane == 0) tk.n = __popc(m0) + __popc(m1);
+    if (lane <= n_rows) {  // first task of batch row `lane`: valid routes below lane*k
+      const int lim = lane * k;
+      const unsigned a0 = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
+      const unsigned a1 = lim >= 64 ? 0xffffffffu : (lim <= 32 ? 0u : ((1u << (lim - 32)) - 1u));
+      ts[lane] = __popc(m0 & a0) + __popc(m1 & a1);
+    }
+  }
+  if (FMT == MOE_W_NVFP4) {  // rows whose |x| reaches 2^14 get a scale below 1
 #pragma unroll
     for (int j = 0; j < kXW; ++j) {
-      const int i = threadIdx.x + j * kST;
-      if (threadIdx.x >= kST || i >= nx8) continue;
+      const int i = threadIdx.x + j * kT;
+      if (i >= nx8) continue;
       const uint32_t wv[4] = {xw[j].x, xw[j].y, xw[j].z, xw[j].w};
       float mx = 0.f;
 #pragma unroll
@@ -442,168 +515,46 @@ ffn_fused_kernel(DevState st, FusedArgs a) {
       if (mx > 16384.f) atomicMax(&xmax[(i * 8) / H], __float_as_uint(mx));
     }
   }
-  tasks_compact(tk, a.R);
-  if (threadIdx.x == 0) {
-    for (int q = 0; q < nstage; ++q) {
-      mbar_init(&rg.full[q], 1);
-      mbar_init(&rg.empty[q], 1);
-    }
-    fence_barrier_init();
-  }
-  __syncthreads();
+  __syncthreads();  // (1) task list, ts, xmax
   const int T = tk.n;
-  if (threadIdx.x <= n_rows) {  // first task of each batch row (tasks are b-major)
-    int t = 0;
-    while (t < T && tk.route[t] / k < (int)threadIdx.x) ++t;
-    ts[threadIdx.x] = t;
-  }
-  __syncthreads();
 
-  // phase A rows of this CTA
-  const int UA = T * I;
-  const int perA = (UA + gridDim.x - 1) / gridDim.x;
-  const int u0 = min(UA, perA * blockIdx.x), u1 = min(UA, u0 + perA);
-  // phase B output rows of this CTA
-  const int UB = n_rows * H;
-  const int perB = (UB + gridDim.x - 1) / gridDim.x;
-  const int ru0 = min(UB, perB * blockIdx.x), ru1 = min(UB, ru0 + perB);
-
-  // shared memory: x | h [T][I] | y [T][perB] | redA [2][2][nslA*rcA] | redB [2][tpc*nslB*rcB] | ring
+  // ---- phase A assignment: whole rows, contiguous per warp
+  const int Gw = gridDim.x * kW, gw = blockIdx.x * kW + warp;
+  const int NA = T * I;
+  const int perA = (NA + Gw - 1) / Gw;
+  const int ra0 = min(NA, gw * perA), ra1 = min(NA, ra0 + perA);
+  const int nitA = (ra1 - ra0) * KC;
+  RowA<FMT> bufA, bufB;
+  auto item_load = [&](RowA<FMT>& buf, int it) {
+    const int r = ra0 + it / KC, c = it % KC;
+    const int t = r / I;
+    buf.load(tk.blob[t], o, H, r - t * I, c, lane);
+  };
+  // ---- phase-B items of this CTA (staged into shared memory after (2))
+  const int bA = ru0 / H, bB = ru1 > ru0 ? (ru1 - 1) / H : bA;
+  auto nlo_of = [&](int b) { return max(ru0 - b * H, 0); };
+  auto nlen_of = [&](int b) { return min(ru1 - b * H, H) - nlo_of(b); };
+  const int cntA = ru1 > ru0 ? (ts[bA + 1] - ts[bA]) * nlen_of(bA) : 0;
+  const int cntB = (ru1 > ru0 && bB != bA) ? (ts[bB + 1] - ts[bB]) * nlen_of(bB) : 0;
+  const int NQ = cntA + cntB;
   uint16_t* xs = reinterpret_cast<uint16_t*>(sm);
-  float* hsm = reinterpret_cast<float*>(sm + ((size_t)n_rows * H * 2 + 127) / 128 * 128);
-  float* ysm = hsm + (size_t)T * I;
-  float* redA = ysm + (size_t)T * perB;
-  const int redA_n = nslA * rcA;
-  float* redB = redA + 4 * redA_n;
-  const int redB_n = tpc * nslB * rcB;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(redB + 2 * redB_n) + 127) / 128 * 128);
-  const BlobOff o(H, I);
+  float* ysm = reinterpret_cast<float*>(sm + ((size_t)n_rows * H * 2 + 127) / 128 * 128);
+  float* hsm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ysm) +
+                                        ((size_t)a.R * perB * 4 + 127) / 128 * 128);
+  uint8_t* stC = reinterpret_cast<uint8_t*>(hsm) + ((size_t)a.htasks * I * 4 + 127) / 128 * 128;
+  uint8_t* stS = stC + (size_t)a.qs * CB;
+  const int qs = min(a.qs, NQ);
 
-  // phase B chunk cursor: (b, row block n, task group t0); rows without tasks skipped
-  struct Cur {
-    int b, n, t0;
-  };
-  auto b_lo = [&](int b) { return max(ru0 - b * H, 0); };
-  auto b_hi = [&](int b) { return min(ru1 - b * H, H); };
-  auto settle = [&](Cur& c) -> bool {
-    while (c.b * H < ru1) {
-      if (ts[c.b] < ts[c.b + 1] && c.n < b_hi(c.b)) {
-        if (c.t0 < ts[c.b]) c.t0 = ts[c.b];
-        if (c.t0 < ts[c.b + 1]) return true;
-        c.t0 = ts[c.b];
-        c.n += rcB;
-        continue;
-      }
-      ++c.b;
-      if (c.b * H >= ru1) return false;
-      c.n = b_lo(c.b);
-      c.t0 = ts[c.b];
-    }
-    return false;
-  };
-  auto advance = [&](Cur& c) -> bool {
-    c.t0 += tpc;
-    return settle(c);
-  };
-  auto start = [&](Cur& c) -> bool {
-    if (ru0 >= ru1) return false;
-    c.b = ru0 / H;
-    c.n = b_lo(c.b);
-    c.t0 = ts[c.b];
-    return settle(c);
-  };
-
-  if (warp == kSW) {  // ================================================ producer
-    if (lane == 0) {
-      int q = 0;
-      bool ok = true;
-      auto acquire = [&](int& s) -> bool {  // next stage, free
-        s = q % nstage;
-        if (q >= nstage && !mbar_wait(&rg.empty[s], (uint32_t)(((q / nstage) - 1) & 1))) {
-          flag_timeout(a.status);
-          return false;
-        }
-        fence_proxy_async();
-        return true;
-      };
-      for (int u = u0; u < u1 && ok;) {  // phase A
-        const int t = u / I, n = u - t * I;
-        const int nr = min(rcA, min(u1 - u, I - n));
-        int s;
-        if (!(ok = acquire(s))) break;
-        uint8_t* dst = ring + (size_t)s * a.stage_bytes;
-        const uint8_t* blob = tk.blob[t];
-        if (FMT == MOE_W_NVFP4) {
-          const uint32_t cb = nr * (H / 2), sb = nr * (H / 16);
-          mbar_expect_tx(&rg.full[s], 2 * (cb + sb));
-          bulk_g2s(dst, blob + o.code[0] + (size_t)n * (H / 2), cb, &rg.full[s]);
-          bulk_g2s(dst + rcA * (H / 2), blob + o.code[1] + (size_t)n * (H / 2), cb, &rg.full[s]);
-          bulk_g2s(dst + 2 * rcA * (H / 2), blob + o.scale[0] + (size_t)n * (H / 16), sb, &rg.full[s]);
-          bulk_g2s(dst + 2 * rcA * (H / 2) + rcA * (H / 16), blob + o.scale[1] + (size_t)n * (H / 16), sb,
-                   &rg.full[s]);
-        } else {
-          const uint32_t rb = nr * H * 2;
-          mbar_expect_tx(&rg.full[s], 2 * rb);
-          bulk_g2s(dst, blob + o.mat[0] + (size_t)n * H * 2, rb, &rg.full[s]);
-          bulk_g2s(dst + (size_t)rcA * H * 2, blob + o.mat[1] + (size_t)n * H * 2, rb, &rg.full[s]);
-        }
-        ++q;
-        u += nr;
-      }
-      Cur c;
-      for (bool more = ok && start(c); more; more = advance(c)) {  // phase B
-        const int nr = min(rcB, b_hi(c.b) - c.n);
-        const int t1 = min(c.t0 + tpc, ts[c.b + 1]);
-        int s;
-        if (!acquire(s)) break;
-        uint8_t* dst = ring + (size_t)s * a.stage_bytes;
-        mbar_expect_tx(&rg.full[s], (t1 - c.t0) * nr * rowB);
-        for (int t = c.t0; t < t1; ++t) {  // stage: task-major, each task rcB rows
-          uint8_t* d = dst + (size_t)(t - c.t0) * rcB * rowB;
-          const uint8_t* blob = tk.blob[t];
-          if (FMT == MOE_W_NVFP4) {
-            bulk_g2s(d, blob + o.code[2] + (size_t)c.n * (I / 2), nr * (I / 2), &rg.full[s]);
-            bulk_g2s(d + rcB * (I / 2), blob + o.scale[2] + (size_t)c.n * (I / 16), nr * (I / 16),
-                     &rg.full[s]);
-          } else {
-            bulk_g2s(d, blob + o.mat[2] + (size_t)c.n * I * 2, nr * I * 2, &rg.full[s]);
-          }
-        }
-        ++q;
-      }
-      producer_drain(rg, nstage, q);
-    }
-    return;
-  }
-
-  // ================================================================ consumers
-  // per-task constants: loads issued now, stored to shared memory before use
-  float cg0 = 1.f, cg1 = 1.f, cg2 = 1.f, cw = 1.f;
-  if (threadIdx.x < T) {
-    if (!SHARED) cw = a.w[tk.route[threadIdx.x]];
-    if (FMT == MOE_W_NVFP4) {
-      const float* gp = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob);
-      cg0 = gp[0];
-      cg1 = gp[1];
-      cg2 = gp[2];
-    }
-  }
-  if (threadIdx.x < n_rows) {
-    float sc = 1.f;  // power of two bringing max |x| below 2^15
-    const float mx = __uint_as_float(xmax[threadIdx.x]);
-    while (mx * sc >= 32768.f) sc *= 0.5f;
-    xscale[threadIdx.x] = sc;
-    xinv[threadIdx.x] = 1.f / sc;
-  }
-  consumers_sync();
+  // ---- x in shared memory
 #pragma unroll
-  for (int j = 0; j < kXW; ++j) {  // x into shared memory (f16 for NVFP4, bf16 otherwise)
-    const int i = threadIdx.x + j * kST;
+  for (int j = 0; j < kXW; ++j) {
+    const int i = threadIdx.x + j * kT;
     if (i >= nx8) continue;
+    const int b = (i * 8) / H, u = i - b * (H / 8);
+    uint4 v = xw[j];
     if (FMT == MOE_W_NVFP4) {
-      const float sc = xscale[(i * 8) / H];
-      const uint32_t wv[4] = {xw[j].x, xw[j].y, xw[j].z, xw[j].w};
+      const float sc = x_scale(__uint_as_float(xmax[b]));
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
       uint32_t hv[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -611,18 +562,98 @@ ffn_fused_kernel(DevState st, FusedArgs a) {
                                              __uint_as_float(wv[e] & 0xffff0000u) * sc);
         hv[e] = *reinterpret_cast<const uint32_t*>(&hh);
       }
-      reinterpret_cast<uint4*>(xs)[i] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-    } else {
-      reinterpret_cast<uint4*>(xs)[i] = xw[j];
+      v = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    }
+    reinterpret_cast<uint4*>(xs)[(size_t)b * (H / 8) + xswz(u)] = v;
+  }
+  if (threadIdx.x < n_rows) {
+    xinv[threadIdx.x] = FMT == MOE_W_NVFP4 ? 1.f / x_scale(__uint_as_float(xmax[threadIdx.x])) : 1.f;
+  }
+  __syncthreads();  // (2) x
+
+  // ---- every byte this CTA needs is requested now: its phase-A rows (the
+  // first two into registers), its phase-B rows (cp.async into shared memory)
+  // and the per-task combine factors.  No CTA-wide barrier follows until the
+  // grid barrier, so each warp computes as soon as its own rows land.
+  if (nitA > 0) item_load(bufA, 0);
+  if (nitA > 1) item_load(bufB, 1);
+  {
+    for (int bi = 0; bi < 2; ++bi) {
+      const int b = bi ? bB : bA;
+      if ((bi ? cntB : cntA) == 0) continue;
+      const int nlo = nlo_of(b), nlen = nlen_of(b), qb = bi ? cntA : 0;
+      for (int t = ts[b]; t < ts[b + 1]; ++t) {
+        const int q0 = qb + (t - ts[b]) * nlen;
+        const int cnt = min(nlen, qs - q0);
+        if (cnt <= 0) break;
+        const uint8_t* blob = tk.blob[t];
+        const uint8_t* srcC = blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB;
+        for (int off = threadIdx.x * 16; off < cnt * CB; off += kT * 16)
+          cp_async16(stC + (size_t)q0 * CB + off, srcC + off);
+        if (FMT == MOE_W_NVFP4) {
+          const uint8_t* srcS = blob + o.scale[2] + (size_t)nlo * SB;
+          for (int off = threadIdx.x * 16; off < cnt * SB; off += kT * 16)
+            cp_async16(stS + (size_t)q0 * SB + off, srcS + off);
+        }
+      }
+    }
+    cp_async_commit();
+  }
+  // per-task combine factor (stored to shared memory before the grid barrier)
+  float cw = 1.f, c2 = 1.f;
+  if (threadIdx.x < T) {
+    if (!SHARED) cw = a.w[tk.route[threadIdx.x]];
+    if (FMT == MOE_W_NVFP4) c2 = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob)[2];
+  }
+
+  // ---------------------------------------------------------------- phase A
+  // Items are (row, chunk) pairs, alternating between two register buffers;
+  // the next item of a buffer is requested as soon as its dot is done.  With
+  // one chunk per row (KC = 1) each buffer holds a whole row and the two rows
+  // are reduced together; with an even KC a row's chunks alternate buffers and
+  // it completes on the second buffer.
+  {
+    const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
+    auto xrow = [&](int it) {
+      const int t = (ra0 + it / KC) / I;
+      return xs4 + (size_t)(tk.route[t] / k) * (H / 8);
+    };
+    auto store_h = [&](int it, float gsum, float usum, float gs0, float gs1) {  // lane 0
+      const int r = ra0 + it / KC, t = r / I;
+      const float xi = xinv[tk.route[t] / k];
+      const float gg = gsum * xi * gs0, uu = usum * xi * gs1;
+      a.h[(size_t)tk.route[t] * I + (r - t * I)] = gg / (1.f + expf(-gg)) * uu;
+    };
+    float ga = 0.f, ua = 0.f, gb = 0.f, ub = 0.f;
+    for (int it = 0; it < nitA; it += 2) {
+      const bool two = it + 1 < nitA;
+      bufA.dot(xrow(it), it % KC, lane, ga, ua);
+      const float a0 = bufA.gs0, a1 = bufA.gs1;
+      if (it + 2 < nitA) item_load(bufA, it + 2);
+      float b0 = 1.f, b1 = 1.f;
+      if (two) {
+        bufB.dot(xrow(it + 1), (it + 1) % KC, lane, gb, ub);
+        b0 = bufB.gs0;
+        b1 = bufB.gs1;
+        if (it + 3 < nitA) item_load(bufB, it + 3);
+      }
+      if (KC == 1) {  // rows it and it + 1 complete
+        const float p[4] = {ga, ua, gb, ub};
+        const float v = reduce4(p, lane);
+        const float va = __shfl_sync(0xffffffffu, v, 8), vb = __shfl_sync(0xffffffffu, v, 16),
+                    vc = __shfl_sync(0xffffffffu, v, 24);
+        if (lane == 0) {
+          store_h(it, v, va, a0, a1);
+          if (two) store_h(it + 1, vb, vc, b0, b1);
+        }
+        ga = ua = gb = ub = 0.f;
+      } else if ((it + 1) % KC == KC - 1) {  // the row of items it, it + 1 completes
+        const float2 gu = reduce2(ga + gb, ua + ub, lane);
+        if (lane == 0) store_h(it + 1, gu.x, gu.y, b0, b1);
+        ga = ua = gb = ub = 0.f;
+      }
     }
   }
-  if (threadIdx.x < T) {
-    tk.gs[threadIdx.x][0] = cg0;
-    tk.gs[threadIdx.x][1] = cg1;
-    tk.gs[threadIdx.x][2] = cg2;
-    tk.wt[threadIdx.x] = cw;
-  }
-  consumers_sync();
   // the shared expert's sigmoid gate, sigmoid(x_b . w_g), in fp32
   if (SHARED && blockIdx.x == 0 && warp < n_rows) {
     float z = 0.f;
@@ -634,229 +665,141 @@ ffn_fused_kernel(DevState st, FusedArgs a) {
     z = wsum(z);
     if (lane == 0) a.gate[warp] = 1.f / (1.f + expf(-z));
   }
-
-  bool failed = false;  // a timed-out wait: keep taking part in the barriers, skip the work
-  int q = 0;
-  // ---------------------------------------------------------------- phase A
-  // items (slice sl of 1024, row r), row fastest, contiguous per warp
-  //   NVFP4: lane L takes elements [32L, 32L+32) of the slice (16 code bytes)
-  //   bf16:  lane L takes elements 8L + 256m + [0, 8), m = 0..3 (4 x 16 bytes)
-  {
-    uint4 xv[4];
-    int xkey = -1;
-    for (int u = u0; u < u1; ++q) {
-      const int t = u / I, n = u - t * I;
-      const int nr = min(rcA, min(u1 - u, I - n));
-      const int s = q % nstage;
-      if (!failed && !mbar_wait(&rg.full[s], (uint32_t)((q / nstage) & 1))) {
-        flag_timeout(a.status);
-        failed = true;
-      }
-      const int b = tk.route[t] / k;
-      const uint8_t* stg = ring + (size_t)s * a.stage_bytes;
-      float* rd = redA + (size_t)(q & 1) * 2 * redA_n;
-      const int items = nslA * nr;
-      const int ipw = (items + kSW - 1) / kSW;
-      const int i0 = min(items, warp * ipw), i1 = min(items, i0 + ipw);
-      int sl = i0 / nr, r = i0 - sl * nr;
-      for (int it = i0; it < i1 && !failed; ++it, (++r == nr ? (r = 0, ++sl) : 0)) {
-        if (sl * 16 + b != xkey) {  // this batch row's x slice into registers
-          const uint16_t* xr = xs + (size_t)b * H + sl * 1024;
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            xv[m] = FMT == MOE_W_NVFP4 ? reinterpret_cast<const uint4*>(xr + lane * 32)[m]
-                                       : *reinterpret_cast<const uint4*>(xr + lane * 8 + 256 * m);
-          xkey = sl * 16 + b;
-        }
-        float g = 0.f, up = 0.f;
-        if (FMT == MOE_W_NVFP4) {
-          const int e0 = sl * 1024 + lane * 32;
-          const uint4 cgw = *reinterpret_cast<const uint4*>(stg + (size_t)r * (H / 2) + e0 / 2);
-          const uint4 cuw = *reinterpret_cast<const uint4*>(stg + (size_t)(rcA + r) * (H / 2) + e0 / 2);
-          const uint8_t* sc = stg + (size_t)2 * rcA * (H / 2);
-          const float2 sg = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(sc + (size_t)r * (H / 16) + e0 / 16));
-          const float2 su =
-              e4m3x2_f32(*reinterpret_cast<const uint16_t*>(sc + (size_t)(rcA + r) * (H / 16) + e0 / 16));
-          g = fmaf(dot8_fp4_h(cgw.x, xv[0]) + dot8_fp4_h(cgw.y, xv[1]), sg.x, 0.f);
-          g = fmaf(dot8_fp4_h(cgw.z, xv[2]) + dot8_fp4_h(cgw.w, xv[3]), sg.y, g);
-          up = fmaf(dot8_fp4_h(cuw.x, xv[0]) + dot8_fp4_h(cuw.y, xv[1]), su.x, 0.f);
-          up = fmaf(dot8_fp4_h(cuw.z, xv[2]) + dot8_fp4_h(cuw.w, xv[3]), su.y, up);
-        } else {
-          const uint8_t* rowg = stg + (size_t)r * H * 2 + (size_t)sl * 2048;
-          const uint8_t* rowu = stg + (size_t)(rcA + r) * H * 2 + (size_t)sl * 2048;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            g = dot8_bf16_bf(*reinterpret_cast<const uint4*>(rowg + lane * 16 + 512 * m), xv[m], g);
-            up = dot8_bf16_bf(*reinterpret_cast<const uint4*>(rowu + lane * 16 + 512 * m), xv[m], up);
-          }
-        }
-        g = wsum(g);
-        up = wsum(up);
-        if (lane == 0) {
-          rd[it] = g;
-          rd[redA_n + it] = up;
-        }
-      }
-      consumers_sync();  // every item of the chunk done, stage no longer read
-      if (threadIdx.x == 0) mbar_arrive_one(&rg.empty[s]);
-      if (threadIdx.x < nr && !failed) {  // one thread per row: slices in a fixed order
-        const int rr = threadIdx.x;
-        float gs = 0.f, us = 0.f;
-        for (int z = 0; z < nslA; ++z) {
-          gs += rd[z * nr + rr];
-          us += rd[redA_n + z * nr + rr];
-        }
-        const float xi = FMT == MOE_W_NVFP4 ? xinv[b] : 1.f;
-        const float gg = gs * xi * tk.gs[t][0], uu = us * xi * tk.gs[t][1];
-        a.h[(size_t)tk.route[t] * I + n + rr] = gg / (1.f + expf(-gg)) * uu;
-      }
-      u += nr;  // rd is double-buffered: the next chunk writes the other half
-    }
-  }
+  if (threadIdx.x < T) tk.wt[threadIdx.x] = cw * c2;  // read after the barrier
 
   // ---------------------------------------------------------------- barrier
-  if (!grid_barrier(a.bar_ctr, a.status)) failed = true;
-  {  // every task's h into shared memory: float4 loads, four in flight per thread
-    const int n4 = T * I / 4, i4 = I / 4;
-    float4* hs4 = reinterpret_cast<float4*>(hsm);
-    const float4* h4 = reinterpret_cast<const float4*>(a.h);
-    for (int i0 = threadIdx.x; i0 < n4; i0 += 4 * kST) {
-      float4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int i = i0 + j * kST;
-        if (i < n4) v[j] = __ldcg(&h4[(size_t)tk.route[i / i4] * i4 + (i % i4)]);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (i0 + j * kST < n4) hs4[i0 + j * kST] = v[j];
+  const bool ok = grid_barrier(a.bar_ctr, a.status);
+  if (!ok) {  // timed out: nothing below is trustworthy
+    cp_async_wait_all();
+    return;
+  }
+  // h of the tasks this CTA's rows need, read once from L2 into shared memory
+  // (every warp reading it from L2 would hammer a few cache lines)
+  const int tlo = ru1 > ru0 ? ts[bA] : 0, thi = ru1 > ru0 ? ts[bB + 1] : 0;
+  {
+    float4* h4 = reinterpret_cast<float4*>(hsm);
+    const int n4 = (thi - tlo) * I / 4, i4 = I / 4;
+    for (int i = threadIdx.x; i < n4; i += kT) {
+      const int tt = tlo + i / i4;
+      h4[i] = __ldcg(reinterpret_cast<const float4*>(a.h + (size_t)tk.route[tt] * I) + (i % i4));
     }
   }
-  if (SHARED && threadIdx.x < n_rows) gate_s[threadIdx.x] = __ldcg(&a.gate[threadIdx.x]);
-  float ysv[kYsPre];  // the shared expert's output for this thread's combine rows
-#pragma unroll
-  for (int m = 0; m < kYsPre; ++m) {
-    const int ru = ru0 + threadIdx.x + m * kST;
-    ysv[m] = (!SHARED && a.ys && ru < ru1) ? a.ys[ru] : 0.f;
-  }
-  consumers_sync();
+  cp_async_wait_all();
+  __syncthreads();  // staged phase-B rows and h visible to every warp
 
   // ---------------------------------------------------------------- phase B
-  // items (task j, slice sl of 512, row r), row fastest, contiguous per warp
-  //   NVFP4: lane L takes elements [16L, 16L+16) of the slice (8 code bytes)
-  //   bf16:  lane L takes elements 8L + 256m + [0, 8), m = 0, 1 (2 x 16 bytes)
+  // warp w takes items [w*ipw, (w+1)*ipw), in runs of up to NG of one task
+  // (NG = 4 for NVFP4; 2 for bf16, whose rows hold twice the registers)
   {
-    float hv[16];
-    int hkey = -1;
-    Cur c;
-    for (bool more = start(c); more; more = advance(c), ++q) {
-      const int nr = min(rcB, b_hi(c.b) - c.n);
-      const int t1 = min(c.t0 + tpc, ts[c.b + 1]);
-      const int nt = t1 - c.t0;
-      const int s = q % nstage;
-      if (!failed && !mbar_wait(&rg.full[s], (uint32_t)((q / nstage) & 1))) {
-        flag_timeout(a.status);
-        failed = true;
-      }
-      const uint8_t* stg = ring + (size_t)s * a.stage_bytes;
-      float* rd = redB + (size_t)(q & 1) * redB_n;
-      const int items = nt * nslB * nr;
-      const int ipw = (items + kSW - 1) / kSW;
-      const int i0 = min(items, warp * ipw), i1 = min(items, i0 + ipw);
-      int r = i0 % nr, sl = (i0 / nr) % nslB, j = (i0 / nr) / nslB;
-      for (int it = i0; it < i1 && !failed;
-           ++it, (++r == nr ? (r = 0, (++sl == nslB ? (sl = 0, ++j) : 0)) : 0)) {
-        const int key = (c.t0 + j) * nslB + sl;
-        if (key != hkey) {  // task's h slice into registers
-          const float* hp = hsm + (size_t)(c.t0 + j) * I + sl * 512;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const float4 v = FMT == MOE_W_NVFP4
-                                 ? reinterpret_cast<const float4*>(hp + lane * 16)[m]
-                                 : *reinterpret_cast<const float4*>(hp + lane * 8 + 256 * (m >> 1) + 4 * (m & 1));
-            hv[4 * m] = v.x;
-            hv[4 * m + 1] = v.y;
-            hv[4 * m + 2] = v.z;
-            hv[4 * m + 3] = v.w;
-          }
-          hkey = key;
-        }
-        const uint8_t* tb = stg + (size_t)j * rcB * rowB;
-        float p;
+    constexpr int NG = FMT == MOE_W_NVFP4 ? 4 : 2;
+    const int ipw = (NQ + kW - 1) / kW;
+    const int q0w = min(NQ, warp * ipw), q1w = min(NQ, q0w + ipw);
+    float hv[32];
+    int ht = -1;
+    for (int q = q0w; q < q1w;) {
+      const int bi = q >= cntA ? 1 : 0;
+      const int b = bi ? bB : bA, qb = bi ? cntA : 0;
+      const int nlo = nlo_of(b), nlen = nlen_of(b);
+      const int t = ts[b] + (q - qb) / nlen;
+      const int n0 = nlo + (q - qb) % nlen;
+      const int run_end = min(q1w, qb + (t - ts[b] + 1) * nlen);  // same task
+      const int cnt = min(NG, run_end - q);
+      if (t != ht) {  // this task's h slice into registers
+        const float* hp = hsm + (size_t)(t - tlo) * I;
         if (FMT == MOE_W_NVFP4) {
-          const int e0 = sl * 512 + lane * 16;
-          const uint2 cw2 = *reinterpret_cast<const uint2*>(tb + (size_t)r * (I / 2) + e0 / 2);
-          const float qd = dot8_fp4_f(cw2.x, hv) + dot8_fp4_f(cw2.y, hv + 8);
-          p = qd * e4m3x2_f32(tb[(size_t)rcB * (I / 2) + (size_t)r * (I / 16) + e0 / 16]).x;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j < 4 * m) {
+              const float4 v = reinterpret_cast<const float4*>(hp + lane * 16 * m)[j];
+              hv[4 * j] = v.x, hv[4 * j + 1] = v.y, hv[4 * j + 2] = v.z, hv[4 * j + 3] = v.w;
+            }
         } else {
-          const uint8_t* row = tb + (size_t)r * I * 2 + (size_t)sl * 1024;
-          p = dot8_bf16_f(*reinterpret_cast<const uint4*>(row + lane * 16), hv, 0.f);
-          p = dot8_bf16_f(*reinterpret_cast<const uint4*>(row + lane * 16 + 512), hv + 8, p);
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            if (s < 2 * m) {
+              const float4 v0 = *reinterpret_cast<const float4*>(hp + 256 * s + 8 * lane);
+              const float4 v1 = *reinterpret_cast<const float4*>(hp + 256 * s + 8 * lane + 4);
+              hv[8 * s] = v0.x, hv[8 * s + 1] = v0.y, hv[8 * s + 2] = v0.z, hv[8 * s + 3] = v0.w;
+              hv[8 * s + 4] = v1.x, hv[8 * s + 5] = v1.y, hv[8 * s + 6] = v1.z, hv[8 * s + 7] = v1.w;
+            }
         }
-        p = wsum(p);
-        if (lane == 0) rd[it] = p;
+        ht = t;
       }
-      consumers_sync();  // stage no longer read; rd complete
-      if (threadIdx.x == 0) mbar_arrive_one(&rg.empty[s]);
-      if (threadIdx.x < nt * nr && !failed) {  // one thread per (task, row): slices in order
-        const int jj = threadIdx.x / nr, rr = threadIdx.x % nr;
-        float y = 0.f;
-        for (int z = 0; z < nslB; ++z) y += rd[(jj * nslB + z) * nr + rr];
-        ysm[(size_t)(c.t0 + jj) * perB + (c.b * H + c.n + rr - ru0)] = y;
+      ItemB<FMT> itm[NG];
+#pragma unroll
+      for (int j = 0; j < NG; ++j) {
+        if (j >= cnt) continue;
+        const int qq = q + j, n = n0 + j;
+        const uint8_t* cp;
+        const uint8_t* sp;
+        if (qq < qs) {
+          cp = stC + (size_t)qq * CB;
+          sp = stS + (size_t)qq * SB;
+        } else {
+          const uint8_t* blob = tk.blob[t];
+          cp = blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)n * CB;
+          sp = blob + o.scale[2] + (size_t)n * SB;
+        }
+        itemb_load<FMT>(itm[j], cp, sp, m, lane);
       }
+      float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NG; ++j) p[j] = j < cnt ? itemb_dot<FMT>(itm[j], hv, m) : 0.f;
+      const float v = reduce4(p, lane);
+      const int j = lane >> 3;
+      if ((lane & 7) == 0 && j < cnt)
+        ysm[(size_t)t * perB + (b * H + n0 + j - ru0)] = v;
+      q += cnt;
     }
   }
-  consumers_sync();  // every per-task row result in ysm
+  __syncthreads();  // every (task, row) result in ysm
   // combine: each output row, its tasks in route order (j ascending), then + ys
-  int m = 0;
-  for (int ru = ru0 + threadIdx.x; ru < ru1; ru += kST, ++m) {
-    const int b = ru / H, n = ru - b * H;
+  int mm = 0;
+  for (int ru = ru0 + threadIdx.x; ru < ru1; ru += kT, ++mm) {
+    const int b = ru / H;
     float acc = 0.f;
     for (int t = ts[b]; t < ts[b + 1]; ++t)
-      acc = fmaf(tk.wt[t] * tk.gs[t][2], ysm[(size_t)t * perB + (ru - ru0)], acc);
+      acc = fmaf(tk.wt[t], ysm[(size_t)t * perB + (ru - ru0)], acc);
     if (SHARED) {
-      a.ys[(size_t)b * H + n] = gate_s[b] * acc;
+      a.ys[ru] = __ldcg(&a.gate[b]) * acc;
     } else {
-      const float yv = m < kYsPre ? ysv[m] : (a.ys ? a.ys[ru] : 0.f);
-      a.out[(size_t)b * H + n] = __float2bfloat16_rn(a.ys ? acc + yv : acc);
+      const float yv = mm < kYsPre ? ysv[mm] : (a.ys ? a.ys[ru] : 0.f);
+      a.out[ru] = __float2bfloat16_rn(a.ys ? acc + yv : acc);
     }
   }
 }
 
 int g_num_sms = 0;
 constexpr size_t kBudget = 200 * 1024;
-constexpr int kStageCapA = 36 * 1024;
-constexpr int kStageCapB = 24 * 1024;
 
 size_t round128(size_t v) { return (v + 127) / 128 * 128; }
 
 struct Plan {
   size_t smem;
-  int nstage, stage_bytes, rcA, rcB, tpc;
+  int qs, htasks;
   bool ok;
 };
 
-Plan fused_plan(int wfmt, int H, int I, int n_rows, int T) {
+// Shared memory: x [n_rows][H] | ysm [T][perB] fp32 | h [htasks][I] fp32 |
+// staged phase-B rows.  A CTA's output rows span at most two batch rows, so
+// it needs the h of at most 2k tasks.
+Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T) {
   Plan p{};
-  const int rowA = wfmt == MOE_W_NVFP4 ? 2 * (H / 2 + H / 16) : 2 * H * 2;
-  const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
-  p.rcA = rows_per_chunk(rowA, kStageCapA);
-  p.rcB = rows_per_chunk(rowB, kStageCapB);
-  p.tpc = kStageCapB / (p.rcB * rowB);
-  p.tpc = p.tpc < 1 ? 1 : (p.tpc > 16 ? 16 : p.tpc);
-  const size_t sA = (size_t)p.rcA * rowA, sB = (size_t)p.tpc * p.rcB * rowB;
-  p.stage_bytes = (int)round128(sA > sB ? sA : sB);
   const int G = g_num_sms > 0 ? g_num_sms : 1;
   const int perB = (n_rows * H + G - 1) / G;
-  const size_t fixed = round128((size_t)n_rows * H * 2) +
-                       round128(((size_t)T * I + (size_t)T * perB + 4 * (size_t)(H / 1024) * p.rcA +
-                                 2 * (size_t)p.tpc * (I / 512) * p.rcB) * 4);
-  p.nstage = fixed < kBudget ? (int)((kBudget - fixed) / p.stage_bytes) : 0;
-  p.nstage = p.nstage > kMaxStages ? kMaxStages : p.nstage;
-  p.smem = fixed + (size_t)p.nstage * p.stage_bytes;
-  p.ok = p.nstage >= 1 && H % 1024 == 0 && H / 1024 <= kSW && I % 512 == 0 && I / 512 <= kSW &&
-         n_rows * H <= kXW * 8 * kST && p.tpc * p.rcB <= kST && (size_t)p.rcA * rowA <= (size_t)kStageCapA &&
-         (size_t)p.rcB * rowB <= (size_t)kStageCapB;
+  const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
+  p.htasks = std::min(T, 2 * k);
+  const size_t fixed = round128((size_t)n_rows * H * 2) + round128((size_t)T * perB * 4) +
+                       round128((size_t)p.htasks * I * 4);
+  const int nq = k * perB * 2;  // at most two batch rows of k tasks each
+  const size_t room = fixed < kBudget ? kBudget - fixed : 0;
+  p.qs = (int)std::min<size_t>((size_t)nq, room / rowB);
+  p.smem = fixed + (size_t)p.qs * rowB;
+  const int CW = wfmt == MOE_W_NVFP4 ? 2048 : 512;
+  const int KC = H / CW;
+  p.ok = fixed <= kBudget && H % CW == 0 && (KC == 1 || KC % 2 == 0) && I % 512 == 0 &&
+         I <= 1024 && perB <= H &&
+         n_rows * H <= kXW * 8 * kT;
   return p;
 }
 
@@ -865,7 +808,7 @@ cudaError_t launch_coop(K kernel, size_t smem, cudaStream_t s, const DevState& s
                         const FusedArgs& a) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(g_num_sms);
-  cfg.blockDim = dim3(kST + 32);
+  cfg.blockDim = dim3(kT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -879,12 +822,9 @@ cudaError_t launch_coop(K kernel, size_t smem, cudaStream_t s, const DevState& s
 cudaError_t launch_fused(const DevState& st, int wfmt, bool shared, const FusedArgs& a0,
                          cudaStream_t s) {
   FusedArgs a = a0;
-  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, a.R);
-  a.nstage = p.nstage;
-  a.stage_bytes = p.stage_bytes;
-  a.rcA = p.rcA;
-  a.rcB = p.rcB;
-  a.tpc = p.tpc;
+  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, a.k, a.R);
+  a.qs = p.qs;
+  a.htasks = p.htasks;
   if (wfmt == MOE_W_NVFP4)
     return shared ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, true>, p.smem, s, st, a)
                   : launch_coop(ffn_fused_kernel<MOE_W_NVFP4, false>, p.smem, s, st, a);
@@ -895,9 +835,9 @@ cudaError_t launch_fused(const DevState& st, int wfmt, bool shared, const FusedA
 }  // namespace
 
 bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks) {
-  if (g_num_sms <= 0 || n_tasks > kMaxTasks || n_rows > 16 || n_rows < 1) return false;
-  if (H % 256 || I % 256) return false;  // every bulk copy 16-byte aligned and sized
-  return fused_plan(wfmt, H, I, n_rows, n_tasks).ok;
+  if (g_num_sms <= 0 || n_tasks > kMaxTasks || n_rows > kMaxRows || n_rows < 1) return false;
+  const int k = (n_tasks + n_rows - 1) / n_rows;
+  return fused_plan(wfmt, H, I, n_rows, k, n_tasks).ok;
 }
 
 cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int max_tasks) {

@@ -18,7 +18,7 @@
 #include "common.cuh"
 
 namespace moe {
-cudaError_t admit_set_smem_limits(int E);
+cudaError_t admit_set_smem_limits(int E, int S);
 cudaError_t gemv_set_smem_limits(int H, int I, int Is, int k_max);
 }  // namespace moe
 
@@ -237,7 +237,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     if (e != cudaSuccess) return fail(cuda_fail(e, "host blob table"));
   }
 
-  e = moe::admit_set_smem_limits(d.n_experts);
+  e = moe::admit_set_smem_limits(d.n_experts, d.n_slots);
   if (e != cudaSuccess) return fail(cuda_fail(e, "admission shared memory"));
   if (compute) {
     // the down kernel stages k routes' intermediates in shared memory
