@@ -58,29 +58,58 @@ __device__ __forceinline__ unsigned long long now_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// 16 bytes global -> shared, asynchronous (completion by cp.async.wait_group)
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src)
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+// generic-proxy accesses of shared memory before async-proxy writes to it
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// read-only weight loads that should not displace anything in L1
-__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
 }
-__device__ __forceinline__ uint32_t ldg_stream4(const void* p) {
-  uint32_t v;
-  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-  return v;
+// L2 policy for weight bytes, which every layer reads once: evicted first, so
+// the streamed weights do not push the kernels' code, the cache state and the
+// activations out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// bulk copy global -> shared (16-byte aligned, size a multiple of 16),
+// completing `bytes` transactions on `bar`, with an L2 cache policy
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `bar` with the given parity; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  while (!mbar_test(bar, parity)) {
+    if (now_ns() - t0 > kWaitNs) return false;
+  }
+  return true;
 }
 
 // ------------------------------------------------------------ decode helpers
@@ -248,74 +277,88 @@ __device__ __forceinline__ float reduce4(const float p[4], int lane) {
   return v;
 }
 
-// ------------------------------------------------------------ phase A rows
-// One gate row and one up row (a chunk of CW elements of each), in registers.
-//   NVFP4 (CW = 2048): lane L holds elements [64L, 64L+64) of the chunk:
-//     32 code bytes and 4 e4m3 block scales per matrix.
-//   bf16  (CW = 512):  lane L holds elements 256s + 8L + [0, 8), s = 0..1.
+// ------------------------------------------------------------ phase A items
+// An item is one chunk of CW elements of one gate row and the same chunk of
+// the up row, brought into a per-warp shared-memory slot by bulk copies:
+//   NVFP4 (CW = 2048): gate codes [1024 B] | up codes [1024 B] | gate scales
+//     [128 B] | up scales [128 B] | the blob's 16-byte global-scale record;
+//     lane L decodes elements [32L, 32L+32) and [1024+32L, 1024+32L+32);
+//   bf16 (CW = 512): gate [1024 B] | up [1024 B]; lane L takes elements
+//     8L + [0, 8) and 256 + 8L + [0, 8).
+// Every lane reads 16 contiguous bytes per load at a 16-byte lane stride, so
+// the shared-memory reads are conflict-free.
 template <int FMT>
-struct RowA;
+struct ItemA;
 template <>
-struct RowA<MOE_W_NVFP4> {
+struct ItemA<MOE_W_NVFP4> {
   static constexpr int CW = 2048;
-  uint4 g0, g1, u0, u1;
-  uint32_t sg, su;
-  float gs0, gs1;  // the row's gate / up global scales (lane 0 only)
-  __device__ __forceinline__ void load(const uint8_t* blob, const BlobOff& o, int H, int i, int c,
-                                       int lane) {
-    if (lane == 0) {
-      gs0 = *reinterpret_cast<const float*>(blob + o.glob);
-      gs1 = *reinterpret_cast<const float*>(blob + o.glob + 4);
-    }
-    const size_t cr = (size_t)i * (H / 2) + c * 1024 + lane * 32;
-    const size_t sr = (size_t)i * (H / 16) + c * 128 + lane * 4;
-    g0 = ldg_stream16(blob + o.code[0] + cr);
-    g1 = ldg_stream16(blob + o.code[0] + cr + 16);
-    u0 = ldg_stream16(blob + o.code[1] + cr);
-    u1 = ldg_stream16(blob + o.code[1] + cr + 16);
-    sg = ldg_stream4(blob + o.scale[0] + sr);
-    su = ldg_stream4(blob + o.scale[1] + sr);
+  static constexpr int BYTES = 2 * 1024 + 2 * 128 + 16;
+  static __device__ __forceinline__ uint32_t issue(uint8_t* slot, const uint8_t* blob,
+                                                   const BlobOff& o, int H, int i, int c,
+                                                   uint64_t* bar, uint64_t pol) {
+    const size_t cr = (size_t)i * (H / 2) + c * 1024, sr = (size_t)i * (H / 16) + c * 128;
+    bulk_g2s(slot, blob + o.code[0] + cr, 1024, bar, pol);
+    bulk_g2s(slot + 1024, blob + o.code[1] + cr, 1024, bar, pol);
+    bulk_g2s(slot + 2048, blob + o.scale[0] + sr, 128, bar, pol);
+    bulk_g2s(slot + 2176, blob + o.scale[1] + sr, 128, bar, pol);
+    bulk_g2s(slot + 2304, blob + o.glob, 16, bar, pol);
+    return BYTES;
   }
-  // x row (16-byte units, swizzled) -> per-lane partial gate / up sums
-  __device__ __forceinline__ void dot(const uint4* xr, int c, int lane, float& g, float& u) const {
-    const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    const float2 sg01 = e4m3x2_f32(sg & 0xffffu), sg23 = e4m3x2_f32(sg >> 16);
-    const float2 su01 = e4m3x2_f32(su & 0xffffu), su23 = e4m3x2_f32(su >> 16);
-    const float sgv[4] = {sg01.x, sg01.y, sg23.x, sg23.y};
-    const float suv[4] = {su01.x, su01.y, su23.x, su23.y};
-    const int u0i = c * 256 + lane * 8;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 xa = xr[xswz(u0i + 2 * j)], xb = xr[xswz(u0i + 2 * j + 1)];
-      g = fmaf(dot8_fp4_h(gw[2 * j], xa) + dot8_fp4_h(gw[2 * j + 1], xb), sgv[j], g);
-      u = fmaf(dot8_fp4_h(uw[2 * j], xa) + dot8_fp4_h(uw[2 * j + 1], xb), suv[j], u);
-    }
+  // per-lane partial gate / up sums over the lane's elements of chunk c
+  static __device__ __forceinline__ void dot(const uint8_t* slot, const uint4* xr, int c, int lane,
+                                             float& g, float& u) {
+    const uint4 g0 = *reinterpret_cast<const uint4*>(slot + lane * 16);
+    const uint4 g1 = *reinterpret_cast<const uint4*>(slot + 512 + lane * 16);
+    const uint4 u0 = *reinterpret_cast<const uint4*>(slot + 1024 + lane * 16);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(slot + 1536 + lane * 16);
+    const float2 sg0 = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(slot + 2048 + lane * 2));
+    const float2 sg1 = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(slot + 2048 + 64 + lane * 2));
+    const float2 su0 = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(slot + 2176 + lane * 2));
+    const float2 su1 = e4m3x2_f32(*reinterpret_cast<const uint16_t*>(slot + 2176 + 64 + lane * 2));
+    const int ua = c * 256 + lane * 4, ub = ua + 128;
+    uint4 x0 = xr[xswz(ua)], x1 = xr[xswz(ua + 1)], x2 = xr[xswz(ua + 2)], x3 = xr[xswz(ua + 3)];
+    g = fmaf(dot8_fp4_h(g0.x, x0) + dot8_fp4_h(g0.y, x1), sg0.x, g);
+    g = fmaf(dot8_fp4_h(g0.z, x2) + dot8_fp4_h(g0.w, x3), sg0.y, g);
+    u = fmaf(dot8_fp4_h(u0.x, x0) + dot8_fp4_h(u0.y, x1), su0.x, u);
+    u = fmaf(dot8_fp4_h(u0.z, x2) + dot8_fp4_h(u0.w, x3), su0.y, u);
+    x0 = xr[xswz(ub)], x1 = xr[xswz(ub + 1)], x2 = xr[xswz(ub + 2)], x3 = xr[xswz(ub + 3)];
+    g = fmaf(dot8_fp4_h(g1.x, x0) + dot8_fp4_h(g1.y, x1), sg1.x, g);
+    g = fmaf(dot8_fp4_h(g1.z, x2) + dot8_fp4_h(g1.w, x3), sg1.y, g);
+    u = fmaf(dot8_fp4_h(u1.x, x0) + dot8_fp4_h(u1.y, x1), su1.x, u);
+    u = fmaf(dot8_fp4_h(u1.z, x2) + dot8_fp4_h(u1.w, x3), su1.y, u);
+  }
+  static __device__ __forceinline__ float gs0(const uint8_t* slot) {
+    return *reinterpret_cast<const float*>(slot + 2304);
+  }
+  static __device__ __forceinline__ float gs1(const uint8_t* slot) {
+    return *reinterpret_cast<const float*>(slot + 2308);
   }
 };
 template <>
-struct RowA<MOE_W_BF16> {
+struct ItemA<MOE_W_BF16> {
   static constexpr int CW = 512;
-  static constexpr float gs0 = 1.f, gs1 = 1.f;
-  uint4 g[2], u[2];
-  __device__ __forceinline__ void load(const uint8_t* blob, const BlobOff& o, int H, int i, int c,
-                                       int lane) {
-    const size_t e = (size_t)i * H + c * 512 + lane * 8;
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      g[s] = ldg_stream16(blob + o.mat[0] + (e + 256 * s) * 2);
-      u[s] = ldg_stream16(blob + o.mat[1] + (e + 256 * s) * 2);
-    }
+  static constexpr int BYTES = 2 * 1024;
+  static __device__ __forceinline__ uint32_t issue(uint8_t* slot, const uint8_t* blob,
+                                                   const BlobOff& o, int H, int i, int c,
+                                                   uint64_t* bar, uint64_t pol) {
+    const size_t e = ((size_t)i * H + c * 512) * 2;
+    bulk_g2s(slot, blob + o.mat[0] + e, 1024, bar, pol);
+    bulk_g2s(slot + 1024, blob + o.mat[1] + e, 1024, bar, pol);
+    return BYTES;
   }
-  __device__ __forceinline__ void dot(const uint4* xr, int c, int lane, float& gs, float& us) const {
+  static __device__ __forceinline__ void dot(const uint8_t* slot, const uint4* xr, int c, int lane,
+                                             float& gs, float& us) {
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const uint4 xv = xr[xswz(c * 64 + 32 * s + lane)];
-      gs = dot8_bf16_bf(g[s], xv, gs);
-      us = dot8_bf16_bf(u[s], xv, us);
+      gs = dot8_bf16_bf(*reinterpret_cast<const uint4*>(slot + 512 * s + lane * 16), xv, gs);
+      us = dot8_bf16_bf(*reinterpret_cast<const uint4*>(slot + 1024 + 512 * s + lane * 16), xv, us);
     }
   }
+  static __device__ __forceinline__ float gs0(const uint8_t*) { return 1.f; }
+  static __device__ __forceinline__ float gs1(const uint8_t*) { return 1.f; }
 };
+constexpr int kSlotBytes = 2432;  // >= ItemA<*>::BYTES, a multiple of 128
 
 // ------------------------------------------------------------ phase B items
 // One down row of one task: I = 512 m elements.
@@ -439,12 +482,14 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   __shared__ int ts[kMaxRows + 1];         // tasks of batch row b: [ts[b], ts[b+1])
   __shared__ unsigned int xmax[kMaxRows];  // per row max |x| (float bits, only when > 2^14)
   __shared__ float xinv[kMaxRows];         // per row 1 / (power-of-two scale applied to x)
+  __shared__ uint64_t bar_a[kW][2];        // per-warp phase-A slot barriers
+  __shared__ uint64_t bar_b;               // the staged phase-B rows
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, I = a.I, k = a.k, n_rows = a.n_rows;
   const int m = I / 512;                                   // 16-element groups per lane (B)
   const int CB = FMT == MOE_W_NVFP4 ? I / 2 : I * 2;       // down row: code bytes
   const int SB = FMT == MOE_W_NVFP4 ? I / 16 : 0;          // down row: scale bytes
-  constexpr int CW = RowA<FMT>::CW;
+  constexpr int CW = ItemA<FMT>::CW;
   const int KC = H / CW;                                   // phase-A chunks per row
   const BlobOff o(H, I);
 
@@ -524,12 +569,6 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const int perA = (NA + Gw - 1) / Gw;
   const int ra0 = min(NA, gw * perA), ra1 = min(NA, ra0 + perA);
   const int nitA = (ra1 - ra0) * KC;
-  RowA<FMT> bufA, bufB;
-  auto item_load = [&](RowA<FMT>& buf, int it) {
-    const int r = ra0 + it / KC, c = it % KC;
-    const int t = r / I;
-    buf.load(tk.blob[t], o, H, r - t * I, c, lane);
-  };
   // ---- phase-B items of this CTA (staged into shared memory after (2))
   const int bA = ru0 / H, bB = ru1 > ru0 ? (ru1 - 1) / H : bA;
   auto nlo_of = [&](int b) { return max(ru0 - b * H, 0); };
@@ -541,7 +580,9 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   float* ysm = reinterpret_cast<float*>(sm + ((size_t)n_rows * H * 2 + 127) / 128 * 128);
   float* hsm = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ysm) +
                                         ((size_t)a.R * perB * 4 + 127) / 128 * 128);
-  uint8_t* stC = reinterpret_cast<uint8_t*>(hsm) + ((size_t)a.htasks * I * 4 + 127) / 128 * 128;
+  uint8_t* ringA = reinterpret_cast<uint8_t*>(hsm) + ((size_t)a.htasks * I * 4 + 127) / 128 * 128;
+  uint8_t* slots = ringA + (size_t)warp * 2 * kSlotBytes;  // this warp's two slots
+  uint8_t* stC = ringA + (size_t)kW * 2 * kSlotBytes;
   uint8_t* stS = stC + (size_t)a.qs * CB;
   const int qs = min(a.qs, NQ);
 
@@ -569,35 +610,62 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   if (threadIdx.x < n_rows) {
     xinv[threadIdx.x] = FMT == MOE_W_NVFP4 ? 1.f / x_scale(__uint_as_float(xmax[threadIdx.x])) : 1.f;
   }
-  __syncthreads();  // (2) x
+  if (lane == 0) {
+    mbar_init(&bar_a[warp][0], 1);
+    mbar_init(&bar_a[warp][1], 1);
+    if (warp == 0) mbar_init(&bar_b, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();  // (2) x, barriers
 
-  // ---- every byte this CTA needs is requested now: its phase-A rows (the
-  // first two into registers), its phase-B rows (cp.async into shared memory)
-  // and the per-task combine factors.  No CTA-wide barrier follows until the
-  // grid barrier, so each warp computes as soon as its own rows land.
-  if (nitA > 0) item_load(bufA, 0);
-  if (nitA > 1) item_load(bufB, 1);
-  {
-    for (int bi = 0; bi < 2; ++bi) {
+  // ---- every byte this CTA needs is requested now: each warp's first two
+  // phase-A items (bulk copies into its two slots) and the CTA's phase-B rows
+  // (bulk copies into the staging area, on one barrier).  No CTA-wide barrier
+  // follows until the grid barrier, so each warp computes as soon as its own
+  // rows land.
+  const uint64_t pol = l2_evict_first();
+  auto issue_a = [&](int it) {  // lane 0
+    const int r = ra0 + it / KC, c = it % KC, t = r / I, sl = it & 1;
+    const uint32_t bytes = ItemA<FMT>::BYTES;
+    mbar_expect_tx(&bar_a[warp][sl], bytes);
+    ItemA<FMT>::issue(slots + sl * kSlotBytes, tk.blob[t], o, H, r - t * I, c, &bar_a[warp][sl],
+                      pol);
+  };
+  if (lane == 0) {
+    if (nitA > 0) issue_a(0);
+    if (nitA > 1) issue_a(1);
+  }
+  if (warp == kW - 1) {  // phase-B staging: one lane per (batch row, task) block
+    const int nblk = (ru1 > ru0) ? (ts[bA + 1] - ts[bA]) + (bB != bA ? ts[bB + 1] - ts[bB] : 0) : 0;
+    uint32_t mine = 0;
+    for (int j = lane; j < nblk; j += 32) {
+      const int bi = j < ts[bA + 1] - ts[bA] ? 0 : 1;
       const int b = bi ? bB : bA;
-      if ((bi ? cntB : cntA) == 0) continue;
-      const int nlo = nlo_of(b), nlen = nlen_of(b), qb = bi ? cntA : 0;
-      for (int t = ts[b]; t < ts[b + 1]; ++t) {
-        const int q0 = qb + (t - ts[b]) * nlen;
-        const int cnt = min(nlen, qs - q0);
-        if (cnt <= 0) break;
-        const uint8_t* blob = tk.blob[t];
-        const uint8_t* srcC = blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB;
-        for (int off = threadIdx.x * 16; off < cnt * CB; off += kT * 16)
-          cp_async16(stC + (size_t)q0 * CB + off, srcC + off);
-        if (FMT == MOE_W_NVFP4) {
-          const uint8_t* srcS = blob + o.scale[2] + (size_t)nlo * SB;
-          for (int off = threadIdx.x * 16; off < cnt * SB; off += kT * 16)
-            cp_async16(stS + (size_t)q0 * SB + off, srcS + off);
-        }
-      }
+      const int t = ts[b] + (bi ? j - (ts[bA + 1] - ts[bA]) : j);
+      const int nlen = nlen_of(b), q0 = (bi ? cntA : 0) + (t - ts[b]) * nlen;
+      const int cnt = min(nlen, qs - q0);
+      if (cnt > 0) mine += (uint32_t)cnt * (CB + SB);
     }
-    cp_async_commit();
+    uint32_t total = mine;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) total += __shfl_xor_sync(0xffffffffu, total, off);
+    if (lane == 0) mbar_expect_tx(&bar_b, total);  // before any of the copies can land
+    __syncwarp();
+    for (int j = lane; j < nblk; j += 32) {
+      const int bi = j < ts[bA + 1] - ts[bA] ? 0 : 1;
+      const int b = bi ? bB : bA;
+      const int t = ts[b] + (bi ? j - (ts[bA + 1] - ts[bA]) : j);
+      const int nlo = nlo_of(b), nlen = nlen_of(b), q0 = (bi ? cntA : 0) + (t - ts[b]) * nlen;
+      const int cnt = min(nlen, qs - q0);
+      if (cnt <= 0) continue;
+      const uint8_t* blob = tk.blob[t];
+      bulk_g2s(stC + (size_t)q0 * CB,
+               blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB,
+               (uint32_t)cnt * CB, &bar_b, pol);
+      if (FMT == MOE_W_NVFP4)
+        bulk_g2s(stS + (size_t)q0 * SB, blob + o.scale[2] + (size_t)nlo * SB, (uint32_t)cnt * SB,
+                 &bar_b, pol);
+    }
   }
   // per-task combine factor (stored to shared memory before the grid barrier)
   float cw = 1.f, c2 = 1.f;
@@ -606,7 +674,22 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     if (FMT == MOE_W_NVFP4) c2 = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob)[2];
   }
 
+  // the shared expert's sigmoid gate, sigmoid(x_b . w_g), in fp32, by the last
+  // CTA (the one least likely to hold phase-A rows), before its phase A
+  if (SHARED && blockIdx.x == gridDim.x - 1 && warp < n_rows) {
+    float z = 0.f;
+    for (int i0 = lane * 8; i0 < H; i0 += 256) {
+      const uint4 gv = *reinterpret_cast<const uint4*>(a.gate_w + i0);
+      const uint4 xv = *reinterpret_cast<const uint4*>(a.x + (size_t)warp * H + i0);
+      z = dot8_bf16_bf(gv, xv, z);
+    }
+    z = wsum(z);
+    if (lane == 0) a.gate[warp] = 1.f / (1.f + expf(-z));
+  }
+
   // ---------------------------------------------------------------- phase A
+  bool failed = false;                          // a timed-out wait: skip the rest
+  int issued = min(nitA, 2), consumed = 0;      // this warp's phase-A items
   // Items are (row, chunk) pairs, alternating between two register buffers;
   // the next item of a buffer is requested as soon as its dot is done.  With
   // one chunk per row (KC = 1) each buffer holds a whole row and the two rows
@@ -625,17 +708,46 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       a.h[(size_t)tk.route[t] * I + (r - t * I)] = gg / (1.f + expf(-gg)) * uu;
     };
     float ga = 0.f, ua = 0.f, gb = 0.f, ub = 0.f;
-    for (int it = 0; it < nitA; it += 2) {
+    auto wait_a = [&](int it) -> bool {  // item `it` landed in its slot (warp-uniform)
+      const bool all =
+          __all_sync(0xffffffffu, mbar_wait(&bar_a[warp][it & 1], (uint32_t)((it >> 1) & 1)));
+      if (all) {
+        consumed = it + 1;
+      } else {
+        failed = true;
+        if (lane == 0) flag_timeout(a.status);
+      }
+      return all;
+    };
+    for (int it = 0; it < nitA && !failed; it += 2) {
       const bool two = it + 1 < nitA;
-      bufA.dot(xrow(it), it % KC, lane, ga, ua);
-      const float a0 = bufA.gs0, a1 = bufA.gs1;
-      if (it + 2 < nitA) item_load(bufA, it + 2);
+      if (!wait_a(it)) break;
+      const uint8_t* sa = slots;
+      ItemA<FMT>::dot(sa, xrow(it), it % KC, lane, ga, ua);
+      const float a0 = ItemA<FMT>::gs0(sa), a1 = ItemA<FMT>::gs1(sa);
+      __syncwarp();  // slot 0 read by every lane
+      if (it + 2 < nitA) {
+        if (lane == 0) {
+          fence_proxy_async();
+          issue_a(it + 2);
+        }
+        issued = it + 3;
+      }
       float b0 = 1.f, b1 = 1.f;
       if (two) {
-        bufB.dot(xrow(it + 1), (it + 1) % KC, lane, gb, ub);
-        b0 = bufB.gs0;
-        b1 = bufB.gs1;
-        if (it + 3 < nitA) item_load(bufB, it + 3);
+        if (!wait_a(it + 1)) break;
+        const uint8_t* sb = slots + kSlotBytes;
+        ItemA<FMT>::dot(sb, xrow(it + 1), (it + 1) % KC, lane, gb, ub);
+        b0 = ItemA<FMT>::gs0(sb);
+        b1 = ItemA<FMT>::gs1(sb);
+        __syncwarp();
+        if (it + 3 < nitA) {
+          if (lane == 0) {
+            fence_proxy_async();
+            issue_a(it + 3);
+          }
+          issued = it + 4;
+        }
       }
       if (KC == 1) {  // rows it and it + 1 complete
         const float p[4] = {ga, ua, gb, ub};
@@ -653,26 +765,21 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
         ga = ua = gb = ub = 0.f;
       }
     }
-  }
-  // the shared expert's sigmoid gate, sigmoid(x_b . w_g), in fp32
-  if (SHARED && blockIdx.x == 0 && warp < n_rows) {
-    float z = 0.f;
-    for (int i0 = lane * 8; i0 < H; i0 += 256) {
-      const uint4 gv = *reinterpret_cast<const uint4*>(a.gate_w + i0);
-      const uint4 xv = *reinterpret_cast<const uint4*>(a.x + (size_t)warp * H + i0);
-      z = dot8_bf16_bf(gv, xv, z);
-    }
-    z = wsum(z);
-    if (lane == 0) a.gate[warp] = 1.f / (1.f + expf(-z));
+    // after a timeout, wait (bounded) for this warp's copies still in flight
+    if (failed && lane == 0)
+      for (int q = consumed; q < issued; ++q) mbar_wait(&bar_a[warp][q & 1], (uint32_t)((q >> 1) & 1));
   }
   if (threadIdx.x < T) tk.wt[threadIdx.x] = cw * c2;  // read after the barrier
 
   // ---------------------------------------------------------------- barrier
   const bool ok = grid_barrier(a.bar_ctr, a.status);
-  if (!ok) {  // timed out: nothing below is trustworthy
-    cp_async_wait_all();
-    return;
-  }
+  const bool staged = mbar_wait(&bar_b, 0);  // the staged phase-B rows (bounded)
+  if (!staged) flag_timeout(a.status);
+  if (!ok || !__syncthreads_and(staged)) return;  // timed out: nothing below is trustworthy
+  // the gate of this thread's combine row, requested now (written before the barrier)
+  const float gate_b = (SHARED && ru0 + (int)threadIdx.x < ru1)
+                           ? __ldcg(&a.gate[(ru0 + (int)threadIdx.x) / H])
+                           : 0.f;
   // h of the tasks this CTA's rows need, read once from L2 into shared memory
   // (every warp reading it from L2 would hammer a few cache lines)
   const int tlo = ru1 > ru0 ? ts[bA] : 0, thi = ru1 > ru0 ? ts[bB + 1] : 0;
@@ -684,8 +791,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       h4[i] = __ldcg(reinterpret_cast<const float4*>(a.h + (size_t)tk.route[tt] * I) + (i % i4));
     }
   }
-  cp_async_wait_all();
-  __syncthreads();  // staged phase-B rows and h visible to every warp
+  __syncthreads();  // h visible to every warp
 
   // ---------------------------------------------------------------- phase B
   // warp w takes items [w*ipw, (w+1)*ipw), in runs of up to NG of one task
@@ -761,7 +867,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     for (int t = ts[b]; t < ts[b + 1]; ++t)
       acc = fmaf(tk.wt[t], ysm[(size_t)t * perB + (ru - ru0)], acc);
     if (SHARED) {
-      a.ys[ru] = __ldcg(&a.gate[b]) * acc;
+      a.ys[ru] = (mm == 0 ? gate_b : __ldcg(&a.gate[b])) * acc;
     } else {
       const float yv = mm < kYsPre ? ysv[mm] : (a.ys ? a.ys[ru] : 0.f);
       a.out[ru] = __float2bfloat16_rn(a.ys ? acc + yv : acc);
@@ -781,7 +887,7 @@ struct Plan {
 };
 
 // Shared memory: x [n_rows][H] | ysm [T][perB] fp32 | h [htasks][I] fp32 |
-// staged phase-B rows.  A CTA's output rows span at most two batch rows, so
+// two phase-A slots per warp | staged phase-B rows.  A CTA's output rows span at most two batch rows, so
 // it needs the h of at most 2k tasks.
 Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T) {
   Plan p{};
@@ -790,7 +896,7 @@ Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T) {
   const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
   p.htasks = std::min(T, 2 * k);
   const size_t fixed = round128((size_t)n_rows * H * 2) + round128((size_t)T * perB * 4) +
-                       round128((size_t)p.htasks * I * 4);
+                       round128((size_t)p.htasks * I * 4) + (size_t)kW * 2 * kSlotBytes;
   const int nq = k * perB * 2;  // at most two batch rows of k tasks each
   const size_t room = fixed < kBudget ? kBudget - fixed : 0;
   p.qs = (int)std::min<size_t>((size_t)nq, room / rowB);
