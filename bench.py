@@ -392,6 +392,72 @@ def admission_sweep(dev: int) -> dict:
     return res
 
 
+def wide_step(dev: int, reps: int = 5) -> dict:
+    """The wide decode step: 600 rows x top-2 = 1,200 routes over 1,024 NVFP4
+    experts (H 2048, I 768) with a 1,100-slot cache, 30% of the experts
+    pre-resident.  The first step admits ~495 misses; its admission, gather and
+    routed FFNs + combine are timed with CUDA events on one stream.  The FFN is
+    then re-timed `reps` times on the resident slots (the same step again: all
+    hits), which is the grouped-FFN figure.  Algorithmic bytes of the FFN: the
+    distinct resident experts' blobs plus activations."""
+    import torch
+
+    import expert_slot_cache_lru_gb300 as m
+    import synth
+    w = synth.workloads()["wide_decode"]
+    blobs = synth.HostBlobs(w, pinned=True)
+    storage = torch.empty(w.n_slots * blobs.stride, dtype=torch.uint8, device="cuda")
+    cache = m.SlotCache(n_layers=1, n_experts=w.n_experts, n_slots=w.n_slots,
+                        pool_mode=m.MOE_POOL_SHARED, hidden=w.hidden, inter=w.inter, wfmt=w.fmt,
+                        shared_inter=0, slot_storage=storage, slot_stride=blobs.stride,
+                        host_blob_ptrs=blobs.addrs(), max_routes=w.routes, max_rows=w.batch)
+    pre = synth.prefill_ids(w)
+    m.moe_cache_prefill(cache.handle, 0, pre, len(pre))
+    ids, wts = synth.make_routing(w, steps=1)
+    d_ids = torch.from_numpy(ids[0, 0].ravel().copy()).cuda()
+    d_w = torch.from_numpy(wts[0, 0].ravel().copy()).cuda()
+    d_x = torch.from_numpy(synth.make_hidden(w, 0)[0].view(np.int16)).cuda()
+    d_slots = torch.empty_like(d_ids)
+    out = torch.empty(w.batch, w.hidden, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    R = w.routes
+    with torch.cuda.stream(s):
+        ev[0].record(s)
+        m.moe_admit(cache.handle, 0, d_ids, d_slots, R, -1, s)
+        ev[1].record(s)
+        m.moe_gather_missing(cache.handle, m.MOE_PLAN_DEMAND, s)
+        ev[2].record(s)
+        m.moe_routed_experts(cache.handle, 0, d_x, d_slots, d_w, w.batch, w.top_k, None, None,
+                             out, s)
+        ev[3].record(s)
+    s.synchronize()
+    st = cache.stats(0)
+    t_adm, t_gat, t_ffn = (ev[i].elapsed_time(ev[i + 1]) for i in range(3))
+    slots = d_slots.cpu().numpy()
+    distinct = len(set(int(v) for v in slots if v >= 0))
+    ffn_bytes = distinct * w.blob_bytes + w.batch * w.hidden * 2 * 2 + R * 8
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            m.moe_routed_experts(cache.handle, 0, d_x, d_slots, d_w, w.batch, w.top_k, None, None,
+                                 out, s)
+            e1.record(s)
+        s.synchronize()
+        times.append(e0.elapsed_time(e1))
+    t_ffn_hot = statistics.median(times)
+    cache.close()
+    return {"routes": R, "distinct_experts": distinct, "misses": int(st["misses"]),
+            "admission_us": round(t_adm * 1e3, 2),
+            "gather_ms": round(t_gat, 3),
+            "gather_gbs": round(st["fetched"] * w.blob_bytes / (t_gat * 1e-3) / 1e9, 1),
+            "ffn_ms_first": round(t_ffn, 3), "ffn_ms": round(t_ffn_hot, 3),
+            "ffn_bytes": ffn_bytes, "ffn_gbs": round(ffn_bytes / (t_ffn_hot * 1e-3) / 1e9, 1),
+            "step_ms": round(t_adm + t_gat + t_ffn, 3)}
+
+
 def cpu_baseline(seconds: float = 15.0) -> dict:
     """The oracle as it stands, single-threaded on this host: admission plus
     fp64 layer math for as many layers of the benchmark's tokens as fit in
@@ -506,6 +572,7 @@ def run_native(args) -> None:
     roof = dec.routed_gemv_roofline(steps=8)
     gather = dec.gather_bandwidth()
     adm = admission_sweep(local)
+    wide = wide_step(local)
     hbm = peaks.get("hbm_gbs", 6800.0)
     line = {
         "metric": METRIC,
@@ -537,6 +604,7 @@ def run_native(args) -> None:
                      "bytes_per_launch": round(roof["bytes_per_launch"]),
                      "peak_source": f"{peaks['_source']} (MEASURED_PEAKS.json hbm_gbs)"},
         "admission_us_per_layer": adm,
+        "wide_decode_step": wide,
         "gather": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in gather.items()},
         "setup_s": {k: round(v, 1) for k, v in dec.setup_s.items()},
         "clocks": sampler.summary(),

@@ -148,6 +148,9 @@ struct FfnScratch {
   float* gate;      // [max_rows] sigmoid gate of the shared expert
   float* ys;        // [max_rows * H] shared expert output (gated)
   unsigned long long* bar;  // grid-barrier counter of the fused FFN kernel (only grows)
+  uint16_t* x16;    // [max_rows * H] x prepared for the grouped kernels
+  float* xinv;      // [max_rows] inverse of the per-row x scale
+  float* y;         // [max_routes * H] per-route down projections (grouped path)
 };
 
 cudaError_t launch_shared_expert(int wfmt, int H, int Is, const void* x, int n_rows,
@@ -171,6 +174,14 @@ cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int
                                  const void* x, const int32_t* slot_ids, const float* w,
                                  int n_rows, int k, const float* shared_y, void* out,
                                  FfnScratch sc, unsigned long long* status, cudaStream_t s);
+
+// Routed FFNs for wide steps, grouped by expert (grouped.cu).
+bool grouped_supported(int wfmt, int H, int I, int E);
+cudaError_t grouped_init(int E);
+cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, int layer,
+                                  const void* x, const int32_t* slot_ids, const float* w,
+                                  int n_rows, int k, const float* shared_y, void* out,
+                                  FfnScratch sc, int max_routes, cudaStream_t s);
 
 // Allocation-free routed FFN (ffn_stream.cu): the scratch is a file-scope
 // device array whose address noalloc_scratch looks up once per device.

@@ -165,6 +165,9 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_hs = cv.take<float>((size_t)d.max_rows * std::max(Is, 1)),
                o_gate = cv.take<float>(d.max_rows),
                o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1)),
+               o_x16 = cv.take<uint16_t>((size_t)d.max_rows * std::max(H, 1)),
+               o_xinv = cv.take<float>(d.max_rows),
+               o_y = cv.take<float>((size_t)d.max_routes * std::max(H, 1)),
                o_status = cv.take<unsigned long long>(1),
                o_bar = cv.take<unsigned long long>(1);
   c->mem_bytes = align_up(cv.off, 256);
@@ -206,6 +209,9 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.gate = reinterpret_cast<float*>(m + o_gate);
   c->sc.ys = reinterpret_cast<float*>(m + o_ys);
   c->sc.bar = reinterpret_cast<unsigned long long*>(m + o_bar);
+  c->sc.x16 = reinterpret_cast<uint16_t*>(m + o_x16);
+  c->sc.xinv = reinterpret_cast<float*>(m + o_xinv);
+  c->sc.y = reinterpret_cast<float*>(m + o_y);
 
   // initial state: nothing resident, every clock at 1
   e = cudaMemset(c->mem, 0, c->mem_bytes);
@@ -244,6 +250,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     c->down_k_max = (int)std::min<size_t>(d.max_routes, (200 * 1024) / ((size_t)I * 4));
     e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
     if (e == cudaSuccess) e = moe::ffn_stream_init(d.wfmt, H, I, Is, d.max_rows, d.max_routes);
+    if (e == cudaSuccess && moe::grouped_supported(d.wfmt, H, I, d.n_experts))
+      e = moe::grouped_init(d.n_experts);
     if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
   }
   e = cudaEventCreateWithFlags(&c->ev_ready, cudaEventDisableTiming);
@@ -384,6 +392,12 @@ static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* s
   if (c->stream_ffn && moe::ffn_stream_supported(d.wfmt, d.hidden, d.inter, n_rows, n_rows * k)) {
     CK(moe::launch_routed_stream(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w, n_rows,
                                  k, with_shared ? c->sc.ys : nullptr, d_out, c->sc, c->st.status, s));
+    return MOE_OK;
+  }
+  if (k > 0 && moe::grouped_supported(d.wfmt, d.hidden, d.inter, d.n_experts)) {
+    CK(moe::launch_routed_grouped(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w,
+                                  n_rows, k, with_shared ? c->sc.ys : nullptr, d_out, c->sc,
+                                  d.max_routes, s));
     return MOE_OK;
   }
   if (k > 0)

@@ -85,7 +85,9 @@
  *   of layer l's prefetch may still read its plan while layer l+1's prefetch
  *   (for l+2) is admitted; moe_gather_missing / moe_rollback_plan with
  *   MOE_PLAN_PREFETCH use the plan of the most recent prefetch call.
- * Route groups (device, int32, written by moe_routed_experts when n_rows > 1):
+ * Route groups (device, int32, written by moe_routed_experts on the grouped
+ * path, i.e. for steps wider than the streaming kernel takes: more than 16
+ * rows or 64 routes):
  *   [G, slot[max_routes], start[max_routes + 1], route[max_routes]]: group g
  *   is the g-th distinct resident expert in ascending id, its slot, and its
  *   routes route[start[g] .. start[g+1]) in ascending route index.
