@@ -177,7 +177,7 @@ cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int
 
 // Routed FFNs for wide steps, grouped by expert (grouped.cu).
 bool grouped_supported(int wfmt, int H, int I, int E);
-cudaError_t grouped_init(int E);
+cudaError_t grouped_init(int E, int H, int I);
 cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, int layer,
                                   const void* x, const int32_t* slot_ids, const float* w,
                                   int n_rows, int k, const float* shared_y, void* out,

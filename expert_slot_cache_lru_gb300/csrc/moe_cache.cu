@@ -251,7 +251,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
     if (e == cudaSuccess) e = moe::ffn_stream_init(d.wfmt, H, I, Is, d.max_rows, d.max_routes);
     if (e == cudaSuccess && moe::grouped_supported(d.wfmt, H, I, d.n_experts))
-      e = moe::grouped_init(d.n_experts);
+      e = moe::grouped_init(d.n_experts, H, I);
     if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
   }
   e = cudaEventCreateWithFlags(&c->ev_ready, cudaEventDisableTiming);
