@@ -275,11 +275,18 @@ __global__ void __launch_bounds__(kWT) gup_kernel(DevState st, int H, int I, int
         const uint8_t* uc = blob + o.code[1] + (size_t)ii * (H / 2);
         const uint8_t* gsc = blob + o.scale[0] + (size_t)ii * (H / 16);
         const uint8_t* usc = blob + o.scale[1] + (size_t)ii * (H / 16);
-        for (int blk = 0; blk < H / 16; blk += 2) {  // two 16-element blocks per step
-          const uint4 gw = *reinterpret_cast<const uint4*>(gc + blk * 8);
-          const uint4 uw = *reinterpret_cast<const uint4*>(uc + blk * 8);
-          const float2 sg = e4m3x2(*reinterpret_cast<const uint16_t*>(gsc + blk));
-          const float2 su = e4m3x2(*reinterpret_cast<const uint16_t*>(usc + blk));
+        // two 16-element blocks per step; the next step's words are in flight
+        uint4 gwn = *reinterpret_cast<const uint4*>(gc), uwn = *reinterpret_cast<const uint4*>(uc);
+        uint32_t sgn = *reinterpret_cast<const uint16_t*>(gsc), sun = *reinterpret_cast<const uint16_t*>(usc);
+        for (int blk = 0; blk < H / 16; blk += 2) {
+          const uint4 gw = gwn, uw = uwn;
+          const float2 sg = e4m3x2(sgn), su = e4m3x2(sun);
+          if (blk + 2 < H / 16) {
+            gwn = *reinterpret_cast<const uint4*>(gc + (blk + 2) * 8);
+            uwn = *reinterpret_cast<const uint4*>(uc + (blk + 2) * 8);
+            sgn = *reinterpret_cast<const uint16_t*>(gsc + blk + 2);
+            sun = *reinterpret_cast<const uint16_t*>(usc + blk + 2);
+          }
           const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w}, uv[4] = {uw.x, uw.y, uw.z, uw.w};
           uint32_t gd[16], ud[16];
 #pragma unroll
@@ -376,9 +383,16 @@ __global__ void __launch_bounds__(kWT) gdown_kernel(DevState st, int H, int I, i
       if (FMT == MOE_W_NVFP4) {
         const uint8_t* dc = blob + o.code[2] + (size_t)nn * (I / 2);
         const uint8_t* ds = blob + o.scale[2] + (size_t)nn * (I / 16);
-        for (int blk = 0; blk < I / 16; blk += 2) {  // two blocks per step
-          const uint4 cw = *reinterpret_cast<const uint4*>(dc + blk * 8);
-          const float2 sc = e4m3x2(*reinterpret_cast<const uint16_t*>(ds + blk));
+        // two blocks per step; the next step's words are in flight
+        uint4 cwn = *reinterpret_cast<const uint4*>(dc);
+        uint32_t scn = *reinterpret_cast<const uint16_t*>(ds);
+        for (int blk = 0; blk < I / 16; blk += 2) {
+          const uint4 cw = cwn;
+          const float2 sc = e4m3x2(scn);
+          if (blk + 2 < I / 16) {
+            cwn = *reinterpret_cast<const uint4*>(dc + (blk + 2) * 8);
+            scn = *reinterpret_cast<const uint16_t*>(ds + blk + 2);
+          }
           const uint32_t ww[4] = {cw.x, cw.y, cw.z, cw.w};
           float wf[32];
 #pragma unroll
@@ -459,6 +473,7 @@ __global__ void __launch_bounds__(kWT) gcombine_kernel(const DevState st, int H,
 }
 
 int g_sms = 0;
+int g_occ[2][2] = {{1, 1}, {1, 1}};  // resident CTAs per SM: [format][gate-up, down]
 
 }  // namespace
 
@@ -484,6 +499,15 @@ cudaError_t grouped_init(int E, int H, int I) {
   lim(gup_kernel<MOE_W_BF16>, (size_t)kNR * H * 2);
   lim(gdown_kernel<MOE_W_NVFP4>, (size_t)kNR * I * 4);
   lim(gdown_kernel<MOE_W_BF16>, (size_t)kNR * I * 4);
+  // persistent grids: as many CTAs as fit on the GPU at once
+  auto occ = [&](auto kern, size_t bytes, int* out) {
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, kWT, bytes);
+    if (*out < 1) *out = 1;
+  };
+  occ(gup_kernel<MOE_W_BF16>, (size_t)kNR * H * 2, &g_occ[MOE_W_BF16][0]);
+  occ(gup_kernel<MOE_W_NVFP4>, (size_t)kNR * H * 2, &g_occ[MOE_W_NVFP4][0]);
+  occ(gdown_kernel<MOE_W_BF16>, (size_t)kNR * I * 4, &g_occ[MOE_W_BF16][1]);
+  occ(gdown_kernel<MOE_W_NVFP4>, (size_t)kNR * I * 4, &g_occ[MOE_W_NVFP4][1]);
   return e;
 }
 
@@ -495,18 +519,20 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
   Groups gr{st.groups, max_routes};
   group_kernel<<<1, kGT, (size_t)st.E * 16, s>>>(st, layer, slot_ids, R, gr);
   const uint16_t* xx = static_cast<const uint16_t*>(x);
-  const int grid = (g_sms > 0 ? g_sms : 1) * 4;
+  const int sms = g_sms > 0 ? g_sms : 1;
+  const int fi = wfmt == MOE_W_NVFP4 ? MOE_W_NVFP4 : MOE_W_BF16;
+  const int grid_u = sms * g_occ[fi][0], grid_d = sms * g_occ[fi][1];
   if (wfmt == MOE_W_NVFP4) {
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
-    gup_kernel<MOE_W_NVFP4><<<grid, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,
+    gup_kernel<MOE_W_NVFP4><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,
                                                                      sc.xinv, k, gr, sc.h);
-    gdown_kernel<MOE_W_NVFP4><<<grid, kWT, (size_t)kNR * I * 4, s>>>(st, H, I, layer, gr, sc.h,
+    gdown_kernel<MOE_W_NVFP4><<<grid_d, kWT, (size_t)kNR * I * 4, s>>>(st, H, I, layer, gr, sc.h,
                                                                       sc.y);
   } else {
     xprep_kernel<MOE_W_BF16><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
-    gup_kernel<MOE_W_BF16><<<grid, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,
+    gup_kernel<MOE_W_BF16><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,
                                                                     sc.xinv, k, gr, sc.h);
-    gdown_kernel<MOE_W_BF16><<<grid, kWT, (size_t)kNR * I * 4, s>>>(st, H, I, layer, gr, sc.h,
+    gdown_kernel<MOE_W_BF16><<<grid_d, kWT, (size_t)kNR * I * 4, s>>>(st, H, I, layer, gr, sc.h,
                                                                      sc.y);
   }
   const size_t n = (size_t)n_rows * H;
