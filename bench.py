@@ -125,7 +125,8 @@ class Decode:
     """The benchmark workload on one GPU: cache, inputs, one-token graph."""
 
     def __init__(self, dev: int, overlap: bool = True, warm_tokens: int = WARM_TOKENS,
-                 total_tokens: int = 512, n_layers: int | None = None, n_slots: int | None = None):
+                 total_tokens: int = 512, n_layers: int | None = None, n_slots: int | None = None,
+                 fused: bool = True):
         import torch
 
         import expert_slot_cache_lru_gb300 as m
@@ -137,6 +138,7 @@ class Decode:
             w = synth.scaled(w, n_layers=n_layers or w.n_layers, n_slots=n_slots or w.n_slots)
         self.w = w
         self.overlap = overlap
+        self.fused = fused
         t0 = time.time()
         self.blobs = synth.HostBlobs(w, pinned=True)
         self.setup_s = {"host_blobs": time.time() - t0}
@@ -186,7 +188,7 @@ class Decode:
 
     def enqueue(self):
         m, w = self.m, self.w
-        flags = m.MOE_OVERLAP if self.overlap else 0
+        flags = (m.MOE_OVERLAP if self.overlap else 0) | (m.MOE_FUSED if self.fused else 0)
         for layer in range(w.n_layers):
             sb, sg = self.shared[layer]
             m.moe_decode_layer(self.cache.handle, layer, self.b_x[layer], self.b_ids[layer],
@@ -516,7 +518,7 @@ def run_native(args) -> None:
                                 device_id=torch.device("cuda", local))
     peaks = measured_peaks()
     dec = Decode(local, overlap=not args.serial, warm_tokens=args.warm_tokens,
-                 n_layers=args.layers, n_slots=args.slots)
+                 n_layers=args.layers, n_slots=args.slots, fused=not args.unfused)
     L = dec.w.n_layers
     props = torch.cuda.get_device_properties(local)
     for _ in range(args.warmup):
@@ -591,11 +593,17 @@ def run_native(args) -> None:
                                "top-8, H 2048, I 512, gated shared expert I 512, 3164-slot LRU, "
                                "batch 1, Zipf(1.1) routing with reuse (~28 misses/token)",
                    "global_batch": ws, "graph": "one CUDA graph per token (40 layers)",
+                   "layer": ("two launches: admission, then gather + shared + routed fused"
+                             if not args.unfused else
+                             "four launches: admission, gather on a side stream (events), "
+                             "shared expert, routed experts" if not args.serial else
+                             "four launches on one stream"),
                    "overlap": not args.serial, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2: each token streams ~637 MB of expert weights",
                    "cache_warmup_tokens": args.warm_tokens},
-        # per layer: admission, demand gather, shared-expert FFN, routed FFN + combine
-        "gpu_launches": args.steps * 4 * L,
+        # per layer: the admission and one fused launch (gather + shared + routed);
+        # unfused: admission, demand gather, shared-expert FFN, routed FFN + combine
+        "gpu_launches": args.steps * (4 if args.unfused else 2) * L,
         "e2e": e2e,
         "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1),
                      "peak": hbm, "unit": "GB/s",
@@ -675,6 +683,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--serial", action="store_true", help="gather on the compute stream (ncu mode)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="four launches per layer (side-stream gather joined by events) instead of "
+                         "the fused layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--warm-tokens", type=int, default=WARM_TOKENS,

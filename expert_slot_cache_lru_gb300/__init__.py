@@ -39,6 +39,7 @@ MOE_POOL_PER_LAYER = 1
 MOE_PLAN_DEMAND = 0
 MOE_PLAN_PREFETCH = 1
 MOE_OVERLAP = 1
+MOE_FUSED = 2
 MOE_STATUS_INVALID_ID = 1
 MOE_STATUS_CAPACITY = 2
 

@@ -151,6 +151,7 @@ struct FfnScratch {
   uint16_t* x16;    // [max_rows * H] x prepared for the grouped kernels
   float* xinv;      // [max_rows] inverse of the per-row x scale
   float* y;         // [max_routes * H] per-route down projections (grouped path)
+  int* gdone;       // [max_routes] pieces of each demand-plan expert copied by a fused layer
 };
 
 cudaError_t launch_shared_expert(int wfmt, int H, int Is, const void* x, int n_rows,
@@ -174,6 +175,16 @@ cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int
                                  const void* x, const int32_t* slot_ids, const float* w,
                                  int n_rows, int k, const float* shared_y, void* out,
                                  FfnScratch sc, unsigned long long* status, cudaStream_t s);
+
+// One launch for a whole decode-sized layer after its admission: the demand
+// (and prefetch) gather, the shared expert and the routed experts (ffn_stream.cu).
+bool layer_stream_supported(int wfmt, int H, int I, int n_rows, int k, bool shared);
+cudaError_t launch_layer_stream(const DevState& st, int wfmt, int H, int I, int layer,
+                                const void* x, const int32_t* slot_ids, const float* w,
+                                int n_rows, int k, const uint8_t* shared_blob,
+                                const void* gate_w, const int32_t* plan0, const int32_t* plan1,
+                                void* out, FfnScratch sc, unsigned long long* status,
+                                cudaStream_t s);
 
 // Routed FFNs for wide steps, grouped by expert (grouped.cu).
 bool grouped_supported(int wfmt, int H, int I, int E);

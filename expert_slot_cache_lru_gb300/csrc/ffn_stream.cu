@@ -39,7 +39,8 @@ namespace {
 
 constexpr int kW = 16;             // warps per CTA
 constexpr int kT = 32 * kW;        // threads per CTA
-constexpr int kMaxTasks = 64;      // routes per call on this path
+constexpr int kMaxRoutes = 64;     // routes per call on this path
+constexpr int kMaxTasks = 80;      // routes plus one shared-expert task per row (fused layer)
 constexpr int kMaxRows = 16;       // batch rows per call on this path
 constexpr int kXW = 4;             // x words (8 elements each) loaded per thread
 constexpr int kYsPre = 1;          // shared-expert outputs prefetched per thread
@@ -47,6 +48,11 @@ constexpr int kYsPre = 1;          // shared-expert outputs prefetched per threa
 // (256 threads x 32 registers), which runs beside this kernel on the side stream.
 constexpr int kMaxReg = 104;
 constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;  // 200 ms
+constexpr int kPiece = 4096;       // gather unit of the fused layer (one warp, 8 x 16 B per lane)
+
+// What one launch computes: the routed experts, the gated shared expert, or
+// (fused layer) both plus the gather of the step's missed experts.
+enum { kRouted = 0, kShared = 1, kLayer = 2 };
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -232,7 +238,10 @@ struct BlobOff {
 // Per-call task list, identical in every CTA: the valid routes in route order.
 struct Tasks {
   int n;
-  int route[kMaxTasks];            // route index r = b*k + j
+  int route[kMaxTasks];            // route index r = b*k + j; R + b for row b's shared task
+  int b[kMaxTasks];                // batch row
+  int pe[kMaxTasks];               // fused layer: index in the demand plan, -1 = resident
+  int slot[kMaxTasks];             // slot id, -1 for the shared expert
   const uint8_t* blob[kMaxTasks];
   float wt[kMaxTasks];             // routing weight x down global scale
 };
@@ -473,10 +482,16 @@ struct FusedArgs {
   int htasks;                  // tasks whose h fits the CTA's h buffer (>= its tasks)
   unsigned long long* status;
   unsigned long long* bar_ctr;
+  // fused layer
+  const uint8_t* shared_blob;  // shared expert (one extra task per row), null = none
+  const int32_t* gplan0;       // demand plan: its experts are copied here and waited on
+  const int32_t* gplan1;       // prefetch plan of the next layer (copied only), or null
+  int* gdone;                  // [plan entries] pieces copied; zero at entry, reset here
 };
 
-template <int FMT, bool SHARED>
+template <int FMT, int MODE>
 __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) {
+  constexpr bool SHARED = MODE == kShared, LAYER = MODE == kLayer;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ Tasks tk;
   __shared__ int ts[kMaxRows + 1];         // tasks of batch row b: [ts[b], ts[b+1])
@@ -510,7 +525,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
 #pragma unroll
   for (int j = 0; j < kYsPre; ++j) {
     const int ru = ru0 + threadIdx.x + j * kT;
-    ysv[j] = (!SHARED && a.ys && ru < ru1) ? a.ys[ru] : 0.f;
+    ysv[j] = (MODE == kRouted && a.ys && ru < ru1) ? a.ys[ru] : 0.f;
   }
   if (threadIdx.x < kMaxRows) xmax[threadIdx.x] = 0u;
   if (warp == 0) {
@@ -528,23 +543,31 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     const unsigned m0 = __ballot_sync(0xffffffffu, b0 != nullptr);
     const unsigned m1 = __ballot_sync(0xffffffffu, b1 != nullptr);
     const unsigned lt = (1u << lane) - 1u;
-    if (b0) {
-      const int p = __popc(m0 & lt);
-      tk.route[p] = lane;
-      tk.blob[p] = b0;
-    }
-    if (b1) {
-      const int p = __popc(m0) + __popc(m1 & lt);
-      tk.route[p] = lane + 32;
-      tk.blob[p] = b1;
-    }
-    if (lane == 0) tk.n = __popc(m0) + __popc(m1);
-    if (lane <= n_rows) {  // first task of batch row `lane`: valid routes below lane*k
-      const int lim = lane * k;
+    // valid routes below route index lim
+    auto below = [&](int lim) {
       const unsigned a0 = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
       const unsigned a1 = lim >= 64 ? 0xffffffffu : (lim <= 32 ? 0u : ((1u << (lim - 32)) - 1u));
-      ts[lane] = __popc(m0 & a0) + __popc(m1 & a1);
+      return __popc(m0 & a0) + __popc(m1 & a1);
+    };
+    const int spr = (LAYER && a.shared_blob) ? 1 : 0;  // shared tasks per row (after its routes)
+    auto put = [&](int p, int r, int b, const uint8_t* blob, int slot) {
+      tk.route[p] = r;
+      tk.b[p] = b;
+      tk.blob[p] = blob;
+      tk.slot[p] = slot;
+      tk.pe[p] = -1;
+    };
+    if (b0) {
+      const int b = SHARED ? lane : lane / k;
+      put(__popc(m0 & lt) + spr * b, lane, b, b0, SHARED ? -1 : a.slot_ids[lane]);
     }
+    if (b1) {
+      const int b = (lane + 32) / k;
+      put(__popc(m0) + __popc(m1 & lt) + spr * b, lane + 32, b, b1, a.slot_ids[lane + 32]);
+    }
+    if (spr && lane < n_rows) put(below((lane + 1) * k) + lane, a.R + lane, lane, a.shared_blob, -1);
+    if (lane == 0) tk.n = __popc(m0) + __popc(m1) + spr * n_rows;
+    if (lane <= n_rows) ts[lane] = below(lane * k) + spr * lane;  // first task of row `lane`
   }
   if (FMT == MOE_W_NVFP4) {  // rows whose |x| reaches 2^14 get a scale below 1
 #pragma unroll
@@ -562,6 +585,19 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   }
   __syncthreads();  // (1) task list, ts, xmax
   const int T = tk.n;
+  // fused layer: the demand plan entry of each task whose expert is being
+  // copied in by this launch (its rows wait for the copy)
+  const int n_pl0 = LAYER && a.gplan0 ? a.gplan0[0] : 0;
+  const int n_pl1 = LAYER && a.gplan1 ? a.gplan1[0] : 0;
+  if (LAYER && warp == 0) {
+    for (int t = lane; t < T; t += 32) {
+      int pe = -1;
+      if (tk.slot[t] >= 0)
+        for (int i = 0; i < n_pl0; ++i)
+          if (a.gplan0[1 + 3 * i] == tk.slot[t]) pe = i;
+      tk.pe[t] = pe;
+    }
+  }
 
   // ---- phase A assignment: whole rows, contiguous per warp
   const int Gw = gridDim.x * kW, gw = blockIdx.x * kW + warp;
@@ -624,17 +660,29 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   // follows until the grid barrier, so each warp computes as soon as its own
   // rows land.
   const uint64_t pol = l2_evict_first();
+  // pieces per expert (a fused layer always has slot storage; 1 keeps the others well defined)
+  const int ppe = LAYER ? max(1, (int)((st.slot_bytes + kPiece - 1) / kPiece)) : 1;
   auto issue_a = [&](int it) {  // lane 0
     const int r = ra0 + it / KC, c = it % KC, t = r / I, sl = it & 1;
     const uint32_t bytes = ItemA<FMT>::BYTES;
+    if (LAYER && tk.pe[t] >= 0) {  // wait (bounded) until this launch copied the expert in
+      const unsigned long long t0 = now_ns();
+      int v = 0;
+      for (;;) {
+        asm volatile("ld.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(a.gdone + tk.pe[t]) : "memory");
+        if (v >= ppe) break;
+        if (now_ns() - t0 > kWaitNs) {
+          flag_timeout(a.status);
+          break;
+        }
+        __nanosleep(500);  // many warps wait on one counter the copying warps increment
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> bulk reads
+    }
     mbar_expect_tx(&bar_a[warp][sl], bytes);
     ItemA<FMT>::issue(slots + sl * kSlotBytes, tk.blob[t], o, H, r - t * I, c, &bar_a[warp][sl],
                       pol);
   };
-  if (lane == 0) {
-    if (nitA > 0) issue_a(0);
-    if (nitA > 1) issue_a(1);
-  }
   if (warp == kW - 1) {  // phase-B staging: one lane per (batch row, task) block
     const int nblk = (ru1 > ru0) ? (ts[bA + 1] - ts[bA]) + (bB != bA ? ts[bB + 1] - ts[bB] : 0) : 0;
     uint32_t mine = 0;
@@ -644,7 +692,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       const int t = ts[b] + (bi ? j - (ts[bA + 1] - ts[bA]) : j);
       const int nlen = nlen_of(b), q0 = (bi ? cntA : 0) + (t - ts[b]) * nlen;
       const int cnt = min(nlen, qs - q0);
-      if (cnt > 0) mine += (uint32_t)cnt * (CB + SB);
+      if (cnt > 0 && !(LAYER && tk.pe[t] >= 0)) mine += (uint32_t)cnt * (CB + SB);
     }
     uint32_t total = mine;
 #pragma unroll
@@ -657,7 +705,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       const int t = ts[b] + (bi ? j - (ts[bA + 1] - ts[bA]) : j);
       const int nlo = nlo_of(b), nlen = nlen_of(b), q0 = (bi ? cntA : 0) + (t - ts[b]) * nlen;
       const int cnt = min(nlen, qs - q0);
-      if (cnt <= 0) continue;
+      if (cnt <= 0 || (LAYER && tk.pe[t] >= 0)) continue;  // copied in by this launch: read later
       const uint8_t* blob = tk.blob[t];
       bulk_g2s(stC + (size_t)q0 * CB,
                blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB,
@@ -667,16 +715,58 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
                  &bar_b, pol);
     }
   }
+  // fused layer: the step's missed experts (and the next layer's prefetches)
+  // are copied from pinned host memory, 4 KiB per warp at a time, by every
+  // warp before its own compute (pieces strided over the CTAs, so all SMs
+  // issue host reads); each finished piece of a demand entry is counted, and
+  // the rows of that expert wait for the full count.  A warp does its pieces
+  // before it can wait on any, and a step without misses has no pieces.
+  if (LAYER && n_pl0 + n_pl1 > 0) {
+    const int gidx = warp * gridDim.x + blockIdx.x, gcnt = Gw;
+    const long total = (long)(n_pl0 + n_pl1) * ppe;
+    for (long p = gidx; p < total; p += gcnt) {
+      const int ei = (int)(p / ppe), j = (int)(p - (long)ei * ppe);
+      const bool demand = ei < n_pl0;
+      const int32_t* plan = demand ? a.gplan0 : a.gplan1;
+      const int i = demand ? ei : ei - n_pl0;
+      const int s = plan[1 + 3 * i], L = plan[2 + 3 * i], e = plan[3 + 3 * i];
+      if ((unsigned)s < (unsigned)st.S && (unsigned)L < (unsigned)st.L && (unsigned)e < (unsigned)st.E) {
+        const size_t off = (size_t)j * kPiece;
+        const int len = (int)min((size_t)kPiece, st.slot_bytes - off);
+        const uint4* src = reinterpret_cast<const uint4*>(st.host_blob[L * st.E + e] + off);
+        uint4* dst = reinterpret_cast<uint4*>(
+            st.slots + ((size_t)pool_of(st, L) * st.S + s) * st.stride + off);
+        const int nv = len / 16;
+        uint4 v[kPiece / 512];
+#pragma unroll
+        for (int u = 0; u < kPiece / 512; ++u)
+          if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
+#pragma unroll
+        for (int u = 0; u < kPiece / 512; ++u)
+          if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
+      }
+      __syncwarp();
+      if (demand && lane == 0) {
+        __threadfence();
+        atomicAdd(a.gdone + i, 1);
+      }
+    }
+  }
+  if (lane == 0) {
+    if (nitA > 0) issue_a(0);
+    if (nitA > 1) issue_a(1);
+  }
+
   // per-task combine factor (stored to shared memory before the grid barrier)
   float cw = 1.f, c2 = 1.f;
   if (threadIdx.x < T) {
-    if (!SHARED) cw = a.w[tk.route[threadIdx.x]];
+    if (MODE != kShared && tk.route[threadIdx.x] < a.R) cw = a.w[tk.route[threadIdx.x]];
     if (FMT == MOE_W_NVFP4) c2 = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob)[2];
   }
 
   // the shared expert's sigmoid gate, sigmoid(x_b . w_g), in fp32, by the last
   // CTA (the one least likely to hold phase-A rows), before its phase A
-  if (SHARED && blockIdx.x == gridDim.x - 1 && warp < n_rows) {
+  if ((SHARED || (LAYER && a.shared_blob)) && blockIdx.x == gridDim.x - 1 && warp < n_rows) {
     float z = 0.f;
     for (int i0 = lane * 8; i0 < H; i0 += 256) {
       const uint4 gv = *reinterpret_cast<const uint4*>(a.gate_w + i0);
@@ -699,11 +789,11 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
     auto xrow = [&](int it) {
       const int t = (ra0 + it / KC) / I;
-      return xs4 + (size_t)(tk.route[t] / k) * (H / 8);
+      return xs4 + (size_t)tk.b[t] * (H / 8);
     };
     auto store_h = [&](int it, float gsum, float usum, float gs0, float gs1) {  // lane 0
       const int r = ra0 + it / KC, t = r / I;
-      const float xi = xinv[tk.route[t] / k];
+      const float xi = xinv[tk.b[t]];
       const float gg = gsum * xi * gs0, uu = usum * xi * gs1;
       a.h[(size_t)tk.route[t] * I + (r - t * I)] = gg / (1.f + expf(-gg)) * uu;
     };
@@ -776,8 +866,14 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const bool staged = mbar_wait(&bar_b, 0);  // the staged phase-B rows (bounded)
   if (!staged) flag_timeout(a.status);
   if (!ok || !__syncthreads_and(staged)) return;  // timed out: nothing below is trustworthy
+  if (LAYER && blockIdx.x == 0)  // every wait on the copies is behind the barrier
+    for (int i = threadIdx.x; i < n_pl0; i += kT) a.gdone[i] = 0;
+  // an expert copied in by this launch: its down global scale is in the slot
+  // only now (read by the combine, after the next block barrier)
+  if (LAYER && FMT == MOE_W_NVFP4 && threadIdx.x < T && tk.pe[threadIdx.x] >= 0)
+    tk.wt[threadIdx.x] = cw * reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob)[2];
   // the gate of this thread's combine row, requested now (written before the barrier)
-  const float gate_b = (SHARED && ru0 + (int)threadIdx.x < ru1)
+  const float gate_b = ((SHARED || (LAYER && a.shared_blob)) && ru0 + (int)threadIdx.x < ru1)
                            ? __ldcg(&a.gate[(ru0 + (int)threadIdx.x) / H])
                            : 0.f;
   // h of the tasks this CTA's rows need, read once from L2 into shared memory
@@ -838,7 +934,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
         const int qq = q + j, n = n0 + j;
         const uint8_t* cp;
         const uint8_t* sp;
-        if (qq < qs) {
+        if (qq < qs && !(LAYER && tk.pe[t] >= 0)) {
           cp = stC + (size_t)qq * CB;
           sp = stS + (size_t)qq * SB;
         } else {
@@ -861,12 +957,19 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   __syncthreads();  // every (task, row) result in ysm
   // combine: each output row, its tasks in route order (j ascending), then + ys
   int mm = 0;
+  const bool has_s = LAYER && a.shared_blob;  // row b's last task is the shared expert
   for (int ru = ru0 + threadIdx.x; ru < ru1; ru += kT, ++mm) {
     const int b = ru / H;
+    const int te = ts[b + 1] - (has_s ? 1 : 0);
     float acc = 0.f;
-    for (int t = ts[b]; t < ts[b + 1]; ++t)
+    for (int t = ts[b]; t < te; ++t)
       acc = fmaf(tk.wt[t], ysm[(size_t)t * perB + (ru - ru0)], acc);
-    if (SHARED) {
+    if (LAYER) {  // routed sum (j ascending), then + gate * shared, as in the two-launch path
+      float yv = 0.f;
+      if (has_s)
+        yv = (mm == 0 ? gate_b : __ldcg(&a.gate[b])) * (tk.wt[te] * ysm[(size_t)te * perB + (ru - ru0)]);
+      a.out[ru] = __float2bfloat16_rn(has_s ? acc + yv : acc);
+    } else if (SHARED) {
       a.ys[ru] = (mm == 0 ? gate_b : __ldcg(&a.gate[b])) * acc;
     } else {
       const float yv = mm < kYsPre ? ysv[mm] : (a.ys ? a.ys[ru] : 0.f);
@@ -925,23 +1028,31 @@ cudaError_t launch_coop(K kernel, size_t smem, cudaStream_t s, const DevState& s
   return cudaLaunchKernelEx(&cfg, kernel, st, a);
 }
 
-cudaError_t launch_fused(const DevState& st, int wfmt, bool shared, const FusedArgs& a0,
+// tasks per batch row and in all, for a launch of `mode`
+int tasks_per_row(int mode, int k, bool shared) { return mode == kLayer ? k + (shared ? 1 : 0) : k; }
+
+cudaError_t launch_fused(const DevState& st, int wfmt, int mode, const FusedArgs& a0,
                          cudaStream_t s) {
   FusedArgs a = a0;
-  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, a.k, a.R);
+  const bool sh = a.shared_blob != nullptr;
+  const int kt = tasks_per_row(mode, a.k, sh);
+  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, kt, a.R + (mode == kLayer && sh ? a.n_rows : 0));
   a.qs = p.qs;
   a.htasks = p.htasks;
-  if (wfmt == MOE_W_NVFP4)
-    return shared ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, true>, p.smem, s, st, a)
-                  : launch_coop(ffn_fused_kernel<MOE_W_NVFP4, false>, p.smem, s, st, a);
-  return shared ? launch_coop(ffn_fused_kernel<MOE_W_BF16, true>, p.smem, s, st, a)
-                : launch_coop(ffn_fused_kernel<MOE_W_BF16, false>, p.smem, s, st, a);
+  if (wfmt == MOE_W_NVFP4) {
+    if (mode == kLayer) return launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kLayer>, p.smem, s, st, a);
+    return mode == kShared ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kShared>, p.smem, s, st, a)
+                           : launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kRouted>, p.smem, s, st, a);
+  }
+  if (mode == kLayer) return launch_coop(ffn_fused_kernel<MOE_W_BF16, kLayer>, p.smem, s, st, a);
+  return mode == kShared ? launch_coop(ffn_fused_kernel<MOE_W_BF16, kShared>, p.smem, s, st, a)
+                         : launch_coop(ffn_fused_kernel<MOE_W_BF16, kRouted>, p.smem, s, st, a);
 }
 
 }  // namespace
 
 bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks) {
-  if (g_num_sms <= 0 || n_tasks > kMaxTasks || n_rows > kMaxRows || n_rows < 1) return false;
+  if (g_num_sms <= 0 || n_tasks > kMaxRoutes || n_rows > kMaxRows || n_rows < 1) return false;
   const int k = (n_tasks + n_rows - 1) / n_rows;
   return fused_plan(wfmt, H, I, n_rows, k, n_tasks).ok;
 }
@@ -954,10 +1065,12 @@ cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int ma
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBudget);
   };
-  set(ffn_fused_kernel<MOE_W_BF16, true>);
-  set(ffn_fused_kernel<MOE_W_NVFP4, true>);
-  set(ffn_fused_kernel<MOE_W_BF16, false>);
-  set(ffn_fused_kernel<MOE_W_NVFP4, false>);
+  set(ffn_fused_kernel<MOE_W_BF16, kShared>);
+  set(ffn_fused_kernel<MOE_W_NVFP4, kShared>);
+  set(ffn_fused_kernel<MOE_W_BF16, kRouted>);
+  set(ffn_fused_kernel<MOE_W_NVFP4, kRouted>);
+  set(ffn_fused_kernel<MOE_W_BF16, kLayer>);
+  set(ffn_fused_kernel<MOE_W_NVFP4, kLayer>);
   (void)wfmt, (void)H, (void)I, (void)Is, (void)max_rows, (void)max_tasks;
   return e;
 }
@@ -983,7 +1096,7 @@ cudaError_t launch_shared_stream(const DevState& st, int wfmt, int H, int Is, co
   a.out = nullptr;
   a.status = status;
   a.bar_ctr = sc.bar;
-  return launch_fused(st, wfmt, true, a, s);
+  return launch_fused(st, wfmt, kShared, a, s);
 }
 
 cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int layer,
@@ -1008,7 +1121,45 @@ cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int
   a.out = static_cast<__nv_bfloat16*>(out);
   a.status = status;
   a.bar_ctr = sc.bar;
-  return launch_fused(st, wfmt, false, a, s);
+  return launch_fused(st, wfmt, kRouted, a, s);
+}
+
+bool layer_stream_supported(int wfmt, int H, int I, int n_rows, int k, bool shared) {
+  if (g_num_sms <= 0 || n_rows < 1 || n_rows > kMaxRows || n_rows * k > kMaxRoutes) return false;
+  const int kt = tasks_per_row(kLayer, k, shared);
+  const int T = n_rows * kt;
+  return T <= kMaxTasks && fused_plan(wfmt, H, I, n_rows, kt, T).ok;
+}
+
+cudaError_t launch_layer_stream(const DevState& st, int wfmt, int H, int I, int layer,
+                                const void* x, const int32_t* slot_ids, const float* w,
+                                int n_rows, int k, const uint8_t* shared_blob,
+                                const void* gate_w, const int32_t* plan0, const int32_t* plan1,
+                                void* out, FfnScratch sc, unsigned long long* status,
+                                cudaStream_t s) {
+  FusedArgs a{};
+  a.H = H;
+  a.I = I;
+  a.layer = layer;
+  a.k = k;
+  a.R = n_rows * k;
+  a.n_rows = n_rows;
+  a.x = static_cast<const uint16_t*>(x);
+  a.slot_ids = slot_ids;
+  a.fixed_blob = nullptr;
+  a.w = w;
+  a.h = sc.h;
+  a.gate_w = static_cast<const uint16_t*>(gate_w);
+  a.gate = sc.gate;
+  a.ys = nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = status;
+  a.bar_ctr = sc.bar;
+  a.shared_blob = shared_blob;
+  a.gplan0 = plan0;
+  a.gplan1 = plan1;
+  a.gdone = sc.gdone;
+  return launch_fused(st, wfmt, kLayer, a, s);
 }
 
 // ---------------------------------------------------------------- allocation-free variant

@@ -161,7 +161,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_grp = cv.take<int32_t>(2 + 3 * (size_t)d.max_routes),
                o_vict = cv.take<int32_t>(vcap), o_los = cv.take<uint64_t>(vcap),
                o_lol = cv.take<int32_t>(vcap), o_hb = cv.take<const uint8_t*>(K),
-               o_h = cv.take<float>((size_t)d.max_routes * std::max(I, 1)),
+               o_h = cv.take<float>(((size_t)d.max_routes + d.max_rows) * std::max(I, 1)),
+               o_gdone = cv.take<int32_t>(std::max(d.max_routes, 1)),
                o_hs = cv.take<float>((size_t)d.max_rows * std::max(Is, 1)),
                o_gate = cv.take<float>(d.max_rows),
                o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1)),
@@ -212,6 +213,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.x16 = reinterpret_cast<uint16_t*>(m + o_x16);
   c->sc.xinv = reinterpret_cast<float*>(m + o_xinv);
   c->sc.y = reinterpret_cast<float*>(m + o_y);
+  c->sc.gdone = reinterpret_cast<int*>(m + o_gdone);
 
   // initial state: nothing resident, every clock at 1
   e = cudaMemset(c->mem, 0, c->mem_bytes);
@@ -460,8 +462,26 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
   if (pf && (layer + 1 >= c->d.n_layers || c->d.max_pred == 0)) return MOE_ERR_INVALID_ARG;
   if (pf && n_pred > c->d.max_pred) return MOE_ERR_CAPACITY;
   const bool overlap = (flags & MOE_OVERLAP) != 0;
-  if (overlap && !side_stream) return MOE_ERR_INVALID_ARG;
   cudaStream_t cs = as_stream(compute_stream), ss = as_stream(side_stream);
+  const moe_cache_desc& dd = c->d;
+  const bool fused = (flags & MOE_FUSED) && c->stream_ffn && dd.slot_bytes > 0 &&
+                     (!d_shared_blob || dd.shared_inter == dd.inter) &&
+                     moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k,
+                                                 d_shared_blob != nullptr);
+  if (fused) {  // admission, then one launch: gathers + shared expert + routed experts
+    CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
+    int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
+    if (pf) {
+      CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, cs));
+      c->last_pf_layer = layer + 1;
+    }
+    CK(moe::launch_layer_stream(c->st, dd.wfmt, dd.hidden, dd.inter, layer, d_x, d_slot_ids, d_w,
+                                n_rows, k, static_cast<const uint8_t*>(d_shared_blob),
+                                d_shared_gate, c->st.plan_demand, pf ? pf_plan : nullptr, d_out,
+                                c->sc, c->st.status, cs));
+    return MOE_OK;
+  }
+  if (overlap && !side_stream) return MOE_ERR_INVALID_ARG;
 
   CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
   int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];

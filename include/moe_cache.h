@@ -128,6 +128,8 @@ typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 
 /* moe_decode_layer flags */
 #define MOE_OVERLAP 1u        /* gather on the side stream, joined by events [P2] */
+#define MOE_FUSED 2u          /* after the admission, one launch does the gathers, the shared
+                                 expert and the routed experts (decode-sized steps) */
 
 /* status_bits of moe_stats */
 #define MOE_STATUS_INVALID_ID 1ull
@@ -276,7 +278,18 @@ MOE_API int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const i
  * receives the rewritten ids (may equal d_ids).  d_pred/n_pred (NULL/0 = none)
  * are predicted ids of layer+1; their gather is queued on the side stream
  * after this layer's demand gather and is joined by layer+1's own wait.  Must
- * not be mixed with moe_gather_missing(MOE_PLAN_PREFETCH) calls of its own. */
+ * not be mixed with moe_gather_missing(MOE_PLAN_PREFETCH) calls of its own.
+ *
+ * With flags & MOE_FUSED, for decode-sized steps (at most 16 rows and 64
+ * routes, the streaming kernel's shapes, and a shared expert of the routed
+ * experts' size), the layer is the admission (and prefetch admission) on
+ * compute_stream followed by one cooperative launch that copies the demand and
+ * prefetch plans' experts from host memory, computes the shared expert and
+ * the routed experts -- the rows of a missed expert wait, inside the launch,
+ * until its bytes have arrived -- and writes d_out.  The overlap of [P2] (the
+ * gather beside the shared expert) happens inside that launch instead of on
+ * two streams; side_stream is not used.  Other shapes fall back to the mode
+ * the remaining flags select.  Results equal the two-launch path's bit for bit. */
 MOE_API int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,
                      const float* d_w, int32_t* d_slot_ids, int n_rows, int k, int fetch_cap,
                      const int32_t* d_pred, int n_pred, const void* d_shared_blob,

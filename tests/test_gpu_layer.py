@@ -25,9 +25,10 @@ class Stepper:
     """Feeds one workload's steps through moe_decode_layer, mirroring every
     admission/prefetch on the oracle."""
 
-    def __init__(self, rig: Rig, overlap: bool = True, n_pred: int = 0):
+    def __init__(self, rig: Rig, overlap: bool = True, n_pred: int = 0, fused: bool = False):
         self.rig = rig
         self.overlap = overlap
+        self.fused = fused
         self.n_pred = n_pred
         self.side = torch.cuda.Stream()
         w = rig.w
@@ -41,7 +42,7 @@ class Stepper:
         d_x = _dev(x)
         d_ids = _dev(ids.reshape(w.n_layers, -1))
         d_w = _dev(wts.reshape(w.n_layers, -1))
-        flags = m.MOE_OVERLAP if self.overlap else 0
+        flags = (m.MOE_OVERLAP if self.overlap else 0) | (m.MOE_FUSED if self.fused else 0)
         refs = []
         for layer in range(w.n_layers):
             pred = None
@@ -104,6 +105,53 @@ def test_overlap_bytes_equal_serial():
         sa.step(t, ids[t], wts[t], x)
         sb.step(t, ids[t], wts[t], x)
         assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16)), f"step {t}"
+
+
+def test_fused_layer_equals_two_launch_path():
+    """MOE_FUSED runs the gather, the shared expert and the routed experts in
+    one launch after the admission; the overlap of [FreeToken issue #753, What
+    we changed] moves inside it.  Slot ids, state and statistics stay exact
+    against the oracle, and the output bytes equal the two-launch path's."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=6, steps=12, n_slots=80)
+    blobs = synth.HostBlobs(w, pinned=True)
+    a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    sa, sb = Stepper(a, True, fused=True), Stepper(b, True)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        sa.step(t, ids[t], wts[t], x)
+        sb.step(t, ids[t], wts[t], x)
+        assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16)), f"step {t}"
+        if t in (0, w.steps - 1):
+            for layer in (0, w.n_layers - 1):
+                ref = a.oracle_layer(layer, x[layer], ids[t, layer], wts[t, layer])
+                assert_close(sa.out[layer], ref, w.fmt, f"step {t} layer {layer}")
+    assert sum(a.sc.stats(l)["fetched"] for l in range(w.n_layers)) > 50
+    assert a.sc.stats(0)["status_bits"] == 0
+
+
+def test_fused_layer_capped_prefetch_bf16():
+    """The hybrid shapes (bf16, H 4096, I 1024, fetch cap 4, look-ahead
+    prefetch of 8 ids under the LFRU guard) through MOE_FUSED: the prefetch
+    plan is copied inside the launch; state and prefetch counters exact, output
+    bytes equal to the two-launch path's."""
+    w = synth.scaled(synth.workloads()["hybrid_prefetch"], n_layers=6, steps=5)
+    blobs = synth.HostBlobs(w, pinned=True)
+    a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    sa, sb = Stepper(a, True, n_pred=w.n_pred, fused=True), Stepper(b, True, n_pred=w.n_pred)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        sa.step(t, ids[t], wts[t], x)
+        sb.step(t, ids[t], wts[t], x)
+        assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16)), f"step {t}"
+    st = [a.sc.stats(l) for l in range(w.n_layers)]
+    assert sum(s["pf_filled"] for s in st) > 0 and sum(s["overflow_routes"] for s in st) > 0
+    # the prefetched experts' bytes arrived: every resident slot holds its expert
+    state = a.oc.state()
+    for s, key in enumerate(state["slot_key"]):
+        if key >= 0:
+            assert np.array_equal(a.slot_bytes(0, s), a.blobs.blob(int(key))), s
 
 
 def test_slot_placement_does_not_change_bits():
