@@ -241,6 +241,7 @@ struct Tasks {
   int route[kMaxTasks];            // route index r = b*k + j; R + b for row b's shared task
   int b[kMaxTasks];                // batch row
   int pe[kMaxTasks];               // fused layer: index in the demand plan, -1 = resident
+  int ord[kMaxTasks];              // phase-A task order (fused layer: copied-in tasks last)
   int slot[kMaxTasks];             // slot id, -1 for the shared expert
   const uint8_t* blob[kMaxTasks];
   float wt[kMaxTasks];             // routing weight x down global scale
@@ -597,14 +598,34 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
           if (a.gplan0[1 + 3 * i] == tk.slot[t]) pe = i;
       tk.pe[t] = pe;
     }
+    __syncwarp();
+    // phase-A order: resident tasks, then the ones this launch copies in, so
+    // that their rows are the last item of the warps that hold them
+    int nres = 0;
+    for (int t0 = 0; t0 < T; t0 += 32)
+      nres += __popc(__ballot_sync(0xffffffffu, t0 + lane < T && tk.pe[t0 + lane] < 0));
+    const unsigned lt = (1u << lane) - 1u;
+    for (int t0 = 0, cr = 0, cm = nres; t0 < T; t0 += 32) {
+      const int t = t0 + lane;
+      const bool res = t < T && tk.pe[t] < 0, mis = t < T && !res;
+      const unsigned br = __ballot_sync(0xffffffffu, res), bm = __ballot_sync(0xffffffffu, mis);
+      if (res) tk.ord[cr + __popc(br & lt)] = t;
+      if (mis) tk.ord[cm + __popc(bm & lt)] = t;
+      cr += __popc(br);
+      cm += __popc(bm);
+    }
   }
 
-  // ---- phase A assignment: whole rows, contiguous per warp
+  // ---- phase A assignment: whole rows of the flattened (task order, i) list,
+  // dealt round-robin over the grid's warps: warp gw takes rows gw, gw + Gw, ...
   const int Gw = gridDim.x * kW, gw = blockIdx.x * kW + warp;
   const int NA = T * I;
-  const int perA = (NA + Gw - 1) / Gw;
-  const int ra0 = min(NA, gw * perA), ra1 = min(NA, ra0 + perA);
-  const int nitA = (ra1 - ra0) * KC;
+  const int nitA = (gw < NA ? (NA - 1 - gw) / Gw + 1 : 0) * KC;
+  auto task_of = [&](int it) {  // the task of this warp's item `it`
+    const int tp = (gw + (it / KC) * Gw) / I;
+    return LAYER ? tk.ord[tp] : tp;
+  };
+  auto row_of = [&](int it) { return (gw + (it / KC) * Gw) % I; };  // its gate/up row
   // ---- phase-B items of this CTA (staged into shared memory after (2))
   const int bA = ru0 / H, bB = ru1 > ru0 ? (ru1 - 1) / H : bA;
   auto nlo_of = [&](int b) { return max(ru0 - b * H, 0); };
@@ -663,26 +684,14 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   // pieces per expert (a fused layer always has slot storage; 1 keeps the others well defined)
   const int ppe = LAYER ? max(1, (int)((st.slot_bytes + kPiece - 1) / kPiece)) : 1;
   auto issue_a = [&](int it) {  // lane 0
-    const int r = ra0 + it / KC, c = it % KC, t = r / I, sl = it & 1;
-    const uint32_t bytes = ItemA<FMT>::BYTES;
-    if (LAYER && tk.pe[t] >= 0) {  // wait (bounded) until this launch copied the expert in
-      const unsigned long long t0 = now_ns();
-      int v = 0;
-      for (;;) {
-        asm volatile("ld.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(a.gdone + tk.pe[t]) : "memory");
-        if (v >= ppe) break;
-        if (now_ns() - t0 > kWaitNs) {
-          flag_timeout(a.status);
-          break;
-        }
-        __nanosleep(500);  // many warps wait on one counter the copying warps increment
-      }
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // generic writes -> bulk reads
-    }
-    mbar_expect_tx(&bar_a[warp][sl], bytes);
-    ItemA<FMT>::issue(slots + sl * kSlotBytes, tk.blob[t], o, H, r - t * I, c, &bar_a[warp][sl],
-                      pol);
+    const int t = task_of(it), sl = it & 1;
+    mbar_expect_tx(&bar_a[warp][sl], ItemA<FMT>::BYTES);
+    ItemA<FMT>::issue(slots + sl * kSlotBytes, tk.blob[t], o, H, row_of(it), it % KC,
+                      &bar_a[warp][sl], pol);
   };
+  // an item of an expert this launch copies in is requested only once the copy
+  // is complete (see wait_copied below); every other item as soon as its slot is free
+  auto deferred = [&](int it) { return LAYER && tk.pe[task_of(it)] >= 0; };
   if (warp == kW - 1) {  // phase-B staging: one lane per (batch row, task) block
     const int nblk = (ru1 > ru0) ? (ts[bA + 1] - ts[bA]) + (bB != bA ? ts[bB + 1] - ts[bB] : 0) : 0;
     uint32_t mine = 0;
@@ -715,16 +724,21 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
                  &bar_b, pol);
     }
   }
+  // this warp's first two phase-A items are requested before any copy work,
+  // so that they land while it copies
+  if (lane == 0) {
+    if (nitA > 0 && !deferred(0)) issue_a(0);
+    if (nitA > 1 && !deferred(1)) issue_a(1);
+  }
   // fused layer: the step's missed experts (and the next layer's prefetches)
-  // are copied from pinned host memory, 4 KiB per warp at a time, by every
-  // warp before its own compute (pieces strided over the CTAs, so all SMs
-  // issue host reads); each finished piece of a demand entry is counted, and
-  // the rows of that expert wait for the full count.  A warp does its pieces
-  // before it can wait on any, and a step without misses has no pieces.
+  // are copied from pinned host memory in 4 KiB pieces, one per warp at a
+  // time, consecutive pieces on consecutive CTAs (so every SM issues host
+  // reads).  Each finished piece of a demand entry is counted, and the rows of
+  // that expert wait for the full count.  A warp does its pieces before it can
+  // wait on any, and a step without misses has no pieces.
   if (LAYER && n_pl0 + n_pl1 > 0) {
-    const int gidx = warp * gridDim.x + blockIdx.x, gcnt = Gw;
     const long total = (long)(n_pl0 + n_pl1) * ppe;
-    for (long p = gidx; p < total; p += gcnt) {
+    for (long p = warp * gridDim.x + blockIdx.x; p < total; p += Gw) {
       const int ei = (int)(p / ppe), j = (int)(p - (long)ei * ppe);
       const bool demand = ei < n_pl0;
       const int32_t* plan = demand ? a.gplan0 : a.gplan1;
@@ -752,10 +766,6 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       }
     }
   }
-  if (lane == 0) {
-    if (nitA > 0) issue_a(0);
-    if (nitA > 1) issue_a(1);
-  }
 
   // per-task combine factor (stored to shared memory before the grid barrier)
   float cw = 1.f, c2 = 1.f;
@@ -778,8 +788,10 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   }
 
   // ---------------------------------------------------------------- phase A
-  bool failed = false;                          // a timed-out wait: skip the rest
-  int issued = min(nitA, 2), consumed = 0;      // this warp's phase-A items
+  bool failed = false;  // a timed-out wait: skip the rest
+  // the item whose copies are in flight on each of the warp's two slots, -1 =
+  // none (warp-uniform: every lane takes the same decisions as lane 0)
+  int inflight[2] = {nitA > 0 && !deferred(0) ? 0 : -1, nitA > 1 && !deferred(1) ? 1 : -1};
   // Items are (row, chunk) pairs, alternating between two register buffers;
   // the next item of a buffer is requested as soon as its dot is done.  With
   // one chunk per row (KC = 1) each buffer holds a whole row and the two rows
@@ -788,21 +800,54 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   {
     const uint4* xs4 = reinterpret_cast<const uint4*>(xs);
     auto xrow = [&](int it) {
-      const int t = (ra0 + it / KC) / I;
-      return xs4 + (size_t)tk.b[t] * (H / 8);
+      return xs4 + (size_t)tk.b[task_of(it)] * (H / 8);
     };
     auto store_h = [&](int it, float gsum, float usum, float gs0, float gs1) {  // lane 0
-      const int r = ra0 + it / KC, t = r / I;
+      const int t = task_of(it);
       const float xi = xinv[tk.b[t]];
       const float gg = gsum * xi * gs0, uu = usum * xi * gs1;
-      a.h[(size_t)tk.route[t] * I + (r - t * I)] = gg / (1.f + expf(-gg)) * uu;
+      a.h[(size_t)tk.route[t] * I + row_of(it)] = gg / (1.f + expf(-gg)) * uu;
     };
     float ga = 0.f, ua = 0.f, gb = 0.f, ub = 0.f;
-    auto wait_a = [&](int it) -> bool {  // item `it` landed in its slot (warp-uniform)
-      const bool all =
-          __all_sync(0xffffffffu, mbar_wait(&bar_a[warp][it & 1], (uint32_t)((it >> 1) & 1)));
+    // fused layer: wait (bounded, the whole warp on lane 0's reads) until this
+    // launch has copied all of task t's expert into its slot
+    auto wait_copied = [&](int t) -> bool {
+      const int* ctr = a.gdone + tk.pe[t];
+      const unsigned long long t0 = now_ns();
+      for (;;) {
+        int s = 0;  // 1: complete, 2: timed out
+        if (lane == 0) {
+          int v;
+          asm volatile("ld.acquire.gpu.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+          s = v >= ppe ? 1 : (now_ns() - t0 > kWaitNs ? 2 : 0);
+        }
+        s = __shfl_sync(0xffffffffu, s, 0);
+        if (s == 1) return true;
+        if (s == 2) {
+          if (lane == 0) flag_timeout(a.status);
+          return false;
+        }
+        __nanosleep(256);
+      }
+    };
+    // item `it` in its slot (warp-uniform); a deferred item is requested here
+    auto wait_a = [&](int it) -> bool {
+      const int sl = it & 1;
+      if (inflight[sl] != it) {  // deferred: its expert is being copied in by this launch
+        if (!wait_copied(task_of(it))) {
+          failed = true;
+          return false;
+        }
+        if (lane == 0) {
+          fence_proxy_async();  // the slot's previous reads before the new bulk writes
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // copied bytes -> bulk reads
+          issue_a(it);
+        }
+        inflight[sl] = it;
+      }
+      const bool all = __all_sync(0xffffffffu, mbar_wait(&bar_a[warp][sl], (uint32_t)((it >> 1) & 1)));
       if (all) {
-        consumed = it + 1;
+        inflight[sl] = -1;
       } else {
         failed = true;
         if (lane == 0) flag_timeout(a.status);
@@ -816,12 +861,12 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       ItemA<FMT>::dot(sa, xrow(it), it % KC, lane, ga, ua);
       const float a0 = ItemA<FMT>::gs0(sa), a1 = ItemA<FMT>::gs1(sa);
       __syncwarp();  // slot 0 read by every lane
-      if (it + 2 < nitA) {
+      if (it + 2 < nitA && !deferred(it + 2)) {
         if (lane == 0) {
           fence_proxy_async();
           issue_a(it + 2);
         }
-        issued = it + 3;
+        inflight[0] = it + 2;
       }
       float b0 = 1.f, b1 = 1.f;
       if (two) {
@@ -831,12 +876,12 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
         b0 = ItemA<FMT>::gs0(sb);
         b1 = ItemA<FMT>::gs1(sb);
         __syncwarp();
-        if (it + 3 < nitA) {
+        if (it + 3 < nitA && !deferred(it + 3)) {
           if (lane == 0) {
             fence_proxy_async();
             issue_a(it + 3);
           }
-          issued = it + 4;
+          inflight[1] = it + 3;
         }
       }
       if (KC == 1) {  // rows it and it + 1 complete
@@ -857,7 +902,8 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     }
     // after a timeout, wait (bounded) for this warp's copies still in flight
     if (failed && lane == 0)
-      for (int q = consumed; q < issued; ++q) mbar_wait(&bar_a[warp][q & 1], (uint32_t)((q >> 1) & 1));
+      for (int sl = 0; sl < 2; ++sl)
+        if (inflight[sl] >= 0) mbar_wait(&bar_a[warp][sl], (uint32_t)((inflight[sl] >> 1) & 1));
   }
   if (threadIdx.x < T) tk.wt[threadIdx.x] = cw * c2;  // read after the barrier
 
