@@ -46,6 +46,33 @@ def dist_env():
     return ws, rank, local
 
 
+# DRAM bytes per launch of the routed FFN kernel from an ncu capture, kept
+# beside the kernel source's hash: the figure is reported only while the
+# source is unchanged since the capture.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ffn_fused_kernel_routed_traffic.txt")
+FFN_SOURCE = os.path.join(ROOT, "expert_slot_cache_lru_gb300", "csrc", "ffn_stream.cu")
+
+
+def source_hash(path: str) -> str:
+    import hashlib
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def routed_traffic() -> dict | None:
+    """{"bytes_per_launch": ..., "source": ...} from the traffic file, or None
+    when it is missing or the kernel source changed since the capture."""
+    try:
+        kv = dict(line.split("=", 1) for line in open(TRAFFIC_FILE).read().split("\n")
+                  if "=" in line and not line.startswith("#"))
+        if kv.get("source_sha256_16") != source_hash(FFN_SOURCE):
+            return None
+        return {"bytes_per_launch": float(kv["dram_bytes_per_launch"]),
+                "source": os.path.relpath(TRAFFIC_FILE, ROOT)}
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -521,6 +548,17 @@ def run_native(args) -> None:
                  n_layers=args.layers, n_slots=args.slots, fused=not args.unfused)
     L = dec.w.n_layers
     props = torch.cuda.get_device_properties(local)
+    # settle: decode for a few seconds first.  Host reads over the CPU link
+    # (the miss gathers) are slower for the first seconds of activity after an
+    # idle period; the timed tokens then measure the steady state.
+    t_settle = time.perf_counter()
+    settle_tokens = 0
+    while time.perf_counter() - t_settle < args.settle_s:
+        for _ in range(50):
+            dec.step()
+        settle_tokens += 50
+        torch.cuda.synchronize()
+    settle_s = time.perf_counter() - t_settle
     for _ in range(args.warmup):
         dec.step()
     torch.cuda.synchronize()
@@ -550,9 +588,15 @@ def run_native(args) -> None:
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     tok_s = ws * args.steps / (ms * 1e-3)
+    if args.routed_only:  # profiler runs: the routed FFN kernel's roofline graph only
+        if rank == 0:
+            roof = dec.routed_gemv_roofline(steps=2)
+            print(json.dumps({"routed_only": True, "layers": L, **roof}), flush=True)
+        return
     if args.decode_only:  # profiler runs: the timed decode only, no sub-measurements
         if rank == 0:
             print(json.dumps({"decode_only": True, "layers": L, "slots": dec.w.n_slots,
+                              "settle_tokens": settle_tokens,
                               "tok_s": round(tok_s, 2), "ms_per_step": round(ms / args.steps, 4)}),
                   flush=True)
         return
@@ -576,6 +620,7 @@ def run_native(args) -> None:
     adm = admission_sweep(local)
     wide = wide_step(local)
     hbm = peaks.get("hbm_gbs", 6800.0)
+    tr = routed_traffic()
     line = {
         "metric": METRIC,
         "value": round(tok_s, 2),
@@ -600,14 +645,20 @@ def run_native(args) -> None:
                              "four launches on one stream"),
                    "overlap": not args.serial, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2: each token streams ~637 MB of expert weights",
-                   "cache_warmup_tokens": args.warm_tokens},
+                   "cache_warmup_tokens": args.warm_tokens,
+                   "settle": f"{settle_tokens} untimed tokens ({settle_s:.1f} s) before the "
+                             f"{args.warmup} warm-up steps: host-link reads reach their steady "
+                             f"rate only after seconds of activity"},
         # per layer: the admission and one fused launch (gather + shared + routed);
         # unfused: admission, demand gather, shared-expert FFN, routed FFN + combine
         "gpu_launches": args.steps * (4 if args.unfused else 2) * L,
         "e2e": e2e,
         "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1),
                      "peak": hbm, "unit": "GB/s",
-                     "frac": round(roof["achieved_gbs"] / hbm, 4), "traffic": None,
+                     "frac": round(roof["achieved_gbs"] / hbm, 4),
+                     "traffic": round(tr["bytes_per_launch"]) if tr else None,
+                     "traffic_source": tr["source"] if tr else
+                     "null: no capture of the current kernel source",
                      "kernel": roof["kernel"], "avg_launch_us": round(roof["avg_launch_us"], 3),
                      "bytes_per_launch": round(roof["bytes_per_launch"]),
                      "peak_source": f"{peaks['_source']} (MEASURED_PEAKS.json hbm_gbs)"},
@@ -686,6 +737,8 @@ def main():
     ap.add_argument("--unfused", action="store_true",
                     help="four launches per layer (side-stream gather joined by events) instead of "
                          "the fused layer")
+    ap.add_argument("--settle-s", type=float, default=3.0,
+                    help="seconds of untimed decode before the warm-up steps (steady state)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--warm-tokens", type=int, default=WARM_TOKENS,
@@ -694,6 +747,9 @@ def main():
     ap.add_argument("--slots", type=int, default=None, help="profiler case: fewer slots")
     ap.add_argument("--decode-only", action="store_true",
                     help="time the decode only and print a short line (profiler runs)")
+    ap.add_argument("--routed-only", action="store_true",
+                    help="after the decode, run only the routed FFN kernel's roofline graph "
+                         "(profiler runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
