@@ -544,6 +544,10 @@ def run_native(args) -> None:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
                                 device_id=torch.device("cuda", local))
     peaks = measured_peaks()
+    if args.wide_only:  # profiler runs: the wide decode step alone
+        if rank == 0:
+            print(json.dumps({"wide_only": True, **wide_step(local)}), flush=True)
+        return
     dec = Decode(local, overlap=not args.serial, warm_tokens=args.warm_tokens,
                  n_layers=args.layers, n_slots=args.slots, fused=not args.unfused)
     L = dec.w.n_layers
@@ -747,6 +751,8 @@ def main():
     ap.add_argument("--slots", type=int, default=None, help="profiler case: fewer slots")
     ap.add_argument("--decode-only", action="store_true",
                     help="time the decode only and print a short line (profiler runs)")
+    ap.add_argument("--wide-only", action="store_true",
+                    help="run only the wide decode step sub-measurement (profiler runs)")
     ap.add_argument("--routed-only", action="store_true",
                     help="after the decode, run only the routed FFN kernel's roofline graph "
                          "(profiler runs)")

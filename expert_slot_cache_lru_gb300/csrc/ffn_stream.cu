@@ -31,6 +31,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -937,68 +938,89 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
 
   // ---------------------------------------------------------------- phase B
   // warp w takes items [w*ipw, (w+1)*ipw), in runs of up to NG of one task
-  // (NG = 4 for NVFP4; 2 for bf16, whose rows hold twice the registers)
+  // (NG = 4 for NVFP4; 2 for bf16, whose rows hold twice the registers).  The
+  // run loop is instantiated for the lane's element count (M = I / 512), and a
+  // run whose rows were all staged reads them with shared-memory loads.
   {
     constexpr int NG = FMT == MOE_W_NVFP4 ? 4 : 2;
     const int ipw = (NQ + kW - 1) / kW;
     const int q0w = min(NQ, warp * ipw), q1w = min(NQ, q0w + ipw);
-    float hv[32];
-    int ht = -1;
-    for (int q = q0w; q < q1w;) {
-      const int bi = q >= cntA ? 1 : 0;
-      const int b = bi ? bB : bA, qb = bi ? cntA : 0;
-      const int nlo = nlo_of(b), nlen = nlen_of(b);
-      const int t = ts[b] + (q - qb) / nlen;
-      const int n0 = nlo + (q - qb) % nlen;
-      const int run_end = min(q1w, qb + (t - ts[b] + 1) * nlen);  // same task
-      const int cnt = min(NG, run_end - q);
-      if (t != ht) {  // this task's h slice into registers
-        const float* hp = hsm + (size_t)(t - tlo) * I;
-        if (FMT == MOE_W_NVFP4) {
+    auto run_b = [&](auto mtag) {
+      constexpr int M = decltype(mtag)::value;
+      if (q0w >= q1w) return;
+      // item q0w: batch row b, task t, row r of the task's nlen rows
+      int b = q0w >= cntA ? bB : bA;
+      int nlo = nlo_of(b), nlen = nlen_of(b);
+      const int qr = q0w - (q0w >= cntA ? cntA : 0);
+      int t = ts[b] + qr / nlen, r = qr % nlen;
+      float hv[16 * M];
+      int ht = -1;
+      for (int q = q0w; q < q1w;) {
+        const int cnt = min(NG, min(q1w - q, nlen - r));  // items of this run: one task
+        if (t != ht) {  // this task's h slice into registers
+          const float* hp = hsm + (size_t)(t - tlo) * I;
+          if (FMT == MOE_W_NVFP4) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (j < 4 * m) {
-              const float4 v = reinterpret_cast<const float4*>(hp + lane * 16 * m)[j];
+            for (int j = 0; j < 4 * M; ++j) {
+              const float4 v = reinterpret_cast<const float4*>(hp + lane * 16 * M)[j];
               hv[4 * j] = v.x, hv[4 * j + 1] = v.y, hv[4 * j + 2] = v.z, hv[4 * j + 3] = v.w;
             }
-        } else {
+          } else {
 #pragma unroll
-          for (int s = 0; s < 4; ++s)
-            if (s < 2 * m) {
+            for (int s = 0; s < 2 * M; ++s) {
               const float4 v0 = *reinterpret_cast<const float4*>(hp + 256 * s + 8 * lane);
               const float4 v1 = *reinterpret_cast<const float4*>(hp + 256 * s + 8 * lane + 4);
               hv[8 * s] = v0.x, hv[8 * s + 1] = v0.y, hv[8 * s + 2] = v0.z, hv[8 * s + 3] = v0.w;
               hv[8 * s + 4] = v1.x, hv[8 * s + 5] = v1.y, hv[8 * s + 6] = v1.z, hv[8 * s + 7] = v1.w;
             }
+          }
+          ht = t;
         }
-        ht = t;
-      }
-      ItemB<FMT> itm[NG];
+        ItemB<FMT> itm[NG];
+        const bool copied = LAYER && tk.pe[t] >= 0;  // copied in by this launch: not staged
+        if (!copied && q + cnt <= qs) {
 #pragma unroll
-      for (int j = 0; j < NG; ++j) {
-        if (j >= cnt) continue;
-        const int qq = q + j, n = n0 + j;
-        const uint8_t* cp;
-        const uint8_t* sp;
-        if (qq < qs && !(LAYER && tk.pe[t] >= 0)) {
-          cp = stC + (size_t)qq * CB;
-          sp = stS + (size_t)qq * SB;
+          for (int j = 0; j < NG; ++j)
+            if (j < cnt)
+              itemb_load<FMT>(itm[j], stC + (size_t)(q + j) * CB, stS + (size_t)(q + j) * SB, M,
+                              lane);
         } else {
           const uint8_t* blob = tk.blob[t];
-          cp = blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)n * CB;
-          sp = blob + o.scale[2] + (size_t)n * SB;
-        }
-        itemb_load<FMT>(itm[j], cp, sp, m, lane);
-      }
-      float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < NG; ++j) p[j] = j < cnt ? itemb_dot<FMT>(itm[j], hv, m) : 0.f;
-      const float v = reduce4(p, lane);
-      const int j = lane >> 3;
-      if ((lane & 7) == 0 && j < cnt)
-        ysm[(size_t)t * perB + (b * H + n0 + j - ru0)] = v;
-      q += cnt;
-    }
+          for (int j = 0; j < NG; ++j) {
+            if (j >= cnt) continue;
+            const int qq = q + j, n = nlo + r + j;
+            if (!copied && qq < qs)
+              itemb_load<FMT>(itm[j], stC + (size_t)qq * CB, stS + (size_t)qq * SB, M, lane);
+            else
+              itemb_load<FMT>(itm[j],
+                              blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)n * CB,
+                              blob + o.scale[2] + (size_t)n * SB, M, lane);
+          }
+        }
+        float p[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < NG; ++j) p[j] = j < cnt ? itemb_dot<FMT>(itm[j], hv, M) : 0.f;
+        const float v = reduce4(p, lane);
+        const int j = lane >> 3;
+        if ((lane & 7) == 0 && j < cnt) ysm[(size_t)t * perB + (b * H + nlo + r + j - ru0)] = v;
+        q += cnt;
+        r += cnt;
+        if (r == nlen) {  // the task's rows are done: the next task, maybe of the next batch row
+          r = 0;
+          ++t;
+          if (t == ts[b + 1] && b != bB) {
+            b = bB;
+            nlo = nlo_of(b);
+            nlen = nlen_of(b);
+          }
+        }
+      }
+    };
+    if (m == 1)
+      run_b(std::integral_constant<int, 1>{});
+    else
+      run_b(std::integral_constant<int, 2>{});
   }
   __syncthreads();  // every (task, row) result in ysm
   // combine: each output row, its tasks in route order (j ascending), then + ys
