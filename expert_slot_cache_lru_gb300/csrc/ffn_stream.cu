@@ -303,7 +303,7 @@ struct ItemA;
 template <>
 struct ItemA<MOE_W_NVFP4> {
   static constexpr int CW = 2048;
-  static constexpr int BYTES = 2 * 1024 + 2 * 128 + 16;
+  static constexpr int BYTES = 2 * 1024 + 2 * 128;
   static __device__ __forceinline__ uint32_t issue(uint8_t* slot, const uint8_t* blob,
                                                    const BlobOff& o, int H, int i, int c,
                                                    uint64_t* bar, uint64_t pol) {
@@ -312,8 +312,13 @@ struct ItemA<MOE_W_NVFP4> {
     bulk_g2s(slot + 1024, blob + o.code[1] + cr, 1024, bar, pol);
     bulk_g2s(slot + 2048, blob + o.scale[0] + sr, 128, bar, pol);
     bulk_g2s(slot + 2176, blob + o.scale[1] + sr, 128, bar, pol);
-    bulk_g2s(slot + 2304, blob + o.glob, 16, bar, pol);
     return BYTES;
+  }
+  // the gate and up global scales, read with a plain load (a 16-byte bulk copy
+  // would cost the SM's bulk-copy unit as much as a 1 KiB one); not through the
+  // read-only path, since a fused layer writes the slot earlier in the launch
+  static __device__ __forceinline__ float2 glob(const uint8_t* blob, const BlobOff& o) {
+    return *reinterpret_cast<const float2*>(blob + o.glob);
   }
   // per-lane partial gate / up sums over the lane's elements of chunk c
   static __device__ __forceinline__ void dot(const uint8_t* slot, const uint4* xr, int c, int lane,
@@ -338,12 +343,6 @@ struct ItemA<MOE_W_NVFP4> {
     u = fmaf(dot8_fp4_h(u1.x, x0) + dot8_fp4_h(u1.y, x1), su1.x, u);
     u = fmaf(dot8_fp4_h(u1.z, x2) + dot8_fp4_h(u1.w, x3), su1.y, u);
   }
-  static __device__ __forceinline__ float gs0(const uint8_t* slot) {
-    return *reinterpret_cast<const float*>(slot + 2304);
-  }
-  static __device__ __forceinline__ float gs1(const uint8_t* slot) {
-    return *reinterpret_cast<const float*>(slot + 2308);
-  }
 };
 template <>
 struct ItemA<MOE_W_BF16> {
@@ -366,8 +365,9 @@ struct ItemA<MOE_W_BF16> {
       us = dot8_bf16_bf(*reinterpret_cast<const uint4*>(slot + 1024 + 512 * s + lane * 16), xv, us);
     }
   }
-  static __device__ __forceinline__ float gs0(const uint8_t*) { return 1.f; }
-  static __device__ __forceinline__ float gs1(const uint8_t*) { return 1.f; }
+  static __device__ __forceinline__ float2 glob(const uint8_t*, const BlobOff&) {
+    return make_float2(1.f, 1.f);
+  }
 };
 constexpr int kSlotBytes = 2432;  // >= ItemA<*>::BYTES, a multiple of 128
 
@@ -684,11 +684,16 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const uint64_t pol = l2_evict_first();
   // pieces per expert (a fused layer always has slot storage; 1 keeps the others well defined)
   const int ppe = LAYER ? max(1, (int)((st.slot_bytes + kPiece - 1) / kPiece)) : 1;
+  // the gate/up global scales of the item in flight on each slot (lane 0)
+  float2 gsl0 = make_float2(1.f, 1.f), gsl1 = make_float2(1.f, 1.f);
   auto issue_a = [&](int it) {  // lane 0
     const int t = task_of(it), sl = it & 1;
     mbar_expect_tx(&bar_a[warp][sl], ItemA<FMT>::BYTES);
     ItemA<FMT>::issue(slots + sl * kSlotBytes, tk.blob[t], o, H, row_of(it), it % KC,
                       &bar_a[warp][sl], pol);
+    const float2 g = ItemA<FMT>::glob(tk.blob[t], o);
+    gsl0 = sl ? gsl0 : g;
+    gsl1 = sl ? g : gsl1;
   };
   // an item of an expert this launch copies in is requested only once the copy
   // is complete (see wait_copied below); every other item as soon as its slot is free
@@ -860,7 +865,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       if (!wait_a(it)) break;
       const uint8_t* sa = slots;
       ItemA<FMT>::dot(sa, xrow(it), it % KC, lane, ga, ua);
-      const float a0 = ItemA<FMT>::gs0(sa), a1 = ItemA<FMT>::gs1(sa);
+      const float a0 = gsl0.x, a1 = gsl0.y;
       __syncwarp();  // slot 0 read by every lane
       if (it + 2 < nitA && !deferred(it + 2)) {
         if (lane == 0) {
@@ -874,8 +879,8 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
         if (!wait_a(it + 1)) break;
         const uint8_t* sb = slots + kSlotBytes;
         ItemA<FMT>::dot(sb, xrow(it + 1), (it + 1) % KC, lane, gb, ub);
-        b0 = ItemA<FMT>::gs0(sb);
-        b1 = ItemA<FMT>::gs1(sb);
+        b0 = gsl1.x;
+        b1 = gsl1.y;
         __syncwarp();
         if (it + 3 < nitA && !deferred(it + 3)) {
           if (lane == 0) {
