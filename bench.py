@@ -642,7 +642,8 @@ def run_native(args) -> None:
                                "top-8, H 2048, I 512, gated shared expert I 512, 3164-slot LRU, "
                                "batch 1, Zipf(1.1) routing with reuse (~28 misses/token)",
                    "global_batch": ws, "graph": "one CUDA graph per token (40 layers)",
-                   "layer": ("two launches: admission, then gather + shared + routed fused"
+                   "layer": ("one launch: CTA 0 admits while the others copy the misses into "
+                             "staging, run the shared and routed experts and combine"
                              if not args.unfused else
                              "four launches: admission, gather on a side stream (events), "
                              "shared expert, routed experts" if not args.serial else
@@ -653,9 +654,9 @@ def run_native(args) -> None:
                    "settle": f"{settle_tokens} untimed tokens ({settle_s:.1f} s) before the "
                              f"{args.warmup} warm-up steps: host-link reads reach their steady "
                              f"rate only after seconds of activity"},
-        # per layer: the admission and one fused launch (gather + shared + routed);
+        # per layer: one launch (admission, gathers, shared + routed experts);
         # unfused: admission, demand gather, shared-expert FFN, routed FFN + combine
-        "gpu_launches": args.steps * (4 if args.unfused else 2) * L,
+        "gpu_launches": args.steps * (4 if args.unfused else 1) * L,
         "e2e": e2e,
         "roofline": {"bound": "hbm", "achieved": round(roof["achieved_gbs"], 1),
                      "peak": hbm, "unit": "GB/s",

@@ -49,7 +49,8 @@ __host__ __device__ inline int pool_of(const DevState& st, int layer) {
 constexpr int kAdmitThreads = 1024;  // admission / prefetch: one CTA of 32 warps
 
 // ---------------------------------------------------------------- block helpers
-// All helpers assume blockDim.x == kAdmitThreads and are called by every thread.
+// All helpers assume blockDim.x == NT (a multiple of 32, at most 1024) and are
+// called by every thread.
 
 struct BlockScratch {
   int warp_i[32];
@@ -68,33 +69,38 @@ __device__ __forceinline__ int warp_incl_scan(int v) {
 }
 
 // Exclusive prefix sum over the block in thread order; *total receives the sum.
+template <int NT = kAdmitThreads>
 __device__ __forceinline__ int block_excl_scan(int v, BlockScratch& bs, int* total) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int incl = warp_incl_scan(v);
   if (lane == 31) bs.warp_i[w] = incl;
   __syncthreads();
   if (w == 0) {
-    int t = bs.warp_i[lane];
+    int t = lane < NW ? bs.warp_i[lane] : 0;
     t = warp_incl_scan(t);
     bs.warp_i[lane] = t;
   }
   __syncthreads();
   const int excl = incl - v + (w > 0 ? bs.warp_i[w - 1] : 0);
-  *total = bs.warp_i[31];
+  *total = bs.warp_i[NW - 1];
   __syncthreads();
   return excl;
 }
 
+template <int NT = kAdmitThreads>
 __device__ __forceinline__ int block_sum(int v, BlockScratch& bs) {
   int total;
-  (void)block_excl_scan(v, bs, &total);
+  (void)block_excl_scan<NT>(v, bs, &total);
   return total;
 }
 
 // Block-wide min and max of 64-bit values.
+template <int NT = kAdmitThreads>
 __device__ __forceinline__ void block_minmax_u64(unsigned long long mn, unsigned long long mx,
                                                  BlockScratch& bs, unsigned long long* omin,
                                                  unsigned long long* omax) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -109,8 +115,8 @@ __device__ __forceinline__ void block_minmax_u64(unsigned long long mn, unsigned
   }
   __syncthreads();
   if (w == 0) {
-    mn = bs.warp_u[lane];
-    mx = bs.warp_v[lane];
+    mn = lane < NW ? bs.warp_u[lane] : ~0ull;
+    mx = lane < NW ? bs.warp_v[lane] : 0ull;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       unsigned long long a = __shfl_xor_sync(0xffffffffu, mn, o);
@@ -133,6 +139,7 @@ __device__ __forceinline__ void block_minmax_u64(unsigned long long mn, unsigned
 // Each returns the cudaError_t of the launch.
 
 size_t admit_smem_bytes(int E, int S);
+bool admit_cached(int E, int S);  // the admission keeps the pool in shared memory
 cudaError_t launch_admit(const DevState& st, int layer, const int32_t* ids, int32_t* out, int R,
                          int cap, cudaStream_t s);
 cudaError_t launch_prefetch(const DevState& st, int layer, const int32_t* pred, int n,
@@ -152,6 +159,12 @@ struct FfnScratch {
   float* xinv;      // [max_rows] inverse of the per-row x scale
   float* y;         // [max_routes * H] per-route down projections (grouped path)
   int* gdone;       // [max_routes] pieces of each demand-plan expert copied by a fused layer
+  // a fused layer with the admission inside the launch (three counters that only grow)
+  unsigned long long* epoch;   // launches (each CTA adds one)
+  unsigned long long* pseq;    // the admission's publication sequence
+  unsigned long long* bar2;    // grid barrier of the computing CTAs
+  uint8_t* stage;              // [stage_n] slot-sized areas the step's misses are copied into
+  int stage_n;
 };
 
 cudaError_t launch_shared_expert(int wfmt, int H, int Is, const void* x, int n_rows,
@@ -185,6 +198,18 @@ cudaError_t launch_layer_stream(const DevState& st, int wfmt, int H, int I, int 
                                 const void* gate_w, const int32_t* plan0, const int32_t* plan1,
                                 void* out, FfnScratch sc, unsigned long long* status,
                                 cudaStream_t s);
+
+// One launch for a whole decode-sized layer including its admission: CTA 0
+// admits (and prefetch-admits layer + 1 when pred is given) while the other
+// CTAs stream the resident experts; the rest as launch_layer_stream.
+bool layer_admit_supported(const DevState& st, int wfmt, int H, int I, int n_rows, int k,
+                           bool shared);
+cudaError_t launch_layer_admit(const DevState& st, int wfmt, int H, int I, int layer,
+                               const void* x, const int32_t* ids, int32_t* slot_out,
+                               const float* w, int n_rows, int k, int cap, const int32_t* pred,
+                               int n_pred, const uint8_t* shared_blob, const void* gate_w,
+                               int32_t* plan1, void* out, FfnScratch sc,
+                               unsigned long long* status, cudaStream_t s);
 
 // Routed FFNs for wide steps, grouped by expert (grouped.cu).
 bool grouped_supported(int wfmt, int H, int I, int E);

@@ -33,6 +33,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "admit_body.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -53,7 +54,7 @@ constexpr int kPiece = 4096;       // gather unit of the fused layer (one warp, 
 
 // What one launch computes: the routed experts, the gated shared expert, or
 // (fused layer) both plus the gather of the step's missed experts.
-enum { kRouted = 0, kShared = 1, kLayer = 2 };
+enum { kRouted = 0, kShared = 1, kLayer = 2, kLayerAdmit = 3 };
 
 // ------------------------------------------------------------ PTX wrappers
 
@@ -75,6 +76,17 @@ __device__ __forceinline__ void fence_barrier_init() {
 // generic-proxy accesses of shared memory before async-proxy writes to it
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
@@ -241,8 +253,11 @@ struct Tasks {
   int n;
   int route[kMaxTasks];            // route index r = b*k + j; R + b for row b's shared task
   int b[kMaxTasks];                // batch row
-  int pe[kMaxTasks];               // fused layer: index in the demand plan, -1 = resident
+  int pe[kMaxTasks];               // fused layer: index in the demand plan, -1 = resident,
+                                   // kPending = not resident when the launch began
   int ord[kMaxTasks];              // phase-A task order (fused layer: copied-in tasks last)
+  unsigned char drop[kMaxTasks];   // admission inside: not admitted (fetch cap)
+  unsigned char pend[kMaxTasks];   // admission inside: not resident when the launch began
   int slot[kMaxTasks];             // slot id, -1 for the shared expert
   const uint8_t* blob[kMaxTasks];
   float wt[kMaxTasks];             // routing weight x down global scale
@@ -424,17 +439,18 @@ __device__ __forceinline__ float itemb_dot(const ItemB<FMT>& it, const float* hv
 
 // ---------------------------------------------------------------- grid barrier
 // One CTA per SM, launched cooperatively, so every CTA of the grid is resident.
-// `ctr` only grows: each launch adds gridDim.x, and a CTA waits until the count
-// reaches the next multiple of gridDim.x.  Release/acquire at GPU scope orders
-// the h written before the barrier with the reads after it.  Bounded spin.
-__device__ bool grid_barrier(unsigned long long* ctr, unsigned long long* status) {
+// `ctr` only grows: each launch adds n (the CTAs taking part), and a CTA waits
+// until the count reaches the next multiple of n.  Release/acquire at GPU
+// scope orders the h written before the barrier with the reads after it.
+// Bounded spin.
+__device__ bool grid_barrier(unsigned long long* ctr, unsigned long long* status, unsigned n) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     unsigned long long old;
     asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
-    const unsigned long long target = (old / gridDim.x + 1) * gridDim.x;
+    const unsigned long long target = (old / n + 1) * n;
     unsigned long long v = 0;
     const unsigned long long t0 = now_ns();
     int ok = 1;
@@ -489,18 +505,82 @@ struct FusedArgs {
   const int32_t* gplan0;       // demand plan: its experts are copied here and waited on
   const int32_t* gplan1;       // prefetch plan of the next layer (copied only), or null
   int* gdone;                  // [plan entries] pieces copied; zero at entry, reset here
+  // fused layer with the admission inside the launch: CTA 0 admits (and
+  // prefetch-admits), the other CTAs compute
+  const int32_t* ids;          // the step's expert ids [R]
+  int32_t* slot_out;           // [R] slot ids, written by the admission
+  int cap;                     // fetch cap (< 0: none)
+  const int32_t* pred;         // the next layer's predicted ids, or null
+  int n_pred;
+  int adm_cached;              // the admission keeps the pool in shared memory
+  unsigned long long* epoch;   // grows by gridDim.x per launch: launch j = old / gridDim.x
+  unsigned long long* pseq;    // 2j+1: slot ids and demand plan of launch j out; 2j+2: prefetch plan too
+  unsigned long long* bar2;    // grid barrier of the computing CTAs
+  uint8_t* stage;              // stage_n slot-sized areas the step's misses are copied into
+  int stage_n;                 // (0: misses wait for the admission and go to their slots)
 };
+
+constexpr int kPending = -2;
+constexpr int kPbWords = 128;  // admission inside: a bitmap over at most 4096 experts
+
+// CTA 0 of a layer launch with the admission inside: the admission of
+// a.layer (the same routine as the standalone kernel, on this CTA's threads),
+// then the prefetch admission of a.layer + 1 when predictions are given.  It
+// needs no word from the computing CTAs: a hit cannot be evicted by its own
+// admission, and an installed miss's map entry carries kMapPending until this
+// launch has copied it in, so a computing CTA reading the map sees a miss as
+// a miss whenever it reads.  It publishes its results with release stores to
+// a.pseq: 2j + 1 once the slot ids and the demand plan of launch j are out,
+// 2j + 2 once the prefetch plan is too.
+__device__ __noinline__ void admit_cta(const DevState& st, const FusedArgs& a, uint8_t* sm,
+                                       unsigned long long j) {
+  using namespace admission;
+  AdmitShared<kT>& sh = *reinterpret_cast<AdmitShared<kT>*>(sm);
+  unsigned char* dyn = sm + (sizeof(AdmitShared<kT>) + 127) / 128 * 128;
+  auto none = [] {};
+  if (a.adm_cached)
+    admit_body<true, kT>(st, a.layer, a.ids, a.slot_out, a.R, a.cap, dyn, sh, none, kMapPending);
+  else
+    admit_body<false, kT>(st, a.layer, a.ids, a.slot_out, a.R, a.cap, dyn, sh, none, kMapPending);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) st_release_u64(a.pseq, 2 * j + 1);
+  if (a.pred && a.n_pred > 0) {
+    prefetch_body<kT>(st, a.layer + 1, a.pred, a.n_pred, const_cast<int32_t*>(a.gplan1),
+                      reinterpret_cast<int*>(dyn), sh);
+    __threadfence();
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) st_release_u64(a.pseq, 2 * j + 2);
+}
 
 template <int FMT, int MODE>
 __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) {
-  constexpr bool SHARED = MODE == kShared, LAYER = MODE == kLayer;
+  constexpr bool SHARED = MODE == kShared, ADMIT = MODE == kLayerAdmit;
+  constexpr bool LAYER = MODE == kLayer || ADMIT;
   extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ unsigned long long s_j;  // admission inside: this launch's index
+  if (ADMIT) {  // every CTA of launch j adds one to a.epoch: j = old / gridDim.x
+    if (threadIdx.x == 32) s_j = atomicAdd(a.epoch, 1ull) / gridDim.x;
+    if (blockIdx.x == 0) {
+      __syncthreads();
+      admit_cta(st, a, sm, s_j);
+      return;
+    }
+  }
+  // the computing CTAs: all of them, or all but CTA 0 when it admits
+  const int GF = (int)gridDim.x - (ADMIT ? 1 : 0), cta = (int)blockIdx.x - (ADMIT ? 1 : 0);
   __shared__ Tasks tk;
   __shared__ int ts[kMaxRows + 1];         // tasks of batch row b: [ts[b], ts[b+1])
   __shared__ unsigned int xmax[kMaxRows];  // per row max |x| (float bits, only when > 2^14)
   __shared__ float xinv[kMaxRows];         // per row 1 / (power-of-two scale applied to x)
   __shared__ uint64_t bar_a[kW][2];        // per-warp phase-A slot barriers
   __shared__ uint64_t bar_b;               // the staged phase-B rows
+  __shared__ int s_npend;                  // admission inside: tasks not resident at entry
+  __shared__ int s_npx;                    // ... their distinct experts (staging entries)
+  __shared__ int s_staged;                 // ... copied into the staging area (else: slots)
+  __shared__ unsigned s_pbits[kPbWords];   // ... bitmap of those experts
+  __shared__ int s_pexp[kMaxRoutes];       // ... in ascending id: staging entry -> expert
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, I = a.I, k = a.k, n_rows = a.n_rows;
   const int m = I / 512;                                   // 16-element groups per lane (B)
@@ -512,8 +592,8 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
 
   // this CTA's output rows (phase B): at most two batch rows (perB <= H)
   const int UB = n_rows * H;
-  const int perB = (UB + gridDim.x - 1) / gridDim.x;
-  const int ru0 = min(UB, perB * (int)blockIdx.x), ru1 = min(UB, ru0 + perB);
+  const int perB = (UB + GF - 1) / GF;
+  const int ru0 = min(UB, perB * cta), ru1 = min(UB, ru0 + perB);
 
   // ---- entry: the slot ids (warp 0) and x (everyone) in flight at once
   const int nx8 = n_rows * H / 8;
@@ -530,20 +610,71 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     ysv[j] = (MODE == kRouted && a.ys && ru < ru1) ? a.ys[ru] : 0.f;
   }
   if (threadIdx.x < kMaxRows) xmax[threadIdx.x] = 0u;
+  auto slot_blob = [&](int s) -> const uint8_t* {
+    return st.slots + ((size_t)pool_of(st, a.layer) * st.S + s) * st.stride;
+  };
   if (warp == 0) {
     const uint8_t* b0 = nullptr;
     const uint8_t* b1 = nullptr;
-    auto resolve = [&](int r) -> const uint8_t* {
-      if (a.fixed_blob) return a.fixed_blob;
-      const int s = a.slot_ids[r];
-      return (unsigned)s < (unsigned)st.S
-                 ? st.slots + ((size_t)pool_of(st, a.layer) * st.S + s) * st.stride
-                 : nullptr;
+    int sl0 = -1, sl1 = -1;       // slot ids (admission inside: the map entry at entry)
+    int e0 = -1, e1 = -1;         // admission inside: expert ids
+    bool v0 = false, v1 = false;  // the route is a task
+    auto resolve = [&](int r, int& slot, int& e) -> bool {
+      if (a.fixed_blob) return true;
+      if (ADMIT) {  // a valid id is a task: resident now, or being admitted by CTA 0
+        e = a.ids[r];
+        if ((unsigned)e >= (unsigned)st.E) return false;
+        slot = st.map[a.layer * st.E + e];  // -1, or kMapPending set: not resident
+        return true;
+      }
+      slot = a.slot_ids[r];
+      return (unsigned)slot < (unsigned)st.S;
     };
-    if (lane < a.R) b0 = resolve(lane);
-    if (lane + 32 < a.R) b1 = resolve(lane + 32);
-    const unsigned m0 = __ballot_sync(0xffffffffu, b0 != nullptr);
-    const unsigned m1 = __ballot_sync(0xffffffffu, b1 != nullptr);
+    if (lane < a.R) v0 = resolve(lane, sl0, e0);
+    if (lane + 32 < a.R) v1 = resolve(lane + 32, sl1, e1);
+    if (v0) b0 = a.fixed_blob ? a.fixed_blob : (sl0 >= 0 ? slot_blob(sl0) : nullptr);
+    if (v1) b1 = sl1 >= 0 ? slot_blob(sl1) : nullptr;
+    int pe0 = -1, pe1 = -1;
+    const bool p0 = ADMIT && v0 && sl0 < 0, p1 = ADMIT && v1 && sl1 < 0;  // missed
+    if (ADMIT) {
+      // the distinct missed experts in ascending id: the staging entries
+      const int nw = (st.E + 31) / 32;
+      for (int w = lane; w < nw; w += 32) s_pbits[w] = 0;
+      __syncwarp();
+      if (p0) atomicOr(&s_pbits[e0 >> 5], 1u << (e0 & 31));
+      if (p1) atomicOr(&s_pbits[e1 >> 5], 1u << (e1 & 31));
+      __syncwarp();
+      auto rank_of = [&](int e) {
+        int r = __popc(s_pbits[e >> 5] & ((1u << (e & 31)) - 1u));
+        for (int w = 0; w < (e >> 5); ++w) r += __popc(s_pbits[w]);
+        return r;
+      };
+      const int x0 = p0 ? rank_of(e0) : -1, x1 = p1 ? rank_of(e1) : -1;
+      if (p0) s_pexp[x0] = e0;
+      if (p1) s_pexp[x1] = e1;
+      int npx = 0;
+      for (int w = lane; w < nw; w += 32) npx += __popc(s_pbits[w]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) npx += __shfl_xor_sync(0xffffffffu, npx, off);
+      // uncapped steps copy their misses at once into staging entries; with a
+      // fetch cap (or too many misses) they wait for the admission's slots
+      const bool stg = a.stage && a.cap < 0 && npx <= a.stage_n;
+      if (stg) {
+        if (p0) b0 = a.stage + (size_t)x0 * st.stride, pe0 = x0;
+        if (p1) b1 = a.stage + (size_t)x1 * st.stride, pe1 = x1;
+      } else {
+        pe0 = p0 ? kPending : -1;
+        pe1 = p1 ? kPending : -1;
+      }
+      const int np = __popc(__ballot_sync(0xffffffffu, p0)) + __popc(__ballot_sync(0xffffffffu, p1));
+      if (lane == 0) {
+        s_npend = np;
+        s_npx = npx;
+        s_staged = stg;
+      }
+    }
+    const unsigned m0 = __ballot_sync(0xffffffffu, v0);
+    const unsigned m1 = __ballot_sync(0xffffffffu, v1);
     const unsigned lt = (1u << lane) - 1u;
     // valid routes below route index lim
     auto below = [&](int lim) {
@@ -552,22 +683,25 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       return __popc(m0 & a0) + __popc(m1 & a1);
     };
     const int spr = (LAYER && a.shared_blob) ? 1 : 0;  // shared tasks per row (after its routes)
-    auto put = [&](int p, int r, int b, const uint8_t* blob, int slot) {
+    auto put = [&](int p, int r, int b, const uint8_t* blob, int slot, int pe, bool pend) {
       tk.route[p] = r;
       tk.b[p] = b;
       tk.blob[p] = blob;
       tk.slot[p] = slot;
-      tk.pe[p] = -1;
+      tk.pe[p] = pe;
+      tk.drop[p] = 0;
+      tk.pend[p] = pend;
     };
-    if (b0) {
+    if (v0) {
       const int b = SHARED ? lane : lane / k;
-      put(__popc(m0 & lt) + spr * b, lane, b, b0, SHARED ? -1 : a.slot_ids[lane]);
+      put(__popc(m0 & lt) + spr * b, lane, b, b0, SHARED ? -1 : sl0, pe0, p0);
     }
-    if (b1) {
+    if (v1) {
       const int b = (lane + 32) / k;
-      put(__popc(m0) + __popc(m1 & lt) + spr * b, lane + 32, b, b1, a.slot_ids[lane + 32]);
+      put(__popc(m0) + __popc(m1 & lt) + spr * b, lane + 32, b, b1, sl1, pe1, p1);
     }
-    if (spr && lane < n_rows) put(below((lane + 1) * k) + lane, a.R + lane, lane, a.shared_blob, -1);
+    if (spr && lane < n_rows)
+      put(below((lane + 1) * k) + lane, a.R + lane, lane, a.shared_blob, -1, -1, false);
     if (lane == 0) tk.n = __popc(m0) + __popc(m1) + spr * n_rows;
     if (lane <= n_rows) ts[lane] = below(lane * k) + spr * lane;  // first task of row `lane`
   }
@@ -589,26 +723,33 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const int T = tk.n;
   // fused layer: the demand plan entry of each task whose expert is being
   // copied in by this launch (its rows wait for the copy)
-  const int n_pl0 = LAYER && a.gplan0 ? a.gplan0[0] : 0;
-  const int n_pl1 = LAYER && a.gplan1 ? a.gplan1[0] : 0;
+  // (admission inside: the plans are not known yet, see ADMIT below)
+  const int n_pl0 = LAYER && !ADMIT && a.gplan0 ? a.gplan0[0] : 0;
+  const int n_pl1 = LAYER && !ADMIT && a.gplan1 ? a.gplan1[0] : 0;
+  const unsigned long long seq0 = ADMIT ? 2 * s_j : 0;  // a.pseq before this launch's admission
+  const int npend = ADMIT ? s_npend : 0;          // tasks whose expert was not resident at entry
+  const int npx = ADMIT ? s_npx : 0;              // ... their distinct experts
+  const bool staged = ADMIT && s_staged;          // ... copied into staging entries at once
   if (LAYER && warp == 0) {
-    for (int t = lane; t < T; t += 32) {
-      int pe = -1;
-      if (tk.slot[t] >= 0)
-        for (int i = 0; i < n_pl0; ++i)
-          if (a.gplan0[1 + 3 * i] == tk.slot[t]) pe = i;
-      tk.pe[t] = pe;
+    if (!ADMIT) {
+      for (int t = lane; t < T; t += 32) {
+        int pe = -1;
+        if (tk.slot[t] >= 0)
+          for (int i = 0; i < n_pl0; ++i)
+            if (a.gplan0[1 + 3 * i] == tk.slot[t]) pe = i;
+        tk.pe[t] = pe;
+      }
     }
     __syncwarp();
     // phase-A order: resident tasks, then the ones this launch copies in, so
     // that their rows are the last item of the warps that hold them
     int nres = 0;
     for (int t0 = 0; t0 < T; t0 += 32)
-      nres += __popc(__ballot_sync(0xffffffffu, t0 + lane < T && tk.pe[t0 + lane] < 0));
+      nres += __popc(__ballot_sync(0xffffffffu, t0 + lane < T && tk.pe[t0 + lane] == -1));
     const unsigned lt = (1u << lane) - 1u;
     for (int t0 = 0, cr = 0, cm = nres; t0 < T; t0 += 32) {
       const int t = t0 + lane;
-      const bool res = t < T && tk.pe[t] < 0, mis = t < T && !res;
+      const bool res = t < T && tk.pe[t] == -1, mis = t < T && !res;
       const unsigned br = __ballot_sync(0xffffffffu, res), bm = __ballot_sync(0xffffffffu, mis);
       if (res) tk.ord[cr + __popc(br & lt)] = t;
       if (mis) tk.ord[cm + __popc(bm & lt)] = t;
@@ -619,7 +760,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
 
   // ---- phase A assignment: whole rows of the flattened (task order, i) list,
   // dealt round-robin over the grid's warps: warp gw takes rows gw, gw + Gw, ...
-  const int Gw = gridDim.x * kW, gw = blockIdx.x * kW + warp;
+  const int Gw = GF * kW, gw = cta * kW + warp;
   const int NA = T * I;
   const int nitA = (gw < NA ? (NA - 1 - gw) / Gw + 1 : 0) * KC;
   auto task_of = [&](int it) {  // the task of this warp's item `it`
@@ -686,18 +827,18 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const int ppe = LAYER ? max(1, (int)((st.slot_bytes + kPiece - 1) / kPiece)) : 1;
   // the gate/up global scales of the item in flight on each slot (lane 0)
   float2 gsl0 = make_float2(1.f, 1.f), gsl1 = make_float2(1.f, 1.f);
-  auto issue_a = [&](int it) {  // lane 0
-    const int t = task_of(it), sl = it & 1;
+  auto issue_a = [&](int it, const uint8_t* blob) {  // lane 0
+    const int sl = it & 1;
     mbar_expect_tx(&bar_a[warp][sl], ItemA<FMT>::BYTES);
-    ItemA<FMT>::issue(slots + sl * kSlotBytes, tk.blob[t], o, H, row_of(it), it % KC,
-                      &bar_a[warp][sl], pol);
-    const float2 g = ItemA<FMT>::glob(tk.blob[t], o);
+    ItemA<FMT>::issue(slots + sl * kSlotBytes, blob, o, H, row_of(it), it % KC, &bar_a[warp][sl],
+                      pol);
+    const float2 g = ItemA<FMT>::glob(blob, o);
     gsl0 = sl ? gsl0 : g;
     gsl1 = sl ? g : gsl1;
   };
   // an item of an expert this launch copies in is requested only once the copy
   // is complete (see wait_copied below); every other item as soon as its slot is free
-  auto deferred = [&](int it) { return LAYER && tk.pe[task_of(it)] >= 0; };
+  auto deferred = [&](int it) { return LAYER && tk.pe[task_of(it)] != -1; };
   if (warp == kW - 1) {  // phase-B staging: one lane per (batch row, task) block
     const int nblk = (ru1 > ru0) ? (ts[bA + 1] - ts[bA]) + (bB != bA ? ts[bB + 1] - ts[bB] : 0) : 0;
     uint32_t mine = 0;
@@ -707,7 +848,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       const int t = ts[b] + (bi ? j - (ts[bA + 1] - ts[bA]) : j);
       const int nlen = nlen_of(b), q0 = (bi ? cntA : 0) + (t - ts[b]) * nlen;
       const int cnt = min(nlen, qs - q0);
-      if (cnt > 0 && !(LAYER && tk.pe[t] >= 0)) mine += (uint32_t)cnt * (CB + SB);
+      if (cnt > 0 && !(LAYER && tk.pe[t] != -1)) mine += (uint32_t)cnt * (CB + SB);
     }
     uint32_t total = mine;
 #pragma unroll
@@ -720,7 +861,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       const int t = ts[b] + (bi ? j - (ts[bA + 1] - ts[bA]) : j);
       const int nlo = nlo_of(b), nlen = nlen_of(b), q0 = (bi ? cntA : 0) + (t - ts[b]) * nlen;
       const int cnt = min(nlen, qs - q0);
-      if (cnt <= 0 || (LAYER && tk.pe[t] >= 0)) continue;  // copied in by this launch: read later
+      if (cnt <= 0 || (LAYER && tk.pe[t] != -1)) continue;  // copied in by this launch: read later
       const uint8_t* blob = tk.blob[t];
       bulk_g2s(stC + (size_t)q0 * CB,
                blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB,
@@ -733,8 +874,8 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   // this warp's first two phase-A items are requested before any copy work,
   // so that they land while it copies
   if (lane == 0) {
-    if (nitA > 0 && !deferred(0)) issue_a(0);
-    if (nitA > 1 && !deferred(1)) issue_a(1);
+    if (nitA > 0 && !deferred(0)) issue_a(0, tk.blob[task_of(0)]);
+    if (nitA > 1 && !deferred(1)) issue_a(1, tk.blob[task_of(1)]);
   }
   // fused layer: the step's missed experts (and the next layer's prefetches)
   // are copied from pinned host memory in 4 KiB pieces, one per warp at a
@@ -742,34 +883,100 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   // reads).  Each finished piece of a demand entry is counted, and the rows of
   // that expert wait for the full count.  A warp does its pieces before it can
   // wait on any, and a step without misses has no pieces.
-  if (LAYER && n_pl0 + n_pl1 > 0) {
-    const long total = (long)(n_pl0 + n_pl1) * ppe;
-    for (long p = warp * gridDim.x + blockIdx.x; p < total; p += Gw) {
-      const int ei = (int)(p / ppe), j = (int)(p - (long)ei * ppe);
-      const bool demand = ei < n_pl0;
-      const int32_t* plan = demand ? a.gplan0 : a.gplan1;
-      const int i = demand ? ei : ei - n_pl0;
-      const int s = plan[1 + 3 * i], L = plan[2 + 3 * i], e = plan[3 + 3 * i];
-      if ((unsigned)s < (unsigned)st.S && (unsigned)L < (unsigned)st.L && (unsigned)e < (unsigned)st.E) {
-        const size_t off = (size_t)j * kPiece;
-        const int len = (int)min((size_t)kPiece, st.slot_bytes - off);
-        const uint4* src = reinterpret_cast<const uint4*>(st.host_blob[L * st.E + e] + off);
-        uint4* dst = reinterpret_cast<uint4*>(
-            st.slots + ((size_t)pool_of(st, L) * st.S + s) * st.stride + off);
-        const int nv = len / 16;
-        uint4 v[kPiece / 512];
-#pragma unroll
-        for (int u = 0; u < kPiece / 512; ++u)
-          if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
-#pragma unroll
-        for (int u = 0; u < kPiece / 512; ++u)
-          if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
+  // admission inside: wait (bounded, the whole warp on lane 0's reads) until
+  // CTA 0 has published pseq >= target; then every lane acquires too
+  auto wait_seq = [&](unsigned long long target) -> bool {
+    const unsigned long long t0 = now_ns();
+    for (;;) {
+      int s = 0;  // 1: published, 2: timed out
+      if (lane == 0) {
+        const unsigned long long v = ld_acquire_u64(a.pseq);
+        s = v >= target ? 1 : (now_ns() - t0 > kWaitNs ? 2 : 0);
       }
-      __syncwarp();
-      if (demand && lane == 0) {
-        __threadfence();
-        atomicAdd(a.gdone + i, 1);
+      s = __shfl_sync(0xffffffffu, s, 0);
+      if (s == 1) {
+        (void)ld_acquire_u64(a.pseq);
+        return true;
       }
+      if (s == 2) {
+        if (lane == 0) flag_timeout(a.status);
+        return false;
+      }
+      __nanosleep(256);
+    }
+  };
+  auto copy_piece = [&](long p, int np0) {  // piece p of the demand plan, then the prefetch plan
+    const int ei = (int)(p / ppe), j = (int)(p - (long)ei * ppe);
+    const bool demand = ei < np0;
+    const int32_t* plan = demand ? a.gplan0 : a.gplan1;
+    const int i = demand ? ei : ei - np0;
+    const int s = plan[1 + 3 * i], L = plan[2 + 3 * i], e = plan[3 + 3 * i];
+    if ((unsigned)s < (unsigned)st.S && (unsigned)L < (unsigned)st.L && (unsigned)e < (unsigned)st.E) {
+      const size_t off = (size_t)j * kPiece;
+      const int len = (int)min((size_t)kPiece, st.slot_bytes - off);
+      const uint4* src = reinterpret_cast<const uint4*>(st.host_blob[L * st.E + e] + off);
+      uint4* dst = reinterpret_cast<uint4*>(
+          st.slots + ((size_t)pool_of(st, L) * st.S + s) * st.stride + off);
+      const int nv = len / 16;
+      uint4 v[kPiece / 512];
+#pragma unroll
+      for (int u = 0; u < kPiece / 512; ++u)
+        if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
+#pragma unroll
+      for (int u = 0; u < kPiece / 512; ++u)
+        if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
+    }
+    __syncwarp();
+    if (demand && lane == 0) {
+      __threadfence();
+      atomicAdd(a.gdone + i, 1);
+    }
+  };
+  // a staging piece: piece p of the step's missed experts, from pinned host
+  // memory into their staging entries (counted like the demand plan's pieces)
+  auto stage_piece = [&](long p) {
+    const int i = (int)(p / ppe), j = (int)(p - (long)i * ppe);
+    const int e = s_pexp[i];
+    const size_t off = (size_t)j * kPiece;
+    const int len = (int)min((size_t)kPiece, st.slot_bytes - off);
+    const uint4* src = reinterpret_cast<const uint4*>(st.host_blob[a.layer * st.E + e] + off);
+    uint4* dst = reinterpret_cast<uint4*>(a.stage + (size_t)i * st.stride + off);
+    const int nv = len / 16;
+    uint4 v[kPiece / 512];
+#pragma unroll
+    for (int u = 0; u < kPiece / 512; ++u)
+      if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
+#pragma unroll
+    for (int u = 0; u < kPiece / 512; ++u)
+      if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(a.gdone + i, 1);
+    }
+  };
+  const bool pf_plan = a.gplan1 && (!ADMIT || (a.pred && a.n_pred > 0));  // a prefetch plan to copy
+  {
+    const long p0 = (long)warp * GF + cta;  // this warp's first piece
+    if (staged) {  // the misses start crossing the host link now, whatever the admission does
+      for (long p = p0; p < (long)npx * ppe; p += Gw) stage_piece(p);
+    } else if (ADMIT) {
+      // a warp can only get pieces below (misses + predictions) * ppe; the
+      // others need not wait for the plans here
+      const long bound = (long)(npend + (pf_plan ? a.n_pred : 0)) * ppe;
+      if (p0 < bound && wait_seq(seq0 + 1)) {
+        const int np0 = a.gplan0[0];
+        for (long p = p0; p < (long)np0 * ppe; p += Gw) copy_piece(p, np0);
+        if (pf_plan && wait_seq(seq0 + 2)) {
+          const long end = (long)(np0 + a.gplan1[0]) * ppe;
+          long p = p0;
+          while (p < (long)np0 * ppe) p += Gw;
+          for (; p < end; p += Gw) copy_piece(p, np0);
+        }
+      }
+    } else if (LAYER && n_pl0 + n_pl1 > 0) {
+      const long total = (long)(n_pl0 + n_pl1) * ppe;
+      for (long p = p0; p < total; p += Gw) copy_piece(p, n_pl0);
     }
   }
 
@@ -777,7 +984,8 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   float cw = 1.f, c2 = 1.f;
   if (threadIdx.x < T) {
     if (MODE != kShared && tk.route[threadIdx.x] < a.R) cw = a.w[tk.route[threadIdx.x]];
-    if (FMT == MOE_W_NVFP4) c2 = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob)[2];
+    if (FMT == MOE_W_NVFP4 && tk.blob[threadIdx.x])  // not yet resident: set after the barrier
+      c2 = reinterpret_cast<const float*>(tk.blob[threadIdx.x] + o.glob)[2];
   }
 
   // the shared expert's sigmoid gate, sigmoid(x_b . w_g), in fp32, by the last
@@ -816,9 +1024,9 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     };
     float ga = 0.f, ua = 0.f, gb = 0.f, ub = 0.f;
     // fused layer: wait (bounded, the whole warp on lane 0's reads) until this
-    // launch has copied all of task t's expert into its slot
-    auto wait_copied = [&](int t) -> bool {
-      const int* ctr = a.gdone + tk.pe[t];
+    // launch has copied all of demand-plan entry pe into its slot
+    auto wait_copied = [&](int pe) -> bool {
+      const int* ctr = a.gdone + pe;
       const unsigned long long t0 = now_ns();
       for (;;) {
         int s = 0;  // 1: complete, 2: timed out
@@ -840,14 +1048,41 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     auto wait_a = [&](int it) -> bool {
       const int sl = it & 1;
       if (inflight[sl] != it) {  // deferred: its expert is being copied in by this launch
-        if (!wait_copied(task_of(it))) {
+        const int t = task_of(it);
+        const uint8_t* blob = tk.blob[t];
+        int pe = tk.pe[t];
+        if (ADMIT && !staged) {  // decided by CTA 0's admission
+          if (!wait_seq(seq0 + 1)) {
+            failed = true;
+            return false;
+          }
+          const int s = a.slot_out[tk.route[t]];
+          blob = s >= 0 ? slot_blob(s) : nullptr;
+          pe = -1;
+          if (s >= 0) {  // its entry in the demand plan
+            const int np = a.gplan0[0];
+            for (int i0 = 0; i0 < np; i0 += 32) {
+              const unsigned hit =
+                  __ballot_sync(0xffffffffu, i0 + lane < np && a.gplan0[1 + 3 * (i0 + lane)] == s);
+              if (hit) {
+                pe = i0 + __ffs(hit) - 1;
+                break;
+              }
+            }
+          }
+        }
+        if (pe >= 0 && !wait_copied(pe)) {
           failed = true;
           return false;
         }
         if (lane == 0) {
-          fence_proxy_async();  // the slot's previous reads before the new bulk writes
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // copied bytes -> bulk reads
-          issue_a(it);
+          if (blob) {
+            fence_proxy_async();  // the slot's previous reads before the new bulk writes
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // copied bytes -> bulk reads
+            issue_a(it, blob);
+          } else {  // not admitted (fetch cap): nothing to copy; its h is never read
+            mbar_arrive(&bar_a[warp][sl]);
+          }
         }
         inflight[sl] = it;
       }
@@ -870,7 +1105,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       if (it + 2 < nitA && !deferred(it + 2)) {
         if (lane == 0) {
           fence_proxy_async();
-          issue_a(it + 2);
+          issue_a(it + 2, tk.blob[task_of(it + 2)]);
         }
         inflight[0] = it + 2;
       }
@@ -885,7 +1120,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
         if (it + 3 < nitA && !deferred(it + 3)) {
           if (lane == 0) {
             fence_proxy_async();
-            issue_a(it + 3);
+            issue_a(it + 3, tk.blob[task_of(it + 3)]);
           }
           inflight[1] = it + 3;
         }
@@ -914,12 +1149,35 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   if (threadIdx.x < T) tk.wt[threadIdx.x] = cw * c2;  // read after the barrier
 
   // ---------------------------------------------------------------- barrier
-  const bool ok = grid_barrier(a.bar_ctr, a.status);
-  const bool staged = mbar_wait(&bar_b, 0);  // the staged phase-B rows (bounded)
-  if (!staged) flag_timeout(a.status);
-  if (!ok || !__syncthreads_and(staged)) return;  // timed out: nothing below is trustworthy
-  if (LAYER && blockIdx.x == 0)  // every wait on the copies is behind the barrier
-    for (int i = threadIdx.x; i < n_pl0; i += kT) a.gdone[i] = 0;
+  const bool ok = grid_barrier(ADMIT ? a.bar2 : a.bar_ctr, a.status, (unsigned)GF);
+  const bool rows_in = mbar_wait(&bar_b, 0);  // the staged phase-B rows (bounded)
+  if (!rows_in) flag_timeout(a.status);
+  if (!ok || !__syncthreads_and(rows_in)) return;  // timed out: nothing below is trustworthy
+  int n_done = staged ? npx : n_pl0;  // piece counters this launch used
+  if (ADMIT && npend > 0) {  // the tasks not resident at entry, as CTA 0 admitted them
+    if (warp == 0) (void)wait_seq(seq0 + 1);  // bounded
+    __syncthreads();
+    (void)ld_acquire_u64(a.pseq);
+    if (!staged) n_done = a.gplan0[0];
+    const int t = threadIdx.x;
+    if (t < T && tk.pend[t]) {
+      const int s = a.slot_out[tk.route[t]];
+      if (s < 0) {
+        tk.drop[t] = 1;  // not admitted (fetch cap, no slot): no output term, as in the
+                         // two-launch path
+      } else if (!staged) {
+        int pe = -1;
+        for (int i = 0; i < n_done && pe < 0; ++i)
+          if (a.gplan0[1 + 3 * i] == s) pe = i;
+        tk.blob[t] = slot_blob(s);
+        tk.slot[t] = s;
+        tk.pe[t] = pe;
+      }
+    }
+    __syncthreads();
+  }
+  if (LAYER && cta == 0)  // every wait on the copies is behind the barrier
+    for (int i = threadIdx.x; i < n_done; i += kT) a.gdone[i] = 0;
   // an expert copied in by this launch: its down global scale is in the slot
   // only now (read by the combine, after the next block barrier)
   if (LAYER && FMT == MOE_W_NVFP4 && threadIdx.x < T && tk.pe[threadIdx.x] >= 0)
@@ -982,8 +1240,9 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
           ht = t;
         }
         ItemB<FMT> itm[NG];
-        const bool copied = LAYER && tk.pe[t] >= 0;  // copied in by this launch: not staged
-        if (!copied && q + cnt <= qs) {
+        const bool copied = LAYER && tk.pe[t] != -1;  // copied in by this launch: not staged
+        if (ADMIT && tk.drop[t]) {  // not admitted: no rows, no output term (warp-uniform)
+        } else if (!copied && q + cnt <= qs) {
 #pragma unroll
           for (int j = 0; j < NG; ++j)
             if (j < cnt)
@@ -1003,12 +1262,14 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
                               blob + o.scale[2] + (size_t)n * SB, M, lane);
           }
         }
-        float p[4] = {0.f, 0.f, 0.f, 0.f};
+        if (!(ADMIT && tk.drop[t])) {
+          float p[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < NG; ++j) p[j] = j < cnt ? itemb_dot<FMT>(itm[j], hv, M) : 0.f;
-        const float v = reduce4(p, lane);
-        const int j = lane >> 3;
-        if ((lane & 7) == 0 && j < cnt) ysm[(size_t)t * perB + (b * H + nlo + r + j - ru0)] = v;
+          for (int j = 0; j < NG; ++j) p[j] = j < cnt ? itemb_dot<FMT>(itm[j], hv, M) : 0.f;
+          const float v = reduce4(p, lane);
+          const int j = lane >> 3;
+          if ((lane & 7) == 0 && j < cnt) ysm[(size_t)t * perB + (b * H + nlo + r + j - ru0)] = v;
+        }
         q += cnt;
         r += cnt;
         if (r == nlen) {  // the task's rows are done: the next task, maybe of the next batch row
@@ -1036,7 +1297,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     const int te = ts[b + 1] - (has_s ? 1 : 0);
     float acc = 0.f;
     for (int t = ts[b]; t < te; ++t)
-      acc = fmaf(tk.wt[t], ysm[(size_t)t * perB + (ru - ru0)], acc);
+      if (!(ADMIT && tk.drop[t])) acc = fmaf(tk.wt[t], ysm[(size_t)t * perB + (ru - ru0)], acc);
     if (LAYER) {  // routed sum (j ascending), then + gate * shared, as in the two-launch path
       float yv = 0.f;
       if (has_s)
@@ -1047,6 +1308,49 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     } else {
       const float yv = mm < kYsPre ? ysv[mm] : (a.ys ? a.ys[ru] : 0.f);
       a.out[ru] = __float2bfloat16_rn(a.ys ? acc + yv : acc);
+    }
+  }
+  if (ADMIT) {
+    // the admitted misses into their slots, and their map entries valid for
+    // later launches (every computing CTA read the map before the barrier)
+    if (npend > 0) {
+      const int np0 = a.gplan0[0];
+      if (staged) {
+        for (long p = (long)warp * GF + cta; p < (long)np0 * ppe; p += Gw) {
+          const int i = (int)(p / ppe), j = (int)(p - (long)i * ppe);
+          const int s = a.gplan0[1 + 3 * i], L = a.gplan0[2 + 3 * i], e = a.gplan0[3 + 3 * i];
+          if ((unsigned)s >= (unsigned)st.S || L != a.layer || (unsigned)e >= (unsigned)st.E) continue;
+          int x = -1;  // its staging entry
+          for (int q = 0; q < npx; ++q)
+            if (s_pexp[q] == e) x = q;
+          if (x >= 0) {
+            const size_t off = (size_t)j * kPiece;
+            const int nv = (int)(min((size_t)kPiece, st.slot_bytes - off) / 16);
+            const uint4* src = reinterpret_cast<const uint4*>(a.stage + (size_t)x * st.stride + off);
+            uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(slot_blob(s)) + off);
+            uint4 v[kPiece / 512];
+#pragma unroll
+            for (int u = 0; u < kPiece / 512; ++u)
+              if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
+#pragma unroll
+            for (int u = 0; u < kPiece / 512; ++u)
+              if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
+          }
+          if (j == 0 && lane == 0) st.map[a.layer * st.E + e] = s;
+        }
+      } else if (cta == 0) {
+        for (int i = threadIdx.x; i < np0; i += kT) {
+          const int s = a.gplan0[1 + 3 * i], e = a.gplan0[3 + 3 * i];
+          if ((unsigned)s < (unsigned)st.S && (unsigned)e < (unsigned)st.E)
+            st.map[a.layer * st.E + e] = s;
+        }
+      }
+    }
+    // staged steps copy the next layer's prefetches last
+    if (staged && pf_plan && wait_seq(seq0 + 2)) {
+      const int np0 = a.gplan0[0], np1 = a.gplan1[0];
+      for (long p = (long)warp * GF + cta; p < (long)np1 * ppe; p += Gw)
+        copy_piece((long)np0 * ppe + p, np0);
     }
   }
 }
@@ -1065,9 +1369,8 @@ struct Plan {
 // Shared memory: x [n_rows][H] | ysm [T][perB] fp32 | h [htasks][I] fp32 |
 // two phase-A slots per warp | staged phase-B rows.  A CTA's output rows span at most two batch rows, so
 // it needs the h of at most 2k tasks.
-Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T) {
+Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T, int G) {
   Plan p{};
-  const int G = g_num_sms > 0 ? g_num_sms : 1;
   const int perB = (n_rows * H + G - 1) / G;
   const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
   p.htasks = std::min(T, 2 * k);
@@ -1083,6 +1386,18 @@ Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T) {
          I <= 1024 && perB <= H &&
          n_rows * H <= kXW * 8 * kT;
   return p;
+}
+
+int grid_of(int mode) {  // computing CTAs (CTA 0 admits in kLayerAdmit)
+  const int G = g_num_sms > 0 ? g_num_sms : 1;
+  return mode == kLayerAdmit ? std::max(1, G - 1) : G;
+}
+
+// Shared memory of CTA 0 in kLayerAdmit: its block state, then the admission's
+// [E] x 3 counters (and the pool's keys when cached), or the prefetch's [E] x 2.
+size_t admit_cta_smem(int E, int S, bool cached) {
+  const size_t adm = 3ull * E * sizeof(int) + (cached ? (size_t)S * 12 : 0);
+  return round128(sizeof(admission::AdmitShared<kT>)) + std::max<size_t>(adm, 2ull * E * sizeof(int));
 }
 
 template <typename K>
@@ -1102,16 +1417,26 @@ cudaError_t launch_coop(K kernel, size_t smem, cudaStream_t s, const DevState& s
 }
 
 // tasks per batch row and in all, for a launch of `mode`
-int tasks_per_row(int mode, int k, bool shared) { return mode == kLayer ? k + (shared ? 1 : 0) : k; }
+int tasks_per_row(int mode, int k, bool shared) {
+  return (mode == kLayer || mode == kLayerAdmit) ? k + (shared ? 1 : 0) : k;
+}
 
 cudaError_t launch_fused(const DevState& st, int wfmt, int mode, const FusedArgs& a0,
                          cudaStream_t s) {
   FusedArgs a = a0;
   const bool sh = a.shared_blob != nullptr;
+  const bool layer = mode == kLayer || mode == kLayerAdmit;
   const int kt = tasks_per_row(mode, a.k, sh);
-  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, kt, a.R + (mode == kLayer && sh ? a.n_rows : 0));
+  const Plan p = fused_plan(wfmt, a.H, a.I, a.n_rows, kt, a.R + (layer && sh ? a.n_rows : 0),
+                            grid_of(mode));
   a.qs = p.qs;
   a.htasks = p.htasks;
+  size_t smem = p.smem;
+  if (mode == kLayerAdmit) smem = std::max(smem, admit_cta_smem(st.E, st.S, a.adm_cached != 0));
+  if (smem > kBudget) return cudaErrorInvalidValue;
+  if (mode == kLayerAdmit)
+    return wfmt == MOE_W_NVFP4 ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kLayerAdmit>, smem, s, st, a)
+                               : launch_coop(ffn_fused_kernel<MOE_W_BF16, kLayerAdmit>, smem, s, st, a);
   if (wfmt == MOE_W_NVFP4) {
     if (mode == kLayer) return launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kLayer>, p.smem, s, st, a);
     return mode == kShared ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kShared>, p.smem, s, st, a)
@@ -1127,7 +1452,7 @@ cudaError_t launch_fused(const DevState& st, int wfmt, int mode, const FusedArgs
 bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks) {
   if (g_num_sms <= 0 || n_tasks > kMaxRoutes || n_rows > kMaxRows || n_rows < 1) return false;
   const int k = (n_tasks + n_rows - 1) / n_rows;
-  return fused_plan(wfmt, H, I, n_rows, k, n_tasks).ok;
+  return fused_plan(wfmt, H, I, n_rows, k, n_tasks, grid_of(kRouted)).ok;
 }
 
 cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int max_tasks) {
@@ -1144,6 +1469,8 @@ cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int ma
   set(ffn_fused_kernel<MOE_W_NVFP4, kRouted>);
   set(ffn_fused_kernel<MOE_W_BF16, kLayer>);
   set(ffn_fused_kernel<MOE_W_NVFP4, kLayer>);
+  set(ffn_fused_kernel<MOE_W_BF16, kLayerAdmit>);
+  set(ffn_fused_kernel<MOE_W_NVFP4, kLayerAdmit>);
   (void)wfmt, (void)H, (void)I, (void)Is, (void)max_rows, (void)max_tasks;
   return e;
 }
@@ -1201,7 +1528,61 @@ bool layer_stream_supported(int wfmt, int H, int I, int n_rows, int k, bool shar
   if (g_num_sms <= 0 || n_rows < 1 || n_rows > kMaxRows || n_rows * k > kMaxRoutes) return false;
   const int kt = tasks_per_row(kLayer, k, shared);
   const int T = n_rows * kt;
-  return T <= kMaxTasks && fused_plan(wfmt, H, I, n_rows, kt, T).ok;
+  return T <= kMaxTasks && fused_plan(wfmt, H, I, n_rows, kt, T, grid_of(kLayer)).ok;
+}
+
+bool layer_admit_supported(const DevState& st, int wfmt, int H, int I, int n_rows, int k,
+                           bool shared) {
+  if (g_num_sms < 2 || st.E > kPbWords * 32 || !layer_stream_supported(wfmt, H, I, n_rows, k, shared))
+    return false;
+  const int kt = tasks_per_row(kLayerAdmit, k, shared);
+  const Plan p = fused_plan(wfmt, H, I, n_rows, kt, n_rows * kt, grid_of(kLayerAdmit));
+  return p.ok && std::max(p.smem, admit_cta_smem(st.E, st.S, false)) <= kBudget;
+}
+
+cudaError_t launch_layer_admit(const DevState& st, int wfmt, int H, int I, int layer,
+                               const void* x, const int32_t* ids, int32_t* slot_out,
+                               const float* w, int n_rows, int k, int cap, const int32_t* pred,
+                               int n_pred, const uint8_t* shared_blob, const void* gate_w,
+                               int32_t* plan1, void* out, FfnScratch sc,
+                               unsigned long long* status, cudaStream_t s) {
+  FusedArgs a{};
+  a.H = H;
+  a.I = I;
+  a.layer = layer;
+  a.k = k;
+  a.R = n_rows * k;
+  a.n_rows = n_rows;
+  a.x = static_cast<const uint16_t*>(x);
+  a.slot_ids = slot_out;
+  a.fixed_blob = nullptr;
+  a.w = w;
+  a.h = sc.h;
+  a.gate_w = static_cast<const uint16_t*>(gate_w);
+  a.gate = sc.gate;
+  a.ys = nullptr;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.status = status;
+  a.bar_ctr = sc.bar;
+  a.shared_blob = shared_blob;
+  a.gplan0 = st.plan_demand;
+  a.gplan1 = plan1;
+  a.gdone = sc.gdone;
+  a.ids = ids;
+  a.slot_out = slot_out;
+  a.cap = cap;
+  a.pred = pred;
+  a.n_pred = pred ? n_pred : 0;
+  a.epoch = sc.epoch;
+  a.stage = sc.stage_n > 0 ? sc.stage : nullptr;
+  a.stage_n = sc.stage_n;
+  a.pseq = sc.pseq;
+  a.bar2 = sc.bar2;
+  const int kt = tasks_per_row(kLayerAdmit, k, shared_blob != nullptr);
+  const Plan p = fused_plan(wfmt, H, I, n_rows, kt, n_rows * kt, grid_of(kLayerAdmit));
+  a.adm_cached = admit_cached(st.E, st.S) &&
+                 std::max(p.smem, admit_cta_smem(st.E, st.S, true)) <= kBudget;
+  return launch_fused(st, wfmt, kLayerAdmit, a, s);
 }
 
 cudaError_t launch_layer_stream(const DevState& st, int wfmt, int H, int I, int layer,

@@ -32,6 +32,7 @@ struct moe_cache {
   DevState st{};
   FfnScratch sc{};
   void* mem = nullptr;       // one allocation for all state and scratch
+  void* stage_mem = nullptr; // staging entries of a layer launch with the admission inside
   size_t mem_bytes = 0;
   cudaEvent_t ev_ready = nullptr, ev_done = nullptr;
   int fail_gathers = 0;
@@ -170,7 +171,9 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_xinv = cv.take<float>(d.max_rows),
                o_y = cv.take<float>((size_t)d.max_routes * std::max(H, 1)),
                o_status = cv.take<unsigned long long>(1),
-               o_bar = cv.take<unsigned long long>(1);
+               o_bar = cv.take<unsigned long long>(1),
+               o_ep = cv.take<unsigned long long>(1), o_pseq = cv.take<unsigned long long>(1),
+               o_bar2 = cv.take<unsigned long long>(1);
   c->mem_bytes = align_up(cv.off, 256);
   e = cudaMalloc(&c->mem, c->mem_bytes);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMalloc(state)"));
@@ -210,6 +213,9 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.gate = reinterpret_cast<float*>(m + o_gate);
   c->sc.ys = reinterpret_cast<float*>(m + o_ys);
   c->sc.bar = reinterpret_cast<unsigned long long*>(m + o_bar);
+  c->sc.epoch = reinterpret_cast<unsigned long long*>(m + o_ep);
+  c->sc.pseq = reinterpret_cast<unsigned long long*>(m + o_pseq);
+  c->sc.bar2 = reinterpret_cast<unsigned long long*>(m + o_bar2);
   c->sc.x16 = reinterpret_cast<uint16_t*>(m + o_x16);
   c->sc.xinv = reinterpret_cast<float*>(m + o_xinv);
   c->sc.y = reinterpret_cast<float*>(m + o_y);
@@ -255,6 +261,19 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     if (e == cudaSuccess && moe::grouped_supported(d.wfmt, H, I, d.n_experts))
       e = moe::grouped_init(d.n_experts, H, I);
     if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
+    // a layer launch with the admission inside copies an uncapped step's misses
+    // into staging entries while the admission runs: up to max_routes of them,
+    // within 64 MB
+    if (d.slot_bytes > 0) {
+      const size_t cap = (64ull << 20) / c->d.slot_stride;
+      const int n = (int)std::min<size_t>((size_t)d.max_routes, cap);
+      if (n > 0) {
+        e = cudaMalloc(&c->stage_mem, (size_t)n * c->d.slot_stride);
+        if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMalloc(staging)"));
+        c->sc.stage = static_cast<uint8_t*>(c->stage_mem);
+        c->sc.stage_n = n;
+      }
+    }
   }
   e = cudaEventCreateWithFlags(&c->ev_ready, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming);
@@ -273,6 +292,7 @@ int moe_cache_destroy(moe_cache* c) {
   if (c->ev_ready) cudaEventDestroy(c->ev_ready);
   if (c->ev_done) cudaEventDestroy(c->ev_done);
   if (c->mem) cudaFree(c->mem);
+  if (c->stage_mem) cudaFree(c->stage_mem);
   delete c;
   return rc;
 }
@@ -468,6 +488,18 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
                      (!d_shared_blob || dd.shared_inter == dd.inter) &&
                      moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k,
                                                  d_shared_blob != nullptr);
+  if (fused && moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k,
+                                         d_shared_blob != nullptr)) {
+    // one launch for the whole layer: admission (and prefetch admission) in
+    // CTA 0, gathers + shared expert + routed experts in the others
+    int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
+    CK(moe::launch_layer_admit(c->st, dd.wfmt, dd.hidden, dd.inter, layer, d_x, d_ids, d_slot_ids,
+                               d_w, n_rows, k, fetch_cap, pf ? d_pred : nullptr, n_pred,
+                               static_cast<const uint8_t*>(d_shared_blob), d_shared_gate,
+                               pf ? pf_plan : nullptr, d_out, c->sc, c->st.status, cs));
+    if (pf) c->last_pf_layer = layer + 1;
+    return MOE_OK;
+  }
   if (fused) {  // admission, then one launch: gathers + shared expert + routed experts
     CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
     int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
