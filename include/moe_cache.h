@@ -128,7 +128,7 @@ typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 
 /* moe_decode_layer flags */
 #define MOE_OVERLAP 1u        /* gather on the side stream, joined by events [P2] */
-#define MOE_FUSED 2u          /* after the admission, one launch does the gathers, the shared
+#define MOE_FUSED 2u          /* one launch per layer: the admission, the gathers, the shared
                                  expert and the routed experts (decode-sized steps) */
 
 /* status_bits of moe_stats */
@@ -281,15 +281,28 @@ MOE_API int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const i
  * not be mixed with moe_gather_missing(MOE_PLAN_PREFETCH) calls of its own.
  *
  * With flags & MOE_FUSED, for decode-sized steps (at most 16 rows and 64
- * routes, the streaming kernel's shapes, and a shared expert of the routed
- * experts' size), the layer is the admission (and prefetch admission) on
- * compute_stream followed by one cooperative launch that copies the demand and
- * prefetch plans' experts from host memory, computes the shared expert and
- * the routed experts -- the rows of a missed expert wait, inside the launch,
- * until its bytes have arrived -- and writes d_out.  The overlap of [P2] (the
- * gather beside the shared expert) happens inside that launch instead of on
- * two streams; side_stream is not used.  Other shapes fall back to the mode
- * the remaining flags select.  Results equal the two-launch path's bit for bit. */
+ * routes, the streaming kernel's shapes, a shared expert of the routed
+ * experts' size, at most 4096 experts per layer), the layer is ONE
+ * cooperative launch on compute_stream:
+ *   - CTA 0 runs the admission (the same algorithm and results as moe_admit,
+ *     writing d_slot_ids, the plan and the stats) and then the prefetch
+ *     admission of layer+1;
+ *   - the other CTAs read the map for the step's experts themselves (a hit
+ *     cannot be evicted by its own admission; an installed miss is marked
+ *     pending in the map until this launch has copied it in), stream the
+ *     resident experts at once and compute the shared and routed experts;
+ *   - an uncapped step's misses are copied from pinned host memory into
+ *     staging entries (up to max_routes experts within 64 MB, allocated at
+ *     create) as soon as they are known, computed from there, and copied into
+ *     their slots at the end of the launch; with a fetch cap they wait for the
+ *     admission's slots and are copied there directly; the prefetch plan's
+ *     experts are copied into their slots in the same launch.
+ * The overlap of [P2] (the gather beside the shared expert) happens inside
+ * that launch instead of on two streams; side_stream is not used.  If the
+ * shapes do not fit, the admission and prefetch run as their own launches
+ * followed by one launch for the rest; other shapes fall back to the mode the
+ * remaining flags select.  Outputs, slot ids, plans, stats and cache state equal
+ * the four-launch path's bit for bit. */
 MOE_API int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,
                      const float* d_w, int32_t* d_slot_ids, int n_rows, int k, int fetch_cap,
                      const int32_t* d_pred, int n_pred, const void* d_shared_blob,
