@@ -108,10 +108,11 @@ def test_overlap_bytes_equal_serial():
 
 
 def test_fused_layer_equals_two_launch_path():
-    """MOE_FUSED runs the gather, the shared expert and the routed experts in
-    one launch after the admission; the overlap of [FreeToken issue #753, What
-    we changed] moves inside it.  Slot ids, state and statistics stay exact
-    against the oracle, and the output bytes equal the two-launch path's."""
+    """MOE_FUSED runs the whole layer in one launch (admission, gather, shared
+    expert, routed experts); the overlap of [FreeToken issue #753, What we
+    changed] moves inside it.  Slot ids, state and statistics stay exact
+    against the oracle, the output bytes equal the two-launch path's, and every
+    resident slot holds its expert's bytes (the misses went through staging)."""
     w = synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=6, steps=12, n_slots=80)
     blobs = synth.HostBlobs(w, pinned=True)
     a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
@@ -128,6 +129,36 @@ def test_fused_layer_equals_two_launch_path():
                 assert_close(sa.out[layer], ref, w.fmt, f"step {t} layer {layer}")
     assert sum(a.sc.stats(l)["fetched"] for l in range(w.n_layers)) > 50
     assert a.sc.stats(0)["status_bits"] == 0
+    state = a.oc.state()
+    for s, key in enumerate(state["slot_key"]):
+        if key >= 0:
+            assert np.array_equal(a.slot_bytes(0, s), a.blobs.blob(int(key))), s
+
+
+def test_fused_layer_uncapped_staging_and_fallback_bf16():
+    """Uncapped hybrid shapes with prefetch: 25 MB blobs leave room for two
+    staging entries (64 MB), so a step with at most two misses copies them
+    through staging and one with more waits for the admission's slots.  Both
+    give the two-launch path's output bytes, exact state, and slots holding
+    their experts."""
+    w = synth.scaled(synth.workloads()["hybrid_prefetch"], n_layers=6, steps=6, fetch_cap=-1)
+    blobs = synth.HostBlobs(w, pinned=True)
+    a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    sa, sb = Stepper(a, True, n_pred=w.n_pred, fused=True), Stepper(b, True, n_pred=w.n_pred)
+    ids, wts = synth.make_routing(w)
+    misses = []
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        before = [a.sc.stats(l)["misses"] for l in range(w.n_layers)]
+        sa.step(t, ids[t], wts[t], x)
+        sb.step(t, ids[t], wts[t], x)
+        misses += [a.sc.stats(l)["misses"] - before[l] for l in range(w.n_layers)]
+        assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16)), f"step {t}"
+    assert any(0 < m <= 2 for m in misses) and any(m > 2 for m in misses), misses
+    state = a.oc.state()
+    for s, key in enumerate(state["slot_key"]):
+        if key >= 0:
+            assert np.array_equal(a.slot_bytes(0, s), a.blobs.blob(int(key))), s
 
 
 def test_fused_layer_capped_prefetch_bf16():
