@@ -163,6 +163,7 @@ struct FfnScratch {
   unsigned long long* epoch;   // launches (each CTA adds one)
   unsigned long long* pseq;    // the admission's publication sequence
   unsigned long long* bar2;    // grid barrier of the computing CTAs
+  unsigned long long* sslot;   // [max_routes] per miss rank: (2j+1) << 32 | slot (~0u: none)
   uint8_t* stage;              // [stage_n] slot-sized areas the step's misses are copied into
   int stage_n;
 };

@@ -516,6 +516,9 @@ struct FusedArgs {
   unsigned long long* epoch;   // grows by gridDim.x per launch: launch j = old / gridDim.x
   unsigned long long* pseq;    // 2j+1: slot ids and demand plan of launch j out; 2j+2: prefetch plan too
   unsigned long long* bar2;    // grid barrier of the computing CTAs
+  // [R] launch j's slot of its misses' rank i (ascending id): (2j+1) << 32 | slot,
+  // low word ~0u when not admitted; the tag makes an older launch's word stale
+  unsigned long long* sslot;
   uint8_t* stage;              // stage_n slot-sized areas the step's misses are copied into
   int stage_n;                 // (0: misses wait for the admission and go to their slots)
 };
@@ -544,6 +547,13 @@ __device__ __noinline__ void admit_cta(const DevState& st, const FusedArgs& a, u
     admit_body<false, kT>(st, a.layer, a.ids, a.slot_out, a.R, a.cap, dyn, sh, none, kMapPending);
   __threadfence();
   __syncthreads();
+  // the slot of each miss rank for the staging copies: the admitted misses are
+  // the first entries of the miss list (ascending id), one plan entry each
+  if (threadIdx.x < a.R) {
+    const int np0 = a.gplan0[0];
+    const uint32_t s = threadIdx.x < np0 ? (uint32_t)a.gplan0[1 + 3 * threadIdx.x] : ~0u;
+    a.sslot[threadIdx.x] = (2 * j + 1) << 32 | s;
+  }
   if (threadIdx.x == 0) st_release_u64(a.pseq, 2 * j + 1);
   if (a.pred && a.n_pred > 0) {
     prefetch_body<kT>(st, a.layer + 1, a.pred, a.n_pred, const_cast<int32_t*>(a.gplan1),
@@ -933,7 +943,12 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     }
   };
   // a staging piece: piece p of the step's missed experts, from pinned host
-  // memory into their staging entries (counted like the demand plan's pieces)
+  // memory into their staging entry and into the slot the admission gave the
+  // expert (a victim: no task of this step reads it), so the end of the launch
+  // only has to make the map entries valid.  While the host reads are in
+  // flight the warp polls CTA 0's word for the entry (the slot, tagged with
+  // this launch); the piece is counted (like the demand plan's pieces) once
+  // it is in the staging entry.
   auto stage_piece = [&](long p) {
     const int i = (int)(p / ppe), j = (int)(p - (long)i * ppe);
     const int e = s_pexp[i];
@@ -946,6 +961,28 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
 #pragma unroll
     for (int u = 0; u < kPiece / 512; ++u)
       if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
+    uint32_t sl = ~0u;  // the slot (warp-uniform), ~0u: none or timed out
+    {
+      const unsigned long long tag = seq0 + 1, t0 = now_ns();
+      for (;;) {
+        int s = 0;  // 1: this launch's word, 2: timed out
+        unsigned long long w = 0;
+        if (lane == 0) {
+          asm volatile("ld.relaxed.gpu.u64 %0, [%1];" : "=l"(w) : "l"(a.sslot + i) : "memory");
+          s = (w >> 32) == (tag & 0xffffffffull) ? 1 : (now_ns() - t0 > kWaitNs ? 2 : 0);
+        }
+        s = __shfl_sync(0xffffffffu, s, 0);
+        if (s == 1) {
+          sl = __shfl_sync(0xffffffffu, (uint32_t)w, 0);
+          break;
+        }
+        if (s == 2) {
+          if (lane == 0) flag_timeout(a.status);
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
 #pragma unroll
     for (int u = 0; u < kPiece / 512; ++u)
       if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
@@ -953,6 +990,12 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     if (lane == 0) {
       __threadfence();
       atomicAdd(a.gdone + i, 1);
+    }
+    if (sl < (uint32_t)st.S) {
+      uint4* sdst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(slot_blob((int)sl)) + off);
+#pragma unroll
+      for (int u = 0; u < kPiece / 512; ++u)
+        if (lane + 32 * u < nv) sdst[lane + 32 * u] = v[u];
     }
   };
   const bool pf_plan = a.gplan1 && (!ADMIT || (a.pred && a.n_pred > 0));  // a prefetch plan to copy
@@ -1311,39 +1354,15 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     }
   }
   if (ADMIT) {
-    // the admitted misses into their slots, and their map entries valid for
-    // later launches (every computing CTA read the map before the barrier)
-    if (npend > 0) {
+    // the admitted misses' map entries valid for later launches: every
+    // computing CTA read the map, and (staged steps) wrote its pieces into the
+    // slots, before the barrier
+    if (npend > 0 && cta == 0) {
       const int np0 = a.gplan0[0];
-      if (staged) {
-        for (long p = (long)warp * GF + cta; p < (long)np0 * ppe; p += Gw) {
-          const int i = (int)(p / ppe), j = (int)(p - (long)i * ppe);
-          const int s = a.gplan0[1 + 3 * i], L = a.gplan0[2 + 3 * i], e = a.gplan0[3 + 3 * i];
-          if ((unsigned)s >= (unsigned)st.S || L != a.layer || (unsigned)e >= (unsigned)st.E) continue;
-          int x = -1;  // its staging entry
-          for (int q = 0; q < npx; ++q)
-            if (s_pexp[q] == e) x = q;
-          if (x >= 0) {
-            const size_t off = (size_t)j * kPiece;
-            const int nv = (int)(min((size_t)kPiece, st.slot_bytes - off) / 16);
-            const uint4* src = reinterpret_cast<const uint4*>(a.stage + (size_t)x * st.stride + off);
-            uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(slot_blob(s)) + off);
-            uint4 v[kPiece / 512];
-#pragma unroll
-            for (int u = 0; u < kPiece / 512; ++u)
-              if (lane + 32 * u < nv) v[u] = src[lane + 32 * u];
-#pragma unroll
-            for (int u = 0; u < kPiece / 512; ++u)
-              if (lane + 32 * u < nv) dst[lane + 32 * u] = v[u];
-          }
-          if (j == 0 && lane == 0) st.map[a.layer * st.E + e] = s;
-        }
-      } else if (cta == 0) {
-        for (int i = threadIdx.x; i < np0; i += kT) {
-          const int s = a.gplan0[1 + 3 * i], e = a.gplan0[3 + 3 * i];
-          if ((unsigned)s < (unsigned)st.S && (unsigned)e < (unsigned)st.E)
-            st.map[a.layer * st.E + e] = s;
-        }
+      for (int i = threadIdx.x; i < np0; i += kT) {
+        const int s = a.gplan0[1 + 3 * i], L = a.gplan0[2 + 3 * i], e = a.gplan0[3 + 3 * i];
+        if ((unsigned)s < (unsigned)st.S && L == a.layer && (unsigned)e < (unsigned)st.E)
+          st.map[a.layer * st.E + e] = s;
       }
     }
     // staged steps copy the next layer's prefetches last
@@ -1578,6 +1597,7 @@ cudaError_t launch_layer_admit(const DevState& st, int wfmt, int H, int I, int l
   a.stage_n = sc.stage_n;
   a.pseq = sc.pseq;
   a.bar2 = sc.bar2;
+  a.sslot = sc.sslot;
   const int kt = tasks_per_row(kLayerAdmit, k, shared_blob != nullptr);
   const Plan p = fused_plan(wfmt, H, I, n_rows, kt, n_rows * kt, grid_of(kLayerAdmit));
   a.adm_cached = admit_cached(st.E, st.S) &&

@@ -47,7 +47,7 @@ namespace {
 thread_local char g_cuda_err[256] = "";
 
 int cuda_fail(cudaError_t e, const char* what) {
-  std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  std::snprintf(g_cuda_err, sizeof g_cuda_err, "%.160s: %.80s (%d)", what, cudaGetErrorString(e), (int)e);
   return MOE_ERR_CUDA;
 }
 
@@ -173,7 +173,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_status = cv.take<unsigned long long>(1),
                o_bar = cv.take<unsigned long long>(1),
                o_ep = cv.take<unsigned long long>(1), o_pseq = cv.take<unsigned long long>(1),
-               o_bar2 = cv.take<unsigned long long>(1);
+               o_bar2 = cv.take<unsigned long long>(1),
+               o_sslot = cv.take<unsigned long long>(std::max(d.max_routes, 1));
   c->mem_bytes = align_up(cv.off, 256);
   e = cudaMalloc(&c->mem, c->mem_bytes);
   if (e != cudaSuccess) return fail(cuda_fail(e, "cudaMalloc(state)"));
@@ -216,6 +217,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.epoch = reinterpret_cast<unsigned long long*>(m + o_ep);
   c->sc.pseq = reinterpret_cast<unsigned long long*>(m + o_pseq);
   c->sc.bar2 = reinterpret_cast<unsigned long long*>(m + o_bar2);
+  c->sc.sslot = reinterpret_cast<unsigned long long*>(m + o_sslot);
   c->sc.x16 = reinterpret_cast<uint16_t*>(m + o_x16);
   c->sc.xinv = reinterpret_cast<float*>(m + o_xinv);
   c->sc.y = reinterpret_cast<float*>(m + o_y);

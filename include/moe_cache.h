@@ -293,10 +293,11 @@ MOE_API int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const i
  *     resident experts at once and compute the shared and routed experts;
  *   - an uncapped step's misses are copied from pinned host memory into
  *     staging entries (up to max_routes experts within 64 MB, allocated at
- *     create) as soon as they are known, computed from there, and copied into
- *     their slots at the end of the launch; with a fetch cap they wait for the
- *     admission's slots and are copied there directly; the prefetch plan's
- *     experts are copied into their slots in the same launch.
+ *     create) as soon as they are known and computed from there; each piece
+ *     also goes into the expert's slot once the admission has chosen it, and
+ *     the pending marks are cleared at the end of the launch; with a fetch cap
+ *     they wait for the admission's slots and are copied there directly; the
+ *     prefetch plan's experts are copied into their slots in the same launch.
  * The overlap of [P2] (the gather beside the shared expert) happens inside
  * that launch instead of on two streams; side_stream is not used.  If the
  * shapes do not fit, the admission and prefetch run as their own launches
