@@ -1232,12 +1232,22 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   // h of the tasks this CTA's rows need, read once from L2 into shared memory
   // (every warp reading it from L2 would hammer a few cache lines)
   const int tlo = ru1 > ru0 ? ts[bA] : 0, thi = ru1 > ru0 ? ts[bB + 1] : 0;
-  {
+  {  // up to kHU loads of each thread in flight before any is stored
+    constexpr int kHU = 4;
     float4* h4 = reinterpret_cast<float4*>(hsm);
     const int n4 = (thi - tlo) * I / 4, i4 = I / 4;
-    for (int i = threadIdx.x; i < n4; i += kT) {
-      const int tt = tlo + i / i4;
-      h4[i] = __ldcg(reinterpret_cast<const float4*>(a.h + (size_t)tk.route[tt] * I) + (i % i4));
+    for (int i0 = threadIdx.x; i0 < n4; i0 += kHU * kT) {
+      float4 hv4[kHU];
+#pragma unroll
+      for (int u = 0; u < kHU; ++u) {
+        const int i = i0 + u * kT;
+        if (i < n4)
+          hv4[u] = __ldcg(reinterpret_cast<const float4*>(a.h + (size_t)tk.route[tlo + i / i4] * I) +
+                          (i % i4));
+      }
+#pragma unroll
+      for (int u = 0; u < kHU; ++u)
+        if (i0 + u * kT < n4) h4[i0 + u * kT] = hv4[u];
     }
   }
   __syncthreads();  // h visible to every warp
