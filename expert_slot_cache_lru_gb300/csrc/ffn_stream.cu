@@ -441,13 +441,13 @@ __device__ __forceinline__ float itemb_dot(const ItemB<FMT>& it, const float* hv
 // One CTA per SM, launched cooperatively, so every CTA of the grid is resident.
 // `ctr` only grows: each launch adds n (the CTAs taking part), and a CTA waits
 // until the count reaches the next multiple of n.  Release/acquire at GPU
-// scope orders the h written before the barrier with the reads after it.
-// Bounded spin.
+// scope orders the h written before the barrier with the reads after it: the
+// block barrier orders every thread's writes before thread 0's release add,
+// and release is cumulative, so no separate fence is needed.  Bounded spin.
 __device__ bool grid_barrier(unsigned long long* ctr, unsigned long long* status, unsigned n) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
     unsigned long long old;
     asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
     const unsigned long long target = (old / n + 1) * n;
