@@ -487,6 +487,101 @@ def wide_step(dev: int, reps: int = 5) -> dict:
             "step_ms": round(t_adm + t_gat + t_ffn, 3)}
 
 
+def hybrid_step(dev: int, warm: int = 4, tokens: int = 8) -> dict:
+    """The hybrid decode: 48 bf16 layers (H 4096, I 1024, 256 experts, top-8),
+    a 1,024-slot shared pool, fetch cap 4 and 8 look-ahead predictions per
+    layer, host blobs aliased onto 96.  Each layer is moe_decode_layer with
+    MOE_FUSED | MOE_HYBRID: the routes the capped admission leaves at -1 run
+    on the host's cores (the hybrid CPU executor) and are added to the GPU's
+    output.  Timed with CUDA events over `tokens` tokens after `warm`; the same
+    pipeline without MOE_HYBRID (the GPU partial alone) is timed beside it on a
+    second cache.  The executor's figure is the expert bytes its -1 routes
+    stream per second of its busy time."""
+    import torch
+
+    import expert_slot_cache_lru_gb300 as m
+    import synth
+    w = synth.workloads()["hybrid_prefetch"]
+    blobs = synth.HostBlobs(w, pinned=True)
+    ids, wts = synth.make_routing(w, steps=warm + tokens)
+    L, R = w.n_layers, w.routes
+    s = torch.cuda.Stream()
+    n_threads = max(1, min(16, os.cpu_count() or 1))
+    res = {"threads": n_threads, "tokens": tokens}
+    for hybrid in (True, False):
+        storage = torch.empty(w.n_slots * blobs.stride, dtype=torch.uint8, device="cuda")
+        cache = m.SlotCache(n_layers=L, n_experts=w.n_experts, n_slots=w.n_slots,
+                            pool_mode=m.MOE_POOL_SHARED, hidden=w.hidden, inter=w.inter,
+                            wfmt=w.fmt, slot_storage=storage, slot_stride=blobs.stride,
+                            host_blob_ptrs=blobs.addrs(), max_routes=R, max_rows=w.batch,
+                            max_pred=w.n_pred)
+        if hybrid:
+            m.moe_hybrid_start(cache.handle, n_threads)
+        flags = m.MOE_FUSED | (m.MOE_HYBRID if hybrid else 0)
+        d_x = torch.empty(L, w.batch, w.hidden, dtype=torch.int16, device="cuda")
+        d_ids = torch.empty(L, R, dtype=torch.int32, device="cuda")
+        d_w = torch.empty(L, R, dtype=torch.float32, device="cuda")
+        d_pred = torch.empty(L, w.n_pred, dtype=torch.int32, device="cuda")
+        d_slots = torch.empty(L, R, dtype=torch.int32, device="cuda")
+        out = torch.empty(L, w.batch, w.hidden, dtype=torch.bfloat16, device="cuda")
+        inputs = []
+        for t in range(warm + tokens):
+            pred = np.stack([synth.make_predictions(w, ids[t, l + 1], t, l) if l + 1 < L else
+                             np.zeros(w.n_pred, np.int32) for l in range(L)]).astype(np.int32)
+            inputs.append((synth.make_hidden(w, t).view(np.int16), ids[t].reshape(L, -1),
+                           wts[t].reshape(L, -1), pred))
+
+        def load(t):
+            x, i, wt, pr = inputs[t]
+            d_x.copy_(torch.from_numpy(x))
+            d_ids.copy_(torch.from_numpy(np.ascontiguousarray(i)))
+            d_w.copy_(torch.from_numpy(np.ascontiguousarray(wt)))
+            d_pred.copy_(torch.from_numpy(pr))
+
+        def layers():
+            for l in range(L):
+                has = l + 1 < L
+                m.moe_decode_layer(cache.handle, l, d_x[l], d_ids[l], d_w[l], d_slots[l], w.batch,
+                                   w.top_k, w.fetch_cap, d_pred[l] if has else None,
+                                   w.n_pred if has else 0, None, None, out[l], s, None, flags)
+
+        with torch.cuda.stream(s):
+            for t in range(warm):
+                load(t)
+                layers()
+        s.synchronize()
+        c0 = m.moe_hybrid_counters(cache.handle) if hybrid else None
+        ms = 0.0
+        for t in range(warm, warm + tokens):  # input copies stay outside the timed region
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                load(t)
+                e0.record(s)
+                layers()
+                e1.record(s)
+            s.synchronize()
+            ms += e0.elapsed_time(e1)
+        st = [cache.stats(l) for l in range(L)]
+        key = "hybrid" if hybrid else "gpu_partial_only"
+        res[key] = {"tok_s": round(tokens / (ms * 1e-3), 2), "ms_per_token": round(ms / tokens, 3),
+                    "timeouts": int(any(x["status_bits"] & 4 for x in st))}
+        if hybrid:
+            c1 = m.moe_hybrid_counters(cache.handle)
+            jobs = c1["jobs"] - c0["jobs"]
+            routes = c1["cpu_routes"] - c0["cpu_routes"]
+            busy = (c1["busy_ns"] - c0["busy_ns"]) * 1e-9
+            res[key].update({"jobs": jobs, "cpu_routes": routes,
+                             "cpu_routes_per_token": round(routes / tokens, 2),
+                             "cpu_busy_us_per_job": round(busy / max(jobs, 1) * 1e6, 1),
+                             "cpu_expert_gbs": round(routes * w.blob_bytes / max(busy, 1e-9) / 1e9,
+                                                     1)})
+            m.moe_hybrid_stop(cache.handle)
+        cache.close()
+        del storage
+        torch.cuda.empty_cache()
+    return res
+
+
 def cpu_baseline(seconds: float = 15.0) -> dict:
     """The oracle as it stands, single-threaded on this host: admission plus
     fp64 layer math for as many layers of the benchmark's tokens as fit in
@@ -547,6 +642,10 @@ def run_native(args) -> None:
     if args.wide_only:  # profiler runs: the wide decode step alone
         if rank == 0:
             print(json.dumps({"wide_only": True, **wide_step(local)}), flush=True)
+        return
+    if args.hybrid_only:
+        if rank == 0:
+            print(json.dumps({"hybrid_only": True, **hybrid_step(local)}), flush=True)
         return
     dec = Decode(local, overlap=not args.serial, warm_tokens=args.warm_tokens,
                  n_layers=args.layers, n_slots=args.slots, fused=not args.unfused)
@@ -623,6 +722,7 @@ def run_native(args) -> None:
     gather = dec.gather_bandwidth()
     adm = admission_sweep(local)
     wide = wide_step(local)
+    hyb = hybrid_step(local) if not args.no_hybrid else None
     hbm = peaks.get("hbm_gbs", 6800.0)
     tr = routed_traffic()
     line = {
@@ -669,6 +769,7 @@ def run_native(args) -> None:
                      "peak_source": f"{peaks['_source']} (MEASURED_PEAKS.json hbm_gbs)"},
         "admission_us_per_layer": adm,
         "wide_decode_step": wide,
+        "hybrid_decode": hyb,
         "gather": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in gather.items()},
         "setup_s": {k: round(v, 1) for k, v in dec.setup_s.items()},
         "clocks": sampler.summary(),
@@ -745,6 +846,9 @@ def main():
     ap.add_argument("--settle-s", type=float, default=3.0,
                     help="seconds of untimed decode before the warm-up steps (steady state)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-hybrid", action="store_true", help="skip the hybrid-executor decode")
+    ap.add_argument("--hybrid-only", action="store_true",
+                    help="run only the hybrid-executor decode and print it")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--warm-tokens", type=int, default=WARM_TOKENS,
                     help="eager tokens that warm the cache before the graph is captured")

@@ -40,6 +40,7 @@ MOE_PLAN_DEMAND = 0
 MOE_PLAN_PREFETCH = 1
 MOE_OVERLAP = 1
 MOE_FUSED = 2
+MOE_HYBRID = 4
 MOE_STATUS_INVALID_ID = 1
 MOE_STATUS_CAPACITY = 2
 
@@ -92,6 +93,10 @@ _SIGS = {
     "moe_read_stats": [_vp, _i, C.POINTER(moe_stats)],
     "moe_device_views": [_vp, C.POINTER(moe_views)],
     "moe_cache_fail_next_gather": [_vp, _i],
+    "moe_hybrid_start": [_vp, _i],
+    "moe_hybrid_stop": [_vp],
+    "moe_hybrid_counters": [_vp, _vp],
+    "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
     "moe_last_cuda_error": [],
     "moe_abi_version": [],
@@ -225,6 +230,41 @@ def moe_device_views(cache: int) -> moe_views:
 
 def moe_cache_fail_next_gather(cache: int, n: int = 1) -> None:
     _check("moe_cache_fail_next_gather", _lib.moe_cache_fail_next_gather(cache, n))
+
+
+def moe_hybrid_start(cache: int, n_threads: int) -> None:
+    _check("moe_hybrid_start", _lib.moe_hybrid_start(cache, n_threads))
+
+
+def moe_hybrid_stop(cache: int) -> None:
+    _check("moe_hybrid_stop", _lib.moe_hybrid_stop(cache))
+
+
+def moe_hybrid_counters(cache: int) -> dict:
+    import numpy as np
+    out = np.zeros(3, np.uint64)
+    _check("moe_hybrid_counters", _lib.moe_hybrid_counters(cache, out.ctypes.data))
+    return {"jobs": int(out[0]), "cpu_routes": int(out[1]), "busy_ns": int(out[2])}
+
+
+def moe_cpu_experts(wfmt: int, hidden: int, inter: int, blob_ptrs, x_bf16, ids, slot_ids, w,
+                    n_threads: int = 1):
+    """The hybrid executor's CPU partial as a host call: ``blob_ptrs`` [E] host
+    blob addresses of one layer, ``x_bf16`` uint16 [B, H], ``ids`` /
+    ``slot_ids`` int32 and ``w`` float32 [B, k]; returns float32 [B, H]."""
+    import numpy as np
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    B = x.shape[0]
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(B, -1)
+    k = ids.shape[1]
+    slot_ids = np.ascontiguousarray(slot_ids, dtype=np.int32).reshape(B, k)
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(B, k)
+    ptrs = np.ascontiguousarray(np.asarray(blob_ptrs, dtype=np.uint64))
+    out = np.empty((B, hidden), np.float32)
+    _check("moe_cpu_experts", _lib.moe_cpu_experts(
+        wfmt, hidden, inter, ptrs.ctypes.data, len(ptrs), x.ctypes.data, ids.ctypes.data,
+        slot_ids.ctypes.data, w.ctypes.data, B, k, n_threads, out.ctypes.data))
+    return out
 
 
 def blob_bytes(wfmt: int, hidden: int, inter: int) -> int:

@@ -33,6 +33,7 @@ def _compile(src: str, extra: list[str]) -> str:
     if os.path.exists(obj) and os.path.getmtime(obj) >= newest and not extra:
         return obj
     cmd = [NVCC, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+           "-Xcompiler", "-ffp-contract=off",
            "-Xcompiler", "-fvisibility=hidden", "-c", src, "-o", obj, *extra]
     subprocess.run(cmd, check=True)
     return obj

@@ -228,4 +228,19 @@ cudaError_t launch_routed_noalloc(int wfmt, int H, int I, const uint8_t* slots, 
                                   const float* w, int n_rows, int k, void* out,
                                   unsigned long long* status, void* scratch, cudaStream_t s);
 
+// The hybrid CPU executor (hybrid.cu): a host thread pool computing the
+// routes left at -1, fed and joined through a mailbox in mapped host memory.
+struct HybridConfig {
+  int wfmt, H, I, E, L, max_rows, max_routes, n_threads;
+  const void* const* host_blobs;  // [L*E] host addresses of the expert blobs
+};
+int hybrid_start(const HybridConfig& c, moe_cpu_exec** out);  // MOE_OK, MOE_ERR_*, or
+                                                               // -1000 - cudaError_t
+void hybrid_stop(moe_cpu_exec* x);
+void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[3]);
+cudaError_t hybrid_post(moe_cpu_exec* x, int layer, const int32_t* ids, const int32_t* slots,
+                        const float* w, const void* xin, int n_rows, int k, cudaStream_t s);
+cudaError_t hybrid_add(moe_cpu_exec* x, void* out, int n_rows, unsigned long long* status,
+                       cudaStream_t s);
+
 }  // namespace moe

@@ -40,6 +40,8 @@ struct moe_cache {
   int down_k_max = 0;        // largest k the down kernel's shared memory was sized for
   int last_pf_layer = 0;     // target layer of the last prefetch enqueued (selects its plan)
   bool stream_ffn = true;    // decode-sized steps use the streaming FFN kernels
+  std::vector<const void*> host_ptrs;  // [L*E] host blob addresses, copied at create
+  moe_cpu_exec* cpu = nullptr;         // hybrid CPU executor, when started
 };
 
 namespace {
@@ -234,6 +236,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   if (e != cudaSuccess) return fail(cuda_fail(e, "state init"));
 
   if (d.slot_bytes > 0) {
+    c->host_ptrs.assign(d.host_experts, d.host_experts + K);
     std::vector<const uint8_t*> dev(K);
     for (size_t k = 0; k < K; ++k) {
       const void* hp = d.host_experts[k];
@@ -291,6 +294,7 @@ int moe_cache_destroy(moe_cache* c) {
   int rc = MOE_OK;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) rc = cuda_fail(e, "destroy sync");
+  moe::hybrid_stop(c->cpu);
   if (c->ev_ready) cudaEventDestroy(c->ev_ready);
   if (c->ev_done) cudaEventDestroy(c->ev_done);
   if (c->mem) cudaFree(c->mem);
@@ -330,7 +334,7 @@ int moe_cache_prefill(moe_cache* c, int layer, const int32_t* h_ids, int n, void
   if (d.slot_bytes > 0) {
     for (int i = 0; i < n; ++i) {
       uint8_t* dst = c->st.slots + ((size_t)p * S + slot_of[i]) * c->st.stride;
-      CK(cudaMemcpyAsync(dst, d.host_experts[(size_t)layer * E + h_ids[i]], d.slot_bytes,
+      CK(cudaMemcpyAsync(dst, c->host_ptrs[(size_t)layer * E + h_ids[i]], d.slot_bytes,
                          cudaMemcpyHostToDevice, as_stream(stream)));
     }
     CK(cudaStreamSynchronize(as_stream(stream)));
@@ -484,13 +488,25 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
   if (pf && (layer + 1 >= c->d.n_layers || c->d.max_pred == 0)) return MOE_ERR_INVALID_ARG;
   if (pf && n_pred > c->d.max_pred) return MOE_ERR_CAPACITY;
   const bool overlap = (flags & MOE_OVERLAP) != 0;
+  const bool hybrid = (flags & MOE_HYBRID) != 0;
+  if (hybrid && !c->cpu) return MOE_ERR_STATE;
   cudaStream_t cs = as_stream(compute_stream), ss = as_stream(side_stream);
+  // hybrid [P1 section 4]: the step goes to the host right after the
+  // admission, and the host's partial is added after the GPU's combine
+  auto post = [&]() -> cudaError_t {
+    return hybrid ? moe::hybrid_post(c->cpu, layer, d_ids, d_slot_ids, d_w, d_x, n_rows, k, cs)
+                  : cudaSuccess;
+  };
+  auto add_cpu = [&]() -> int {
+    if (hybrid) CK(moe::hybrid_add(c->cpu, d_out, n_rows, c->st.status, cs));
+    return MOE_OK;
+  };
   const moe_cache_desc& dd = c->d;
   const bool fused = (flags & MOE_FUSED) && c->stream_ffn && dd.slot_bytes > 0 &&
                      (!d_shared_blob || dd.shared_inter == dd.inter) &&
                      moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k,
                                                  d_shared_blob != nullptr);
-  if (fused && moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k,
+  if (fused && !hybrid && moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k,
                                          d_shared_blob != nullptr)) {
     // one launch for the whole layer: admission (and prefetch admission) in
     // CTA 0, gathers + shared expert + routed experts in the others
@@ -504,6 +520,7 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
   }
   if (fused) {  // admission, then one launch: gathers + shared expert + routed experts
     CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
+    CK(post());
     int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
     if (pf) {
       CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, cs));
@@ -513,11 +530,12 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
                                 n_rows, k, static_cast<const uint8_t*>(d_shared_blob),
                                 d_shared_gate, c->st.plan_demand, pf ? pf_plan : nullptr, d_out,
                                 c->sc, c->st.status, cs));
-    return MOE_OK;
+    return add_cpu();
   }
   if (overlap && !side_stream) return MOE_ERR_INVALID_ARG;
 
   CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
+  CK(post());
   int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
   if (pf) {
     CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, cs));
@@ -529,7 +547,7 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
     if ((rc = run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out, cs)))
       return rc;
     if (pf) CK(moe::launch_gather(c->st, pf_plan, c->gather_grid, cs));
-    return MOE_OK;
+    return add_cpu();
   }
   // fork
   CK(cudaEventRecord(c->ev_ready, cs));
@@ -545,7 +563,38 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
   if (side_err != cudaSuccess) return cuda_fail(side_err, "gather (side stream)");
   if (join != cudaSuccess) return cuda_fail(join, "join");
   if (shared_rc != MOE_OK) return shared_rc;
-  return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out, cs);
+  if ((rc = run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out,
+                       cs)))
+    return rc;
+  return add_cpu();
+}
+
+int moe_hybrid_start(moe_cache* c, int n_threads) {
+  if (!c || n_threads < 1 || n_threads > 256) return MOE_ERR_INVALID_ARG;
+  if (c->cpu || c->d.hidden <= 0 || c->host_ptrs.empty()) return MOE_ERR_STATE;
+  moe::HybridConfig hc{c->d.wfmt, c->d.hidden, c->d.inter, c->d.n_experts, c->d.n_layers,
+                       c->d.max_rows, c->d.max_routes, n_threads, c->host_ptrs.data()};
+  const int rc = moe::hybrid_start(hc, &c->cpu);
+  if (rc <= -1000) return cuda_fail((cudaError_t)(-1000 - rc), "hybrid executor");
+  return rc;
+}
+
+int moe_hybrid_stop(moe_cache* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (!c->cpu) return MOE_OK;
+  const cudaError_t e = cudaDeviceSynchronize();
+  moe::hybrid_stop(c->cpu);
+  c->cpu = nullptr;
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "hybrid stop sync");
+}
+
+int moe_hybrid_counters(moe_cache* c, uint64_t h_out[3]) {
+  if (!c || !h_out) return MOE_ERR_INVALID_ARG;
+  if (!c->cpu) return MOE_ERR_STATE;
+  unsigned long long v[3];
+  moe::hybrid_counters(c->cpu, v);
+  for (int i = 0; i < 3; ++i) h_out[i] = v[i];
+  return MOE_OK;
 }
 
 int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out) {

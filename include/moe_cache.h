@@ -130,6 +130,8 @@ typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 #define MOE_OVERLAP 1u        /* gather on the side stream, joined by events [P2] */
 #define MOE_FUSED 2u          /* one launch per layer: the admission, the gathers, the shared
                                  expert and the routed experts (decode-sized steps) */
+#define MOE_HYBRID 4u         /* routes left at -1 run on the host's cores and are added to
+                                 the output (needs moe_hybrid_start) [P1] */
 
 /* status_bits of moe_stats */
 #define MOE_STATUS_INVALID_ID 1ull
@@ -137,6 +139,7 @@ typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 #define MOE_STATUS_TIMEOUT 4ull   /* a bounded device wait gave up (reported in every layer) */
 
 typedef struct moe_cache moe_cache; /* opaque */
+typedef struct moe_cpu_exec moe_cpu_exec; /* opaque: a cache's hybrid CPU executor */
 
 typedef struct {
   int n_layers;                    /* > 0 */
@@ -309,6 +312,50 @@ MOE_API int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int
                      const int32_t* d_pred, int n_pred, const void* d_shared_blob,
                      const void* d_shared_gate, void* d_out, void* compute_stream,
                      void* side_stream, unsigned flags);
+
+/* ---------------------------------------------------------- hybrid CPU executor
+ * [P1 section 4 "How decode works after this PR", section 5 "How routes are
+ * split"]: the routes a capped admission leaves at -1 (fetch-cap overflow or
+ * no evictable slot) are computed on the host from the pinned host blobs,
+ * while the GPU computes the routes that got a slot; the partial outputs are
+ * added.  For route r = b*k + j with slot -1 and a valid expert id e:
+ *   h = silu(W_g x_b) * (W_u x_b),  cpu[b] = sum_j w[b,j] * (W_d h)   (fp32,
+ *   j ascending; rows without such a route give 0),
+ * and with MOE_HYBRID the layer output becomes
+ *   out[b] = bf16( float(gpu_out[b]) + cpu[b] ),
+ * gpu_out being the output moe_decode_layer computes without the flag.
+ *
+ * moe_hybrid_start: start the cache's executor, a pool of n_threads (1..256)
+ * host threads, and its mailbox (mapped pinned memory, max_rows*H inputs and
+ * outputs).  The host blob pointers given at create are read by these
+ * threads; they must be host-readable (pinned host memory is).  MOE_ERR_STATE
+ * if one is running or the cache has no expert shapes / host blobs.
+ * moe_hybrid_stop: synchronise the device and stop the pool (also done by
+ * moe_cache_destroy).
+ *
+ * With flags & MOE_HYBRID, moe_decode_layer enqueues, right after the
+ * admission, a kernel that posts the step (ids, slot ids, weights, x) to the
+ * mailbox with a system-scope release of a job number; the pool takes the
+ * job, computes the CPU partial and publishes the number back; after the GPU
+ * experts and the combine a second kernel waits for it (bounded: after 1 s it
+ * sets MOE_STATUS_TIMEOUT and leaves the GPU partial) and adds the partial.
+ * Every step posts a job, even one without -1 routes, so a captured graph
+ * does not depend on the hit pattern; both kernels are capturable.  With
+ * MOE_FUSED the admission runs as its own launch, followed by the post and
+ * the one-launch gather + experts kernel.  MOE_ERR_STATE if no executor runs. */
+MOE_API int moe_hybrid_start(moe_cache* c, int n_threads);
+MOE_API int moe_hybrid_stop(moe_cache* c);
+/* jobs done, CPU routes computed, nanoseconds the coordinator spent on jobs */
+MOE_API int moe_hybrid_counters(moe_cache* c, uint64_t h_out[3]);
+
+/* The CPU partial above as a plain host function (no GPU, no cache): h_blobs
+ * [n_experts] host blob addresses of one layer; h_x bf16 [n_rows][H]; h_ids,
+ * h_slot_ids int32 and h_w float [n_rows][k]; h_out float [n_rows][H].  Uses
+ * n_threads host threads (1..256); the result does not depend on n_threads. */
+MOE_API int moe_cpu_experts(int wfmt, int hidden, int inter, const void* const* h_blobs,
+                            int n_experts, const uint16_t* h_x, const int32_t* h_ids,
+                            const int32_t* h_slot_ids, const float* h_w, int n_rows, int k,
+                            int n_threads, float* h_out);
 
 /* Copy one layer's counters to the host.  Synchronises the device. */
 MOE_API int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out);

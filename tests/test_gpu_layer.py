@@ -25,8 +25,10 @@ class Stepper:
     """Feeds one workload's steps through moe_decode_layer, mirroring every
     admission/prefetch on the oracle."""
 
-    def __init__(self, rig: Rig, overlap: bool = True, n_pred: int = 0, fused: bool = False):
+    def __init__(self, rig: Rig, overlap: bool = True, n_pred: int = 0, fused: bool = False,
+                 hybrid: bool = False):
         self.rig = rig
+        self.hybrid = hybrid
         self.overlap = overlap
         self.fused = fused
         self.n_pred = n_pred
@@ -42,7 +44,8 @@ class Stepper:
         d_x = _dev(x)
         d_ids = _dev(ids.reshape(w.n_layers, -1))
         d_w = _dev(wts.reshape(w.n_layers, -1))
-        flags = (m.MOE_OVERLAP if self.overlap else 0) | (m.MOE_FUSED if self.fused else 0)
+        flags = ((m.MOE_OVERLAP if self.overlap else 0) | (m.MOE_FUSED if self.fused else 0) |
+                 (m.MOE_HYBRID if self.hybrid else 0))
         refs = []
         for layer in range(w.n_layers):
             pred = None
@@ -320,3 +323,91 @@ def test_hybrid_capped_prefetch_partial_plus_cpu():
                 assert np.all(np.abs(got - full) <= atol + rtol * np.abs(full)), (t, layer)
     tot = [rig.sc.stats(l) for l in range(w.n_layers)]
     assert sum(s["overflow_routes"] for s in tot) > 0 and sum(s["pf_filled"] for s in tot) > 0
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_hybrid_executor_adds_the_cpu_partial(fused):
+    """MOE_HYBRID [FreeToken PR #491, sections 4-5]: the routes the capped
+    admission leaves at -1 run on the host's cores and are added to the GPU's
+    output; the whole layer must match the fp64 oracle's full layer (all
+    routes) within the bf16 tolerance, every step posts one job (also steps
+    with no -1 route), and the executor counts exactly the -1 routes."""
+    w = synth.scaled(synth.workloads()["hybrid_prefetch"], n_layers=6, steps=4)
+    rig = Rig(w)
+    rig.m.moe_hybrid_start(rig.sc.handle, 8)
+    st = Stepper(rig, n_pred=w.n_pred, fused=fused, hybrid=True)
+    ids, wts = synth.make_routing(w)
+    n_cpu = 0
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        refs = st.step(t, ids[t], wts[t], x)
+        for layer in range(w.n_layers):
+            n_cpu += int((refs[layer]["slots"] < 0).sum())
+            full = rig.oracle_layer(layer, x[layer], ids[t, layer], wts[t, layer])
+            assert_close(st.out[layer], full, w.fmt, what=f"step {t} layer {layer}")
+    c = rig.m.moe_hybrid_counters(rig.sc.handle)
+    assert c["jobs"] == w.steps * w.n_layers
+    assert c["cpu_routes"] == n_cpu > 0
+    for layer in range(w.n_layers):
+        assert not rig.sc.stats(layer)["status_bits"] & 4  # no timed-out wait
+    rig.m.moe_hybrid_stop(rig.sc.handle)
+
+
+def test_hybrid_graph_replay_equals_eager():
+    """The hybrid layers captured once as a CUDA graph and replayed with new
+    routes equal the eager calls byte for byte, cache state included: the
+    host side is driven by the job numbers the graph's kernels post."""
+    w = synth.scaled(synth.workloads()["hybrid_prefetch"], n_layers=6, steps=4)
+    blobs = synth.HostBlobs(w, pinned=True)
+    eager, graphed = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    m = graphed.m
+    for r in (eager, graphed):
+        m.moe_hybrid_start(r.sc.handle, 8)
+    se = Stepper(eager, n_pred=w.n_pred, fused=True, hybrid=True)
+    ids, wts = synth.make_routing(w)
+    L, R = w.n_layers, w.routes
+    b_x = torch.empty(L, w.batch, w.hidden, dtype=torch.int16, device="cuda")
+    b_ids = torch.empty(L, R, dtype=torch.int32, device="cuda")
+    b_w = torch.empty(L, R, dtype=torch.float32, device="cuda")
+    b_pred = torch.empty(L, w.n_pred, dtype=torch.int32, device="cuda")
+    b_slots = torch.empty(L, R, dtype=torch.int32, device="cuda")
+    b_out = torch.empty(L, w.batch, w.hidden, dtype=torch.bfloat16, device="cuda")
+    cs = torch.cuda.Stream()
+    flags = m.MOE_FUSED | m.MOE_HYBRID
+
+    def enqueue():
+        for layer in range(L):
+            has_pred = layer + 1 < L
+            m.moe_decode_layer(graphed.sc.handle, layer, b_x[layer], b_ids[layer], b_w[layer],
+                               b_slots[layer], w.batch, w.top_k, w.fetch_cap,
+                               b_pred[layer] if has_pred else None, w.n_pred if has_pred else 0,
+                               None, None, b_out[layer], cs, None, flags)
+
+    def load(t):
+        b_x.copy_(_dev(synth.make_hidden(w, t)))
+        b_ids.copy_(_dev(ids[t].reshape(L, -1)))
+        b_w.copy_(_dev(wts[t].reshape(L, -1)))
+        for layer in range(L - 1):
+            b_pred[layer].copy_(_dev(synth.make_predictions(w, ids[t, layer + 1], t, layer)))
+
+    load(0)
+    with torch.cuda.stream(cs):
+        enqueue()
+    torch.cuda.synchronize()
+    se.step(0, ids[0], wts[0], synth.make_hidden(w, 0))
+    assert torch.equal(b_out.view(torch.int16), se.out.view(torch.int16))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        enqueue()
+    for t in range(1, w.steps):
+        load(t)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        se.step(t, ids[t], wts[t], synth.make_hidden(w, t))
+        assert torch.equal(b_out.view(torch.int16), se.out.view(torch.int16)), f"token {t}"
+        assert torch.equal(b_slots, se.slots)
+    for layer in range(L):
+        assert graphed.sc.stats(layer) == eager.sc.stats(layer)
+    ce, cg = (m.moe_hybrid_counters(r.sc.handle) for r in (eager, graphed))
+    assert ce["jobs"] == cg["jobs"] == w.steps * L and ce["cpu_routes"] == cg["cpu_routes"]
