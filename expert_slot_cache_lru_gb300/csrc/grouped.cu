@@ -348,6 +348,159 @@ __global__ void __launch_bounds__(kWT) gup_kernel(DevState st, int H, int I, int
   }
 }
 
+// ------------------------------------------------------------ 3b. gate / up, staged
+// The NVFP4 gate/up kernel for H a multiple of 64, with the same arithmetic as
+// gup_kernel (so the same bits) but a different data path: a work item's 256
+// weight rows are streamed through shared memory in stages of 64 elements
+// (32 code bytes and 4 scale bytes per row and matrix), kNS stages in flight
+// with cp.async.  The copies are coalesced -- two lanes per row, 16 rows per
+// warp instruction, whole 32-byte sectors -- where one-row-per-thread global
+// loads touch 32 lines per instruction.  Each thread then reads its own row
+// from shared memory; the two 16-byte halves of a row's 32 code bytes are
+// swapped on every other group of four rows, so a quarter-warp's 16-byte
+// reads fall on eight distinct bank groups.
+constexpr int kNS = 4;                    // stages in flight
+constexpr int kStC = 32 * kRowsItem;      // code bytes per matrix per stage
+constexpr int kStS = 4 * kRowsItem;       // scale bytes per matrix per stage
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_stages() {  // all but the kNS - 2 newest groups landed
+  asm volatile("cp.async.wait_group %0;" ::"n"(kNS - 2) : "memory");
+}
+// the 16-byte half c of row r's 32 code bytes within a stage
+__device__ __forceinline__ int half_at(int r, int c) { return r * 32 + ((c ^ (r >> 2)) & 1) * 16; }
+
+// Stage s of one matrix's rows [r0, r0 + 256) (clamped to n_rows - 1): codes
+// (row stride cb bytes) at dc, scales (row stride sb) at ds.
+__device__ __forceinline__ void stage_rows(uint8_t* dc, uint8_t* ds, const uint8_t* codes,
+                                           const uint8_t* scales, int r0, int n_rows, int cb,
+                                           int sb, int s) {
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int rr = (t >> 1) + (kRowsItem / 2) * u, c = t & 1;
+    const int row = min(r0 + rr, n_rows - 1);
+    cp16(dc + half_at(rr, c), codes + (size_t)row * cb + s * 32 + c * 16);
+  }
+  const int row = min(r0 + t, n_rows - 1);
+  cp4(ds + t * 4, scales + (size_t)row * sb + s * 4);
+}
+
+__global__ void __launch_bounds__(kWT, 2) gup_staged_kernel(DevState st, int H, int I, int layer,
+                                                            const uint16_t* __restrict__ x16,
+                                                            const float* __restrict__ xinv,
+                                                            int k, Groups gr,
+                                                            float* __restrict__ h) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint4* xs = reinterpret_cast<uint4*>(dsm);  // [kNR][H / 8]
+  uint8_t* stg = dsm + (size_t)kNR * H * 2;   // [kNS][gate codes | up codes | gate sc | up sc]
+  constexpr int kStage = 2 * kStC + 2 * kStS;
+  const int G = gr.G();
+  const int nch = (I + kRowsItem - 1) / kRowsItem;
+  const int Hu = H / 8, nst = H / 64;
+  const Off o(H, I);
+  const size_t pbase = (size_t)pool_of(st, layer) * st.S;
+  const int t = threadIdx.x;
+  for (int item = blockIdx.x; item < G * nch; item += gridDim.x) {
+    const int g = item / nch, ch = item - g * nch;
+    const int ra = gr.start()[g], rb = gr.start()[g + 1];
+    const uint8_t* blob = st.slots + (pbase + gr.slot()[g]) * st.stride;
+    const int i0 = ch * kRowsItem, i = i0 + t;
+    const float gs0 = reinterpret_cast<const float*>(blob + o.glob)[0];
+    const float gs1 = reinterpret_cast<const float*>(blob + o.glob)[1];
+    auto issue = [&](int s) {
+      uint8_t* b = stg + (s % kNS) * kStage;
+      stage_rows(b, b + 2 * kStC, blob + o.code[0], blob + o.scale[0], i0, I, H / 2, H / 16, s);
+      stage_rows(b + kStC, b + 2 * kStC + kStS, blob + o.code[1], blob + o.scale[1], i0, I, H / 2,
+                 H / 16, s);
+    };
+    for (int q0 = ra; q0 < rb; q0 += kNR) {  // up to kNR routes per pass
+      const int nq = min(kNR, rb - q0);
+      __syncthreads();  // the previous pass's x and stages no longer read
+      for (int v = t; v < nq * Hu; v += kWT) {
+        const int j = v / Hu, un = v - j * Hu;
+        const int b = gr.route()[q0 + j] / k;
+        xs[v] = reinterpret_cast<const uint4*>(x16 + (size_t)b * H)[un];
+      }
+#pragma unroll
+      for (int s = 0; s < kNS - 1; ++s) {
+        if (s < nst) issue(s);
+        cp_commit();
+      }
+      float ga[kNR] = {0.f, 0.f, 0.f, 0.f}, ua[kNR] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < nst; ++s) {
+        cp_wait_stages();
+        __syncthreads();  // stage s (and, at s = 0, x) visible; stage s - 1 no longer read
+        if (s + kNS - 1 < nst) issue(s + kNS - 1);
+        cp_commit();
+        const uint8_t* b = stg + (s % kNS) * kStage;
+        const uint32_t sgw = *reinterpret_cast<const uint32_t*>(b + 2 * kStC + t * 4);
+        const uint32_t suw = *reinterpret_cast<const uint32_t*>(b + 2 * kStC + kStS + t * 4);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {  // the stage's two block pairs
+          const uint4 gw = *reinterpret_cast<const uint4*>(b + half_at(t, c));
+          const uint4 uw = *reinterpret_cast<const uint4*>(b + kStC + half_at(t, c));
+          const float2 sg = e4m3x2(c ? sgw >> 16 : sgw & 0xffffu);
+          const float2 su = e4m3x2(c ? suw >> 16 : suw & 0xffffu);
+          const int blk = 4 * s + 2 * c;
+          const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w}, uv[4] = {uw.x, uw.y, uw.z, uw.w};
+          uint32_t gd[16], ud[16];
+#pragma unroll
+          for (int wd = 0; wd < 4; ++wd) {
+            gd[4 * wd] = e2m1x2<0>(gv[wd]);
+            gd[4 * wd + 1] = e2m1x2<1>(gv[wd]);
+            gd[4 * wd + 2] = e2m1x2<2>(gv[wd]);
+            gd[4 * wd + 3] = e2m1x2<3>(gv[wd]);
+            ud[4 * wd] = e2m1x2<0>(uv[wd]);
+            ud[4 * wd + 1] = e2m1x2<1>(uv[wd]);
+            ud[4 * wd + 2] = e2m1x2<2>(uv[wd]);
+            ud[4 * wd + 3] = e2m1x2<3>(uv[wd]);
+          }
+#pragma unroll
+          for (int j = 0; j < kNR; ++j) {
+            if (j >= nq) break;
+            const uint4* xr = xs + (size_t)j * Hu + blk * 2;  // 32 elements = 4 units
+            const uint4 x0 = xr[0], x1 = xr[1], x2 = xr[2], x3 = xr[3];
+            const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                     x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+            float p = 0.f, q = 0.f, p2 = 0.f, q2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              p = fma2h(gd[e], xv[e], p);
+              q = fma2h(ud[e], xv[e], q);
+              p2 = fma2h(gd[8 + e], xv[8 + e], p2);
+              q2 = fma2h(ud[8 + e], xv[8 + e], q2);
+            }
+            ga[j] = fmaf(p, sg.x, fmaf(p2, sg.y, ga[j]));
+            ua[j] = fmaf(q, su.x, fmaf(q2, su.y, ua[j]));
+          }
+        }
+      }
+      if (i < I) {
+#pragma unroll
+        for (int j = 0; j < kNR; ++j) {
+          if (j >= nq) break;
+          const int r = gr.route()[q0 + j];
+          const float xi = xinv[r / k];
+          const float gg = ga[j] * xi * gs0, uu = ua[j] * xi * gs1;
+          h[(size_t)r * I + i] = gg / (1.f + expf(-gg)) * uu;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ 4. down
 // Work item (group g, 256 rows of H): every lane owns one output row n and
 // computes its whole dot product with the h of up to kNR of the group's
@@ -452,6 +605,100 @@ __global__ void __launch_bounds__(kWT) gdown_kernel(DevState st, int H, int I, i
   }
 }
 
+// ------------------------------------------------------------ 4b. down, staged
+// The NVFP4 down kernel for I a multiple of 64: gdown_kernel's arithmetic
+// over rows streamed through shared memory as in gup_staged_kernel.
+__global__ void __launch_bounds__(kWT, 2) gdown_staged_kernel(DevState st, int H, int I,
+                                                              int layer, Groups gr,
+                                                              const float* __restrict__ h,
+                                                              float* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t dsm[];
+  float* hsm = reinterpret_cast<float*>(dsm);  // [kNR][I]
+  uint8_t* stg = dsm + (size_t)kNR * I * 4;    // [kNS][codes | scales]
+  constexpr int kStage = kStC + kStS;
+  const int G = gr.G();
+  const int nch = (H + kRowsItem - 1) / kRowsItem;
+  const int nst = I / 64;
+  const Off o(H, I);
+  const size_t pbase = (size_t)pool_of(st, layer) * st.S;
+  const int t = threadIdx.x;
+  for (int item = blockIdx.x; item < G * nch; item += gridDim.x) {
+    const int g = item / nch, ch = item - g * nch;
+    const int ra = gr.start()[g], rb = gr.start()[g + 1];
+    const uint8_t* blob = st.slots + (pbase + gr.slot()[g]) * st.stride;
+    const float gs2 = reinterpret_cast<const float*>(blob + o.glob)[2];
+    const int n0 = ch * kRowsItem, n = n0 + t;
+    auto issue = [&](int s) {
+      uint8_t* b = stg + (s % kNS) * kStage;
+      stage_rows(b, b + kStC, blob + o.code[2], blob + o.scale[2], n0, H, I / 2, I / 16, s);
+    };
+    for (int q0 = ra; q0 < rb; q0 += kNR) {
+      const int nq = min(kNR, rb - q0);
+      __syncthreads();
+      for (int v = t; v < nq * I / 4; v += kWT) {
+        const int j = v / (I / 4), f = v - j * (I / 4);
+        reinterpret_cast<float4*>(hsm)[v] =
+            __ldcg(reinterpret_cast<const float4*>(h + (size_t)gr.route()[q0 + j] * I) + f);
+      }
+#pragma unroll
+      for (int s = 0; s < kNS - 1; ++s) {
+        if (s < nst) issue(s);
+        cp_commit();
+      }
+      float acc[kNR] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < nst; ++s) {
+        cp_wait_stages();
+        __syncthreads();
+        if (s + kNS - 1 < nst) issue(s + kNS - 1);
+        cp_commit();
+        const uint8_t* b = stg + (s % kNS) * kStage;
+        const uint32_t scw = *reinterpret_cast<const uint32_t*>(b + kStC + t * 4);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(b + half_at(t, c));
+          const float2 sc = e4m3x2(c ? scw >> 16 : scw & 0xffffu);
+          const int blk = 4 * s + 2 * c;
+          const uint32_t ww[4] = {cw.x, cw.y, cw.z, cw.w};
+          float wf[32];
+#pragma unroll
+          for (int wd = 0; wd < 4; ++wd) {
+            const float2 a0 = f16x2_f32(e2m1x2<0>(ww[wd])), a1 = f16x2_f32(e2m1x2<1>(ww[wd]));
+            const float2 a2 = f16x2_f32(e2m1x2<2>(ww[wd])), a3 = f16x2_f32(e2m1x2<3>(ww[wd]));
+            wf[8 * wd] = a0.x, wf[8 * wd + 1] = a0.y, wf[8 * wd + 2] = a1.x, wf[8 * wd + 3] = a1.y;
+            wf[8 * wd + 4] = a2.x, wf[8 * wd + 5] = a2.y, wf[8 * wd + 6] = a3.x, wf[8 * wd + 7] = a3.y;
+          }
+#pragma unroll
+          for (int j = 0; j < kNR; ++j) {
+            if (j >= nq) break;
+            const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)j * I + blk * 16);
+            float p = 0.f, p2 = 0.f;
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const float4 hv = hp[e4], hv2 = hp[4 + e4];
+              p = fmaf(wf[4 * e4], hv.x, p);
+              p = fmaf(wf[4 * e4 + 1], hv.y, p);
+              p = fmaf(wf[4 * e4 + 2], hv.z, p);
+              p = fmaf(wf[4 * e4 + 3], hv.w, p);
+              p2 = fmaf(wf[16 + 4 * e4], hv2.x, p2);
+              p2 = fmaf(wf[16 + 4 * e4 + 1], hv2.y, p2);
+              p2 = fmaf(wf[16 + 4 * e4 + 2], hv2.z, p2);
+              p2 = fmaf(wf[16 + 4 * e4 + 3], hv2.w, p2);
+            }
+            acc[j] = fmaf(p, sc.x, fmaf(p2, sc.y, acc[j]));
+          }
+        }
+      }
+      if (n < H) {
+#pragma unroll
+        for (int j = 0; j < kNR; ++j) {
+          if (j >= nq) break;
+          y[(size_t)gr.route()[q0 + j] * H + n] = acc[j] * gs2;
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ 5. combine
 __global__ void __launch_bounds__(kWT) gcombine_kernel(const DevState st, int H, int k,
                                                        const int32_t* __restrict__ slot_ids,
@@ -474,6 +721,15 @@ __global__ void __launch_bounds__(kWT) gcombine_kernel(const DevState st, int H,
 
 int g_sms = 0;
 int g_occ[2][2] = {{1, 1}, {1, 1}};  // resident CTAs per SM: [format][gate-up, down]
+int g_occ_staged[2] = {1, 1};        // ... of the staged NVFP4 kernels
+
+size_t gup_staged_smem(int H) { return (size_t)kNR * H * 2 + (size_t)kNS * (2 * kStC + 2 * kStS); }
+size_t gdown_staged_smem(int I) { return (size_t)kNR * I * 4 + (size_t)kNS * (kStC + kStS); }
+// the staged NVFP4 kernels take whole 64-element stages of every row
+bool staged_ok(int H, int I) {
+  return H % 64 == 0 && I % 64 == 0 && gup_staged_smem(H) <= 200 * 1024 &&
+         gdown_staged_smem(I) <= 200 * 1024;
+}
 
 }  // namespace
 
@@ -508,6 +764,12 @@ cudaError_t grouped_init(int E, int H, int I) {
   occ(gup_kernel<MOE_W_NVFP4>, (size_t)kNR * H * 2, &g_occ[MOE_W_NVFP4][0]);
   occ(gdown_kernel<MOE_W_BF16>, (size_t)kNR * I * 4, &g_occ[MOE_W_BF16][1]);
   occ(gdown_kernel<MOE_W_NVFP4>, (size_t)kNR * I * 4, &g_occ[MOE_W_NVFP4][1]);
+  if (staged_ok(H, I)) {
+    lim(gup_staged_kernel, gup_staged_smem(H));
+    lim(gdown_staged_kernel, gdown_staged_smem(I));
+    occ(gup_staged_kernel, gup_staged_smem(H), &g_occ_staged[0]);
+    occ(gdown_staged_kernel, gdown_staged_smem(I), &g_occ_staged[1]);
+  }
   return e;
 }
 
@@ -522,7 +784,13 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
   const int sms = g_sms > 0 ? g_sms : 1;
   const int fi = wfmt == MOE_W_NVFP4 ? MOE_W_NVFP4 : MOE_W_BF16;
   const int grid_u = sms * g_occ[fi][0], grid_d = sms * g_occ[fi][1];
-  if (wfmt == MOE_W_NVFP4) {
+  if (wfmt == MOE_W_NVFP4 && staged_ok(H, I)) {
+    xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
+    gup_staged_kernel<<<sms * g_occ_staged[0], kWT, gup_staged_smem(H), s>>>(
+        st, H, I, layer, sc.x16, sc.xinv, k, gr, sc.h);
+    gdown_staged_kernel<<<sms * g_occ_staged[1], kWT, gdown_staged_smem(I), s>>>(
+        st, H, I, layer, gr, sc.h, sc.y);
+  } else if (wfmt == MOE_W_NVFP4) {
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
     gup_kernel<MOE_W_NVFP4><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,
                                                                      sc.xinv, k, gr, sc.h);
