@@ -43,14 +43,6 @@ inline float bf16f(uint16_t v) {
   std::memcpy(&f, &u, 4);
   return f;
 }
-// fp32 -> bf16 bits, round to nearest even (finite inputs)
-inline uint16_t f_bf16(float f) {
-  uint32_t u;
-  std::memcpy(&u, &f, 4);
-  if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return (uint16_t)(u >> 16);
-}
 
 // FP4 E2M1 (1 sign, 2 exponent, 1 mantissa bit, bias 1, no inf / NaN): the
 // sixteen codes as fp32, built from the bit fields.

@@ -94,6 +94,12 @@ def test_host_side_validation(m):
         with pytest.raises(m.MoeError) as ei:
             m.moe_cache_create(desc())
         assert ei.value.code == m.MOE_ERR_CUDA
+    # the hybrid executor's entry points check their arguments on the host
+    for call in (lambda: m.moe_hybrid_start(0, 4), lambda: m.moe_hybrid_stop(0),
+                 lambda: m.moe_hybrid_counters(0)):
+        with pytest.raises(m.MoeError) as ei:
+            call()
+        assert ei.value.code == m.MOE_ERR_INVALID_ARG
 
 
 def test_blob_bytes_agree_with_header_layout(m):
