@@ -53,6 +53,19 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ffn_fused_kernel_routed_traffic.t
 FFN_SOURCE = os.path.join(ROOT, "expert_slot_cache_lru_gb300", "csrc", "ffn_stream.cu")
 
 
+def replica_rate(local_s: float, units: int, ws: int, device="cpu") -> tuple[float, float]:
+    """Whole-job rate of ws independent replicas: every rank processed `units`
+    in `local_s` seconds; the job took the slowest rank's time (max over
+    ranks), so the rate is ws * units / max_s.  Returns (rate, max_s)."""
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([local_s], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local_s = float(t.item())
+    return ws * units / local_s, local_s
+
+
 def source_hash(path: str) -> str:
     import hashlib
     with open(path, "rb") as f:
@@ -685,12 +698,8 @@ def run_native(args) -> None:
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    tok_s = ws * args.steps / (ms * 1e-3)
+    tok_s, max_s = replica_rate(e0.elapsed_time(e1) * 1e-3, args.steps, ws, "cuda")
+    ms = max_s * 1e3
     if args.routed_only:  # profiler runs: the routed FFN kernel's roofline graph only
         if rank == 0:
             roof = dec.routed_gemv_roofline(steps=2)
@@ -710,12 +719,8 @@ def run_native(args) -> None:
     t0 = time.perf_counter()
     for _ in range(args.steps):
         dec.step_e2e()
-    e2e_s = time.perf_counter() - t0
-    if ws > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": ws * args.steps / e2e_s, "unit": "tok/s",
+    e2e_rate, _ = replica_rate(time.perf_counter() - t0, args.steps, ws, "cuda")
+    e2e = {"value": e2e_rate, "unit": "tok/s",
            "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
 
     roof = dec.routed_gemv_roofline(steps=8)
