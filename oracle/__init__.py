@@ -30,6 +30,7 @@ STATUS_INVALID_ID = 1
 STATUS_CAPACITY = 2
 FMT_BF16 = 0
 FMT_NVFP4 = 1
+FMT_MXFP4 = 2
 
 
 def build(force: bool = False) -> str:
@@ -71,6 +72,8 @@ def lib():
         L.om_e2m1.argtypes = [C.c_int]
         L.om_e4m3.restype = C.c_double
         L.om_e4m3.argtypes = [C.c_int]
+        L.om_e8m0.restype = C.c_double
+        L.om_e8m0.argtypes = [C.c_int]
         L.om_bf16.restype = C.c_double
         L.om_bf16.argtypes = [C.c_uint16]
         L.om_blob_bytes.restype = C.c_uint64
@@ -202,6 +205,10 @@ def e2m1(code: int) -> float:
 
 def e4m3(byte: int) -> float:
     return lib().om_e4m3(byte)
+
+
+def e8m0(byte: int) -> float:
+    return lib().om_e8m0(byte)
 
 
 def bf16(bits: int) -> float:

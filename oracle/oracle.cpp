@@ -480,6 +480,13 @@ double om_e4m3(int byte) {
   return s ? -mag : mag;
 }
 
+// E8M0 (OCP Microscaling Formats spec, the shared block scale): 8 exponent
+// bits, bias 127, no sign and no mantissa: 2^(e - 127); 0xFF is NaN.
+double om_e8m0(int byte) {
+  const int e = byte & 255;
+  return e == 255 ? NAN : std::ldexp(1.0, e - 127);
+}
+
 // bfloat16: the upper 16 bits of an IEEE binary32.
 double om_bf16(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -497,9 +504,25 @@ namespace {
 // up, down e4m3 block scales (one per 16 consecutive elements of a row), then
 // three fp32 per-matrix global scales padded to 16 bytes.  Gate and up are
 // [I, H], down is [H, I].  bf16: gate, up, down, row-major.
+// MXFP4 (OCP Microscaling: MXFP4 blocks of 32 e2m1 elements sharing one
+// E8M0 scale): the same three code banks, then the gate, up, down E8M0 scales
+// (one per 32 consecutive elements of a row); no global scale.
 struct Layout {
   uint64_t code[3], scale[3], glob, total;
 };
+Layout mxfp4_layout(int H, int I) {
+  Layout L{};
+  const uint64_t ih = (uint64_t)I * H;
+  L.code[0] = 0;
+  L.code[1] = ih / 2;
+  L.code[2] = ih;
+  L.scale[0] = 3 * ih / 2;
+  L.scale[1] = L.scale[0] + ih / 32;
+  L.scale[2] = L.scale[1] + ih / 32;
+  L.glob = L.scale[2] + ih / 32;  // no global scales: the blob ends here
+  L.total = (L.glob + 15) / 16 * 16;
+  return L;
+}
 Layout nvfp4_layout(int H, int I) {
   Layout L{};
   const uint64_t ih = (uint64_t)I * H;
@@ -519,6 +542,7 @@ Layout nvfp4_layout(int H, int I) {
 uint64_t om_blob_bytes(int fmt, int H, int I) {
   if (fmt == OFMT_BF16) return 6ull * H * I;
   if (fmt == OFMT_NVFP4) return nvfp4_layout(H, I).total;
+  if (fmt == OFMT_MXFP4) return mxfp4_layout(H, I).total;
   return 0;
 }
 
@@ -532,6 +556,20 @@ int om_dequant(int fmt, const uint8_t* blob, int H, int I, int which, double* ou
       uint16_t b;
       std::memcpy(&b, w + i, 2);
       out[i] = om_bf16(b);
+    }
+    return 0;
+  }
+  if (fmt == OFMT_MXFP4) {  // element = e2m1(code) * 2^(scale - 127)
+    const Layout L = mxfp4_layout(H, I);
+    const uint8_t* codes = blob + L.code[which];
+    const uint8_t* scales = blob + L.scale[which];
+    for (int n = 0; n < rows; ++n) {
+      for (int k = 0; k < cols; ++k) {
+        const uint64_t idx = (uint64_t)n * cols + k;
+        const uint8_t byte = codes[idx / 2];
+        const int nib = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+        out[idx] = om_e2m1(nib) * om_e8m0(scales[(uint64_t)n * (cols / 32) + k / 32]);
+      }
     }
     return 0;
   }

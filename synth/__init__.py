@@ -36,6 +36,7 @@ import numpy as np
 
 FMT_BF16 = 0
 FMT_NVFP4 = 1
+FMT_MXFP4 = 2
 
 # stream ids of the seed sequence
 S_WEIGHTS, S_PERM, S_ROUTING, S_HIDDEN, S_PRED, S_RWEIGHTS, S_SHARED, S_PREFILL, S_ALIAS = range(1, 10)
@@ -176,9 +177,23 @@ def nvfp4_banks(hidden: int, inter: int) -> dict:
     return o
 
 
+def mxfp4_banks(hidden: int, inter: int) -> dict:
+    """Byte offsets of an MXFP4 blob: the same code banks as NVFP4, then
+    gate/up scales [I, H/32] and down scales [H, I/32] (E8M0, one per 32
+    consecutive elements of a row); no global scales; padded to 16 bytes."""
+    ih = inter * hidden
+    o = {"code": [0, ih // 2, ih], "scale": [3 * ih // 2, 3 * ih // 2 + ih // 32,
+                                             3 * ih // 2 + 2 * (ih // 32)]}
+    o["end"] = 3 * ih // 2 + 3 * (ih // 32)
+    o["total"] = (o["end"] + 15) // 16 * 16
+    return o
+
+
 def blob_bytes(fmt: int, hidden: int, inter: int) -> int:
     if fmt == FMT_BF16:
         return 6 * hidden * inter
+    if fmt == FMT_MXFP4:
+        return mxfp4_banks(hidden, inter)["total"]
     return nvfp4_banks(hidden, inter)["total"]
 
 
@@ -187,6 +202,13 @@ def fill_blob(out: np.ndarray, fmt: int, hidden: int, inter: int, rng: Rng) -> N
     if fmt == FMT_BF16:
         w = rng.normal(3 * hidden * inter) * 0.02
         out[:] = to_bf16_bits(w).view(np.uint8)
+        return
+    if fmt == FMT_MXFP4:  # random codes; block scales 2^-9 .. 2^-6 (E8M0 118..121)
+        o = mxfp4_banks(hidden, inter)
+        n_codes = o["scale"][0]
+        out[:n_codes] = rng.bytes(n_codes)
+        out[n_codes:o["end"]] = np.uint8(118) + (rng.bytes(o["end"] - n_codes) & np.uint8(3))
+        out[o["end"]:o["total"]] = 0
         return
     o = nvfp4_banks(hidden, inter)
     n_codes = o["scale"][0]

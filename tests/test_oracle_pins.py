@@ -294,6 +294,22 @@ def test_e4m3_exhaustive_against_torch():
     assert oracle.e4m3(0x7E) == 448.0 and oracle.e4m3(0x01) == 2.0 ** -9 and oracle.e4m3(0x38) == 1.0
 
 
+def test_e8m0_exhaustive_against_torch():
+    """E8M0, the MXFP4 block scale (OCP Microscaling Formats): every code
+    against torch's float8_e8m0fnu, plus the spec's anchors."""
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("this torch has no float8_e8m0fnu")
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64)
+    for b in range(256):
+        got, want = oracle.e8m0(b), float(ref[b])
+        if math.isnan(want):
+            assert math.isnan(got), b
+        else:
+            assert got == want, b
+    assert oracle.e8m0(127) == 1.0 and oracle.e8m0(0) == 2.0 ** -127
+    assert oracle.e8m0(254) == 2.0 ** 127 and math.isnan(oracle.e8m0(255))
+
+
 def test_bf16_against_torch():
     bits = np.arange(0, 65536, 37, dtype=np.uint16)
     ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
@@ -319,6 +335,37 @@ def _np_dequant_nvfp4(blob: np.ndarray, H: int, I: int, which: int) -> np.ndarra
     return w * g
 
 
+def _np_dequant_mxfp4(blob: np.ndarray, H: int, I: int, which: int) -> np.ndarray:
+    """Independent numpy decode of one MXFP4 matrix: e2m1 codes from the OCP
+    table fixture, one power-of-two scale per 32 row elements."""
+    table = np.array(gold("e2m1_ocp.json")["values"])
+    banks = synth.mxfp4_banks(H, I)
+    rows, cols = (H, I) if which == 2 else (I, H)
+    codes = blob[banks["code"][which]:banks["code"][which] + rows * cols // 2]
+    nib = np.empty(rows * cols, np.int64)
+    nib[0::2] = codes & 15
+    nib[1::2] = codes >> 4
+    sc = blob[banks["scale"][which]:banks["scale"][which] + rows * cols // 32].astype(np.int64)
+    scale = np.ldexp(1.0, sc - 127)
+    return table[nib].reshape(rows, cols) * np.repeat(scale.reshape(rows, cols // 32), 32, axis=1)
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_mxfp4_dequant_against_numpy(which):
+    H, I = 64, 96
+    blob = np.empty(synth.blob_bytes(synth.FMT_MXFP4, H, I), np.uint8)
+    synth.fill_blob(blob, synth.FMT_MXFP4, H, I, synth.Rng(6, which))
+    assert oracle.blob_bytes(oracle.FMT_MXFP4, H, I) == len(blob) == 3 * H * I // 2 + 3 * H * I // 32
+    got = oracle.dequant(oracle.FMT_MXFP4, blob, H, I, which)
+    assert np.array_equal(got, _np_dequant_mxfp4(blob, H, I, which))
+    # a planted change of one scale moves exactly its 32 elements by a power of two
+    banks = synth.mxfp4_banks(H, I)
+    b2 = blob.copy()
+    b2[banks["scale"][which]] += 1
+    d = oracle.dequant(oracle.FMT_MXFP4, b2, H, I, which)
+    assert np.array_equal(d[0, :32], 2 * got[0, :32]) and np.array_equal(d[0, 32:], got[0, 32:])
+
+
 @pytest.mark.parametrize("which", [0, 1, 2])
 def test_nvfp4_dequant_against_numpy(which):
     H, I = 64, 96
@@ -335,7 +382,7 @@ def _np_ffn(Wg, Wu, Wd, x):
     return Wd @ (g / (1 + np.exp(-g)) * u)
 
 
-@pytest.mark.parametrize("fmt", [oracle.FMT_BF16, oracle.FMT_NVFP4])
+@pytest.mark.parametrize("fmt", [oracle.FMT_BF16, oracle.FMT_NVFP4, oracle.FMT_MXFP4])
 def test_expert_ffn_against_numpy(fmt):
     H, I = 64, 128
     blob = np.empty(synth.blob_bytes(fmt, H, I), np.uint8)
