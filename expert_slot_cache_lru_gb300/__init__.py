@@ -34,6 +34,7 @@ MOE_ERR_SCRATCH = -8
 MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 MOE_W_BF16 = 0
 MOE_W_NVFP4 = 1
+MOE_W_MXFP4 = 2
 MOE_POOL_SHARED = 0
 MOE_POOL_PER_LAYER = 1
 MOE_PLAN_DEMAND = 0
@@ -271,6 +272,8 @@ def blob_bytes(wfmt: int, hidden: int, inter: int) -> int:
     """Bytes of one expert blob in the layout of moe_cache.h."""
     if wfmt == MOE_W_BF16:
         return 6 * hidden * inter
+    if wfmt == MOE_W_MXFP4:
+        return 3 * hidden * inter // 2 + 3 * hidden * inter // 32
     return 3 * hidden * inter // 2 + 3 * hidden * inter // 16 + 16
 
 

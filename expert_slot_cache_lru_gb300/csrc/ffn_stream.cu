@@ -169,6 +169,12 @@ __device__ __forceinline__ float2 e4m3x2_f32(uint32_t v16) {
       : "r"(v16));
   return h2_f32(h2);
 }
+// an E8M0 block scale (MXFP4): 2^(e - 127), from its exponent bits; 0 is the
+// subnormal 2^-127, 255 is NaN
+__device__ __forceinline__ float e8m0_f32(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u) : (e == 255 ? __uint_as_float(0x7fffffffu)
+                                                            : __uint_as_float(e << 23));
+}
 // c + w.lo * x.lo + w.hi * x.hi, half operands, fp32 result (exact products)
 __device__ __forceinline__ float fma2_h(uint32_t w2, uint32_t x2, float c) {
   float d;
@@ -231,17 +237,18 @@ __device__ __forceinline__ float wsum(float v) {
 
 // Offsets inside a blob (layout of moe_cache.h).
 struct BlobOff {
-  size_t code[3], scale[3], glob;  // NVFP4
+  size_t code[3], scale[3], glob;  // NVFP4 and MXFP4 (MXFP4: no global scales)
   size_t mat[3];                   // bf16
-  __device__ BlobOff(int H, int I) {
+  __device__ BlobOff(int H, int I, int fmt) {
     const size_t ih = (size_t)I * H;
+    const size_t sb = ih / (fmt == MOE_W_MXFP4 ? 32 : 16);  // scale bytes per matrix
     code[0] = 0;
     code[1] = ih / 2;
     code[2] = ih;
     scale[0] = 3 * ih / 2;
-    scale[1] = scale[0] + ih / 16;
-    scale[2] = scale[1] + ih / 16;
-    glob = scale[2] + ih / 16;
+    scale[1] = scale[0] + sb;
+    scale[2] = scale[1] + sb;
+    glob = scale[2] + sb;
     mat[0] = 0;
     mat[1] = ih * 2;
     mat[2] = ih * 4;
@@ -384,6 +391,48 @@ struct ItemA<MOE_W_BF16> {
     return make_float2(1.f, 1.f);
   }
 };
+// MXFP4: chunks of 2048 elements as NVFP4; one E8M0 scale per 32 elements, so
+// each lane's 32-element block has one scale and no global scale applies:
+//   gate codes [1024 B] | up codes [1024 B] | gate scales [64 B] | up scales [64 B].
+template <>
+struct ItemA<MOE_W_MXFP4> {
+  static constexpr int CW = 2048;
+  static constexpr int BYTES = 2 * 1024 + 2 * 64;
+  static __device__ __forceinline__ uint32_t issue(uint8_t* slot, const uint8_t* blob,
+                                                   const BlobOff& o, int H, int i, int c,
+                                                   uint64_t* bar, uint64_t pol) {
+    const size_t cr = (size_t)i * (H / 2) + c * 1024, sr = (size_t)i * (H / 32) + c * 64;
+    bulk_g2s(slot, blob + o.code[0] + cr, 1024, bar, pol);
+    bulk_g2s(slot + 1024, blob + o.code[1] + cr, 1024, bar, pol);
+    bulk_g2s(slot + 2048, blob + o.scale[0] + sr, 64, bar, pol);
+    bulk_g2s(slot + 2112, blob + o.scale[1] + sr, 64, bar, pol);
+    return BYTES;
+  }
+  static __device__ __forceinline__ float2 glob(const uint8_t*, const BlobOff&) {
+    return make_float2(1.f, 1.f);
+  }
+  static __device__ __forceinline__ void dot(const uint8_t* slot, const uint4* xr, int c, int lane,
+                                             float& g, float& u) {
+    const uint4 g0 = *reinterpret_cast<const uint4*>(slot + lane * 16);
+    const uint4 g1 = *reinterpret_cast<const uint4*>(slot + 512 + lane * 16);
+    const uint4 u0 = *reinterpret_cast<const uint4*>(slot + 1024 + lane * 16);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(slot + 1536 + lane * 16);
+    const float sg0 = e8m0_f32(slot[2048 + lane]), sg1 = e8m0_f32(slot[2048 + 32 + lane]);
+    const float su0 = e8m0_f32(slot[2112 + lane]), su1 = e8m0_f32(slot[2112 + 32 + lane]);
+    const int ua = c * 256 + lane * 4, ub = ua + 128;
+    uint4 x0 = xr[xswz(ua)], x1 = xr[xswz(ua + 1)], x2 = xr[xswz(ua + 2)], x3 = xr[xswz(ua + 3)];
+    g = fmaf((dot8_fp4_h(g0.x, x0) + dot8_fp4_h(g0.y, x1)) +
+             (dot8_fp4_h(g0.z, x2) + dot8_fp4_h(g0.w, x3)), sg0, g);
+    u = fmaf((dot8_fp4_h(u0.x, x0) + dot8_fp4_h(u0.y, x1)) +
+             (dot8_fp4_h(u0.z, x2) + dot8_fp4_h(u0.w, x3)), su0, u);
+    x0 = xr[xswz(ub)], x1 = xr[xswz(ub + 1)], x2 = xr[xswz(ub + 2)], x3 = xr[xswz(ub + 3)];
+    g = fmaf((dot8_fp4_h(g1.x, x0) + dot8_fp4_h(g1.y, x1)) +
+             (dot8_fp4_h(g1.z, x2) + dot8_fp4_h(g1.w, x3)), sg1, g);
+    u = fmaf((dot8_fp4_h(u1.x, x0) + dot8_fp4_h(u1.y, x1)) +
+             (dot8_fp4_h(u1.z, x2) + dot8_fp4_h(u1.w, x3)), su1, u);
+  }
+};
+
 constexpr int kSlotBytes = 2432;  // >= ItemA<*>::BYTES, a multiple of 128
 
 // ------------------------------------------------------------ phase B items
@@ -410,6 +459,15 @@ __device__ __forceinline__ void itemb_load(ItemB<FMT>& it, const uint8_t* codes,
       it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
       it.w[1].x = *reinterpret_cast<const uint16_t*>(scales + lane * 2);
     }
+  } else if (FMT == MOE_W_MXFP4) {  // the lane's 16 (m = 1) or 32 elements: one 32-block scale
+    if (m == 1) {
+      const uint2 cw = *reinterpret_cast<const uint2*>(codes + lane * 8);
+      it.w[0] = make_uint4(cw.x, cw.y, 0u, 0u);
+      it.w[1].x = scales[lane >> 1];
+    } else {
+      it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
+      it.w[1].x = scales[lane];
+    }
   } else {
     it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
     it.w[1] = *reinterpret_cast<const uint4*>(codes + 512 + lane * 16);
@@ -426,6 +484,10 @@ __device__ __forceinline__ float itemb_dot(const ItemB<FMT>& it, const float* hv
     float p = (dot8_fp4_f(it.w[0].x, hv) + dot8_fp4_f(it.w[0].y, hv + 8)) * sc.x;
     if (m == 2) p = fmaf(dot8_fp4_f(it.w[0].z, hv + 16) + dot8_fp4_f(it.w[0].w, hv + 24), sc.y, p);
     return p;
+  } else if (FMT == MOE_W_MXFP4) {
+    float p = dot8_fp4_f(it.w[0].x, hv) + dot8_fp4_f(it.w[0].y, hv + 8);
+    if (m == 2) p += dot8_fp4_f(it.w[0].z, hv + 16) + dot8_fp4_f(it.w[0].w, hv + 24);
+    return p * e8m0_f32(it.w[1].x & 0xffu);
   } else {
     float p = dot8_bf16_f(it.w[0], hv, 0.f);
     p = dot8_bf16_f(it.w[1], hv + 8, p);
@@ -568,6 +630,7 @@ template <int FMT, int MODE>
 __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) {
   constexpr bool SHARED = MODE == kShared, ADMIT = MODE == kLayerAdmit;
   constexpr bool LAYER = MODE == kLayer || ADMIT;
+  constexpr bool FP4 = FMT != MOE_W_BF16;  // NVFP4 or MXFP4 experts: e2m1 codes, f16 x
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ unsigned long long s_j;  // admission inside: this launch's index
   if (ADMIT) {  // every CTA of launch j adds one to a.epoch: j = old / gridDim.x
@@ -594,11 +657,11 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.H, I = a.I, k = a.k, n_rows = a.n_rows;
   const int m = I / 512;                                   // 16-element groups per lane (B)
-  const int CB = FMT == MOE_W_NVFP4 ? I / 2 : I * 2;       // down row: code bytes
-  const int SB = FMT == MOE_W_NVFP4 ? I / 16 : 0;          // down row: scale bytes
+  const int CB = FP4 ? I / 2 : I * 2;                      // down row: code bytes
+  const int SB = FMT == MOE_W_NVFP4 ? I / 16 : (FP4 ? I / 32 : 0);  // down row: scale bytes
   constexpr int CW = ItemA<FMT>::CW;
   const int KC = H / CW;                                   // phase-A chunks per row
-  const BlobOff o(H, I);
+  const BlobOff o(H, I, FMT);
 
   // this CTA's output rows (phase B): at most two batch rows (perB <= H)
   const int UB = n_rows * H;
@@ -715,7 +778,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     if (lane == 0) tk.n = __popc(m0) + __popc(m1) + spr * n_rows;
     if (lane <= n_rows) ts[lane] = below(lane * k) + spr * lane;  // first task of row `lane`
   }
-  if (FMT == MOE_W_NVFP4) {  // rows whose |x| reaches 2^14 get a scale below 1
+  if (FP4) {  // rows whose |x| reaches 2^14 get a scale below 1
 #pragma unroll
     for (int j = 0; j < kXW; ++j) {
       const int i = threadIdx.x + j * kT;
@@ -802,7 +865,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     if (i >= nx8) continue;
     const int b = (i * 8) / H, u = i - b * (H / 8);
     uint4 v = xw[j];
-    if (FMT == MOE_W_NVFP4) {
+    if (FP4) {
       const float sc = x_scale(__uint_as_float(xmax[b]));
       const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
       uint32_t hv[4];
@@ -817,7 +880,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
     reinterpret_cast<uint4*>(xs)[(size_t)b * (H / 8) + xswz(u)] = v;
   }
   if (threadIdx.x < n_rows) {
-    xinv[threadIdx.x] = FMT == MOE_W_NVFP4 ? 1.f / x_scale(__uint_as_float(xmax[threadIdx.x])) : 1.f;
+    xinv[threadIdx.x] = FP4 ? 1.f / x_scale(__uint_as_float(xmax[threadIdx.x])) : 1.f;
   }
   if (lane == 0) {
     mbar_init(&bar_a[warp][0], 1);
@@ -874,9 +937,9 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
       if (cnt <= 0 || (LAYER && tk.pe[t] != -1)) continue;  // copied in by this launch: read later
       const uint8_t* blob = tk.blob[t];
       bulk_g2s(stC + (size_t)q0 * CB,
-               blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB,
+               blob + (FP4 ? o.code[2] : o.mat[2]) + (size_t)nlo * CB,
                (uint32_t)cnt * CB, &bar_b, pol);
-      if (FMT == MOE_W_NVFP4)
+      if (FP4)
         bulk_g2s(stS + (size_t)q0 * SB, blob + o.scale[2] + (size_t)nlo * SB, (uint32_t)cnt * SB,
                  &bar_b, pol);
     }
@@ -1258,7 +1321,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   // run loop is instantiated for the lane's element count (M = I / 512), and a
   // run whose rows were all staged reads them with shared-memory loads.
   {
-    constexpr int NG = FMT == MOE_W_NVFP4 ? 4 : 2;
+    constexpr int NG = FP4 ? 4 : 2;
     const int ipw = (NQ + kW - 1) / kW;
     const int q0w = min(NQ, warp * ipw), q1w = min(NQ, q0w + ipw);
     auto run_b = [&](auto mtag) {
@@ -1275,7 +1338,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
         const int cnt = min(NG, min(q1w - q, nlen - r));  // items of this run: one task
         if (t != ht) {  // this task's h slice into registers
           const float* hp = hsm + (size_t)(t - tlo) * I;
-          if (FMT == MOE_W_NVFP4) {
+          if (FP4) {
 #pragma unroll
             for (int j = 0; j < 4 * M; ++j) {
               const float4 v = reinterpret_cast<const float4*>(hp + lane * 16 * M)[j];
@@ -1311,7 +1374,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
               itemb_load<FMT>(itm[j], stC + (size_t)qq * CB, stS + (size_t)qq * SB, M, lane);
             else
               itemb_load<FMT>(itm[j],
-                              blob + (FMT == MOE_W_NVFP4 ? o.code[2] : o.mat[2]) + (size_t)n * CB,
+                              blob + (FP4 ? o.code[2] : o.mat[2]) + (size_t)n * CB,
                               blob + o.scale[2] + (size_t)n * SB, M, lane);
           }
         }
@@ -1401,7 +1464,7 @@ struct Plan {
 Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T, int G) {
   Plan p{};
   const int perB = (n_rows * H + G - 1) / G;
-  const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : I * 2;
+  const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : (wfmt == MOE_W_MXFP4 ? I / 2 + I / 32 : I * 2);
   p.htasks = std::min(T, 2 * k);
   const size_t fixed = round128((size_t)n_rows * H * 2) + round128((size_t)T * perB * 4) +
                        round128((size_t)p.htasks * I * 4) + (size_t)kW * 2 * kSlotBytes;
@@ -1409,7 +1472,7 @@ Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T, int G) {
   const size_t room = fixed < kBudget ? kBudget - fixed : 0;
   p.qs = (int)std::min<size_t>((size_t)nq, room / rowB);
   p.smem = fixed + (size_t)p.qs * rowB;
-  const int CW = wfmt == MOE_W_NVFP4 ? 2048 : 512;
+  const int CW = wfmt == MOE_W_BF16 ? 512 : 2048;
   const int KC = H / CW;
   p.ok = fixed <= kBudget && H % CW == 0 && (KC == 1 || KC % 2 == 0) && I % 512 == 0 &&
          I <= 1024 && perB <= H &&
@@ -1450,6 +1513,23 @@ int tasks_per_row(int mode, int k, bool shared) {
   return (mode == kLayer || mode == kLayerAdmit) ? k + (shared ? 1 : 0) : k;
 }
 
+template <int FMT>
+cudaError_t launch_mode(int mode, size_t smem, cudaStream_t s, const DevState& st,
+                        const FusedArgs& a) {
+  switch (mode) {
+    case kLayerAdmit: return launch_coop(ffn_fused_kernel<FMT, kLayerAdmit>, smem, s, st, a);
+    case kLayer: return launch_coop(ffn_fused_kernel<FMT, kLayer>, smem, s, st, a);
+    case kShared: return launch_coop(ffn_fused_kernel<FMT, kShared>, smem, s, st, a);
+    default: return launch_coop(ffn_fused_kernel<FMT, kRouted>, smem, s, st, a);
+  }
+}
+cudaError_t launch_format(int wfmt, int mode, size_t smem, cudaStream_t s, const DevState& st,
+                          const FusedArgs& a) {
+  if (wfmt == MOE_W_NVFP4) return launch_mode<MOE_W_NVFP4>(mode, smem, s, st, a);
+  if (wfmt == MOE_W_MXFP4) return launch_mode<MOE_W_MXFP4>(mode, smem, s, st, a);
+  return launch_mode<MOE_W_BF16>(mode, smem, s, st, a);
+}
+
 cudaError_t launch_fused(const DevState& st, int wfmt, int mode, const FusedArgs& a0,
                          cudaStream_t s) {
   FusedArgs a = a0;
@@ -1463,17 +1543,7 @@ cudaError_t launch_fused(const DevState& st, int wfmt, int mode, const FusedArgs
   size_t smem = p.smem;
   if (mode == kLayerAdmit) smem = std::max(smem, admit_cta_smem(st.E, st.S, a.adm_cached != 0));
   if (smem > kBudget) return cudaErrorInvalidValue;
-  if (mode == kLayerAdmit)
-    return wfmt == MOE_W_NVFP4 ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kLayerAdmit>, smem, s, st, a)
-                               : launch_coop(ffn_fused_kernel<MOE_W_BF16, kLayerAdmit>, smem, s, st, a);
-  if (wfmt == MOE_W_NVFP4) {
-    if (mode == kLayer) return launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kLayer>, p.smem, s, st, a);
-    return mode == kShared ? launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kShared>, p.smem, s, st, a)
-                           : launch_coop(ffn_fused_kernel<MOE_W_NVFP4, kRouted>, p.smem, s, st, a);
-  }
-  if (mode == kLayer) return launch_coop(ffn_fused_kernel<MOE_W_BF16, kLayer>, p.smem, s, st, a);
-  return mode == kShared ? launch_coop(ffn_fused_kernel<MOE_W_BF16, kShared>, p.smem, s, st, a)
-                         : launch_coop(ffn_fused_kernel<MOE_W_BF16, kRouted>, p.smem, s, st, a);
+  return launch_format(wfmt, mode, mode == kLayerAdmit ? smem : p.smem, s, st, a);
 }
 
 }  // namespace
@@ -1500,6 +1570,10 @@ cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int ma
   set(ffn_fused_kernel<MOE_W_NVFP4, kLayer>);
   set(ffn_fused_kernel<MOE_W_BF16, kLayerAdmit>);
   set(ffn_fused_kernel<MOE_W_NVFP4, kLayerAdmit>);
+  set(ffn_fused_kernel<MOE_W_MXFP4, kShared>);
+  set(ffn_fused_kernel<MOE_W_MXFP4, kRouted>);
+  set(ffn_fused_kernel<MOE_W_MXFP4, kLayer>);
+  set(ffn_fused_kernel<MOE_W_MXFP4, kLayerAdmit>);
   (void)wfmt, (void)H, (void)I, (void)Is, (void)max_rows, (void)max_tasks;
   return e;
 }

@@ -737,7 +737,7 @@ bool grouped_supported(int wfmt, int H, int I, int E) {
   const bool smem = (size_t)E * 16 <= 200 * 1024 && (size_t)kNR * H * 2 <= 200 * 1024 &&
                     (size_t)kNR * I * 4 <= 200 * 1024;
   if (wfmt == MOE_W_NVFP4) return smem && H % 32 == 0 && I % 32 == 0;
-  return smem && H % 8 == 0 && I % 8 == 0;
+  return wfmt == MOE_W_BF16 && smem && H % 8 == 0 && I % 8 == 0;
 }
 
 cudaError_t grouped_init(int E, int H, int I) {

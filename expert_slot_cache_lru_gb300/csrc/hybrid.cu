@@ -74,22 +74,30 @@ struct E4m3Table {
     }
   }
 };
+// E8M0 (the MXFP4 block scale: 8 exponent bits, bias 127; 255 is NaN).
+struct E8m0Table {
+  float v[256];
+  E8m0Table() {
+    for (int c = 0; c < 256; ++c) v[c] = c == 255 ? NAN : std::ldexp(1.f, c - 127);
+  }
+};
 const E2m1Table kE2m1;
 const E4m3Table kE4m3;
+const E8m0Table kE8m0;
 
 // ---------------------------------------------------------------- one expert
 // Byte offsets of the banks of an expert blob (the layout of moe_cache.h).
 struct Banks {
   size_t code[3], scale[3], glob;
-  Banks(int H, int I) {
-    const size_t hi = (size_t)H * I;
+  Banks(int H, int I, int fmt) {
+    const size_t hi = (size_t)H * I, sb = hi / (fmt == MOE_W_MXFP4 ? 32 : 16);
     code[0] = 0;
     code[1] = hi / 2;
     code[2] = hi;
     scale[0] = 3 * hi / 2;
-    scale[1] = scale[0] + hi / 16;
-    scale[2] = scale[1] + hi / 16;
-    glob = scale[2] + hi / 16;
+    scale[1] = scale[0] + sb;
+    scale[2] = scale[1] + sb;
+    glob = scale[2] + sb;
   }
 };
 
@@ -122,6 +130,23 @@ inline float dot_fp4(const uint8_t* codes, const uint8_t* scales, const float* x
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// The same for one MXFP4 row: per block of 32 elements the e2m1 products are
+// summed, then scaled by the block's power of two; blocks go to four sums.
+inline float dot_mx(const uint8_t* codes, const uint8_t* scales, const float* x, int n) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int blk = 0; blk < n / 32; ++blk) {
+    const uint8_t* c = codes + blk * 16;
+    const float* xb = x + blk * 32;
+    float s = 0.f;
+    for (int u = 0; u < 16; ++u) {
+      s += kE2m1.v[c[u] & 15] * xb[2 * u];
+      s += kE2m1.v[c[u] >> 4] * xb[2 * u + 1];
+    }
+    acc[blk & 3] += s * kE8m0.v[scales[blk]];
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // Row `r` of bank `which` (0 gate, 1 up: [I][H]; 2 down: [H][I]) dotted with x.
 inline float row_dot(int wfmt, const uint8_t* blob, const Banks& bk, int H, int I, int which,
                      int r, const float* x) {
@@ -130,6 +155,9 @@ inline float row_dot(int wfmt, const uint8_t* blob, const Banks& bk, int H, int 
     const uint16_t* m = reinterpret_cast<const uint16_t*>(blob) + (size_t)which * H * I;
     return dot_bf16(m + (size_t)r * n, x, n);
   }
+  if (wfmt == MOE_W_MXFP4)
+    return dot_mx(blob + bk.code[which] + (size_t)r * (n / 2),
+                  blob + bk.scale[which] + (size_t)r * (n / 32), x, n);
   float g;
   std::memcpy(&g, blob + bk.glob + 4 * which, 4);
   return dot_fp4(blob + bk.code[which] + (size_t)r * (n / 2),
@@ -192,7 +220,7 @@ struct Work {
   void task_a(int t) const {
     const int q = t / blkA, i0 = (t % blkA) * kRowsA, i1 = std::min(I, i0 + kRowsA);
     const Route& rt = routes[(size_t)q];
-    const Banks bk(H, I);
+    const Banks bk(H, I, wfmt);
     const float* xb = x + (size_t)rt.b * H;
     for (int i = i0; i < i1; ++i) {
       const float g = row_dot(wfmt, rt.blob, bk, H, I, 0, i, xb);
@@ -203,7 +231,7 @@ struct Work {
 
   void task_b(int t) const {
     const int b = t / blkB, n0 = (t % blkB) * kRowsB, n1 = std::min(H, n0 + kRowsB);
-    const Banks bk(H, I);
+    const Banks bk(H, I, wfmt);
     for (int n = n0; n < n1; ++n) {
       float acc = 0.f;
       for (int q = first[b]; q < first[(size_t)b + 1]; ++q)
@@ -522,7 +550,8 @@ extern "C" {
 int moe_cpu_experts(int wfmt, int hidden, int inter, const void* const* h_blobs, int n_experts,
                     const uint16_t* h_x, const int32_t* h_ids, const int32_t* h_slot_ids,
                     const float* h_w, int n_rows, int k, int n_threads, float* h_out) {
-  if ((wfmt != MOE_W_BF16 && wfmt != MOE_W_NVFP4) || hidden <= 0 || inter <= 0 || hidden % 32 ||
+  if ((wfmt != MOE_W_BF16 && wfmt != MOE_W_NVFP4 && wfmt != MOE_W_MXFP4) || hidden <= 0 ||
+      inter <= 0 || hidden % 32 ||
       inter % 32 || n_experts <= 0 || !h_blobs || n_rows < 0 || k < 0 || n_threads < 1 ||
       n_threads > 256)
     return MOE_ERR_INVALID_ARG;

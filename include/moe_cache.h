@@ -70,6 +70,15 @@
  *                float32 global scale of gate, up, down, 4 bytes of padding;
  *                3*H*I/2 + 3*H*I/16 + 16 bytes.
  *                element (n,k) = e2m1(code) * e4m3(scale[n][k/16]) * global.
+ *   MOE_W_MXFP4: the same three code banks, then gate scales [I][H/32], up
+ *                scales [I][H/32], down scales [H][I/32] (E8M0: 2^(s - 127),
+ *                0xFF = NaN, one per 32 consecutive row elements), no global
+ *                scale; 3*H*I/2 + 3*H*I/32 bytes [P1 section 7 lists MXFP4
+ *                among the expert formats; layout of the OCP Microscaling
+ *                MXFP4 blocks].  element (n,k) = e2m1(code) * 2^(scale[n][k/32] - 127).
+ *                Decode-sized steps only (the streaming kernels, H a multiple
+ *                of 2048, I of 512) and the hybrid CPU executor; wider steps
+ *                return MOE_ERR_UNSUPPORTED.
  *   H, I and shared_inter must be multiples of 32 (checked at create).
  * Shared expert: a blob of the same format with I = shared_inter, plus a gate
  *   vector w_g bf16 [H]: shared(x) = sigmoid(x . w_g) * FFN_shared(x).
@@ -122,7 +131,7 @@ enum moe_err {
   MOE_ERR_SCRATCH = -8        /* request larger than MOE_NOALLOC_SCRATCH_BYTES allows */
 };
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_MXFP4 = 2 } moe_wfmt;
 typedef enum { MOE_POOL_SHARED = 0, MOE_POOL_PER_LAYER = 1 } moe_pool_mode;
 typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 

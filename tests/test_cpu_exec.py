@@ -14,7 +14,8 @@ import expert_slot_cache_lru_gb300 as m
 import oracle
 import synth
 
-FMT = {synth.FMT_BF16: m.MOE_W_BF16, synth.FMT_NVFP4: m.MOE_W_NVFP4}
+FMT = {synth.FMT_BF16: m.MOE_W_BF16, synth.FMT_NVFP4: m.MOE_W_NVFP4,
+       synth.FMT_MXFP4: m.MOE_W_MXFP4}
 
 
 def _case(w, batch, seed, frac_cpu=0.5):
@@ -46,6 +47,8 @@ SHAPES = {
     "bf16_tiny": synth.scaled(synth.workloads()["tiny"], n_experts=16, top_k=2),
     "nvfp4_small": synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=1, n_experts=8,
                                 hidden=256, inter=128, top_k=4),
+    "mxfp4_small": synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=1, n_experts=8,
+                                hidden=256, inter=128, top_k=4, fmt=synth.FMT_MXFP4),
 }
 
 

@@ -411,3 +411,32 @@ def test_hybrid_graph_replay_equals_eager():
         assert graphed.sc.stats(layer) == eager.sc.stats(layer)
     ce, cg = (m.moe_hybrid_counters(r.sc.handle) for r in (eager, graphed))
     assert ce["jobs"] == cg["jobs"] == w.steps * L and ce["cpu_routes"] == cg["cpu_routes"]
+
+
+def test_mxfp4_layer_fused_equals_four_launch_path_and_oracle():
+    """MXFP4 experts (e2m1 codes, one E8M0 scale per 32 row elements; the
+    formats of FreeToken PR #491, section 7, "What did not change", include
+    MXFP4): the one-launch layer equals the four-launch path byte for byte,
+    both match the fp64 oracle within the fp4 tolerance, and every resident
+    slot holds its expert's bytes.  The shared expert is MXFP4 as well."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], fmt=synth.FMT_MXFP4, n_layers=4,
+                     steps=8, n_slots=60)
+    blobs = synth.HostBlobs(w, pinned=True)
+    a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
+    sa, sb = Stepper(a, True, fused=True), Stepper(b, True)
+    ids, wts = synth.make_routing(w)
+    for t in range(w.steps):
+        x = synth.make_hidden(w, t)
+        sa.step(t, ids[t], wts[t], x)
+        sb.step(t, ids[t], wts[t], x)
+        assert torch.equal(sa.out.view(torch.int16), sb.out.view(torch.int16)), f"step {t}"
+        if t in (0, w.steps - 1):
+            for layer in range(w.n_layers):
+                ref = a.oracle_layer(layer, x[layer], ids[t, layer], wts[t, layer])
+                assert_close(sa.out[layer], ref, w.fmt, f"step {t} layer {layer}")
+    assert sum(a.sc.stats(l)["fetched"] for l in range(w.n_layers)) > 20
+    assert a.sc.stats(0)["status_bits"] == 0
+    state = a.oc.state()
+    for s, key in enumerate(state["slot_key"]):
+        if key >= 0:
+            assert np.array_equal(a.slot_bytes(0, s), a.blobs.blob(int(key))), s
