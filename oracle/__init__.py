@@ -31,6 +31,7 @@ STATUS_CAPACITY = 2
 FMT_BF16 = 0
 FMT_NVFP4 = 1
 FMT_MXFP4 = 2
+FMT_Q4_0 = 3
 
 
 def build(force: bool = False) -> str:
@@ -74,6 +75,8 @@ def lib():
         L.om_e4m3.argtypes = [C.c_int]
         L.om_e8m0.restype = C.c_double
         L.om_e8m0.argtypes = [C.c_int]
+        L.om_f16.restype = C.c_double
+        L.om_f16.argtypes = [C.c_uint16]
         L.om_bf16.restype = C.c_double
         L.om_bf16.argtypes = [C.c_uint16]
         L.om_blob_bytes.restype = C.c_uint64
@@ -209,6 +212,10 @@ def e4m3(byte: int) -> float:
 
 def e8m0(byte: int) -> float:
     return lib().om_e8m0(byte)
+
+
+def f16(bits: int) -> float:
+    return lib().om_f16(bits)
 
 
 def bf16(bits: int) -> float:

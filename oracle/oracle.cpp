@@ -487,6 +487,17 @@ double om_e8m0(int byte) {
   return e == 255 ? NAN : std::ldexp(1.0, e - 127);
 }
 
+// IEEE binary16: 1 sign bit, 5 exponent bits with bias 15, 10 mantissa bits;
+// exponent 0 is subnormal m * 2^-24, exponent 31 is inf (m = 0) or NaN.
+double om_f16(uint16_t bits) {
+  const int s = bits >> 15, e = (bits >> 10) & 31, m = bits & 1023;
+  double mag;
+  if (e == 31) mag = m ? NAN : INFINITY;
+  else if (e == 0) mag = std::ldexp((double)m, -24);
+  else mag = std::ldexp(1.0 + m / 1024.0, e - 15);
+  return s ? -mag : mag;
+}
+
 // bfloat16: the upper 16 bits of an IEEE binary32.
 double om_bf16(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -510,6 +521,24 @@ namespace {
 struct Layout {
   uint64_t code[3], scale[3], glob, total;
 };
+// Q4_0 arithmetic (blocks of 32 weights sharing an fp16 scale d, weight =
+// d * (q - 8) for the 4-bit unsigned code q), laid out in banks like the fp4
+// formats: gate, up, down codes (two per byte, the even element in the low
+// nibble), then gate, up, down fp16 scales (one per 32 consecutive elements
+// of a row), padded to 16 bytes.
+Layout q4_layout(int H, int I) {
+  Layout L{};
+  const uint64_t ih = (uint64_t)I * H;
+  L.code[0] = 0;
+  L.code[1] = ih / 2;
+  L.code[2] = ih;
+  L.scale[0] = 3 * ih / 2;
+  L.scale[1] = L.scale[0] + ih / 16;  // 2 bytes per 32 elements
+  L.scale[2] = L.scale[1] + ih / 16;
+  L.glob = L.scale[2] + ih / 16;
+  L.total = (L.glob + 15) / 16 * 16;
+  return L;
+}
 Layout mxfp4_layout(int H, int I) {
   Layout L{};
   const uint64_t ih = (uint64_t)I * H;
@@ -543,6 +572,7 @@ uint64_t om_blob_bytes(int fmt, int H, int I) {
   if (fmt == OFMT_BF16) return 6ull * H * I;
   if (fmt == OFMT_NVFP4) return nvfp4_layout(H, I).total;
   if (fmt == OFMT_MXFP4) return mxfp4_layout(H, I).total;
+  if (fmt == OFMT_Q4_0) return q4_layout(H, I).total;
   return 0;
 }
 
@@ -556,6 +586,22 @@ int om_dequant(int fmt, const uint8_t* blob, int H, int I, int which, double* ou
       uint16_t b;
       std::memcpy(&b, w + i, 2);
       out[i] = om_bf16(b);
+    }
+    return 0;
+  }
+  if (fmt == OFMT_Q4_0) {  // element = f16(scale) * (code - 8)
+    const Layout L = q4_layout(H, I);
+    const uint8_t* codes = blob + L.code[which];
+    const uint8_t* scales = blob + L.scale[which];
+    for (int n = 0; n < rows; ++n) {
+      for (int k = 0; k < cols; ++k) {
+        const uint64_t idx = (uint64_t)n * cols + k;
+        const uint8_t byte = codes[idx / 2];
+        const int q = (k % 2 == 0) ? (byte & 15) : (byte >> 4);
+        uint16_t d;
+        std::memcpy(&d, scales + 2 * ((uint64_t)n * (cols / 32) + k / 32), 2);
+        out[idx] = om_f16(d) * (double)(q - 8);
+      }
     }
     return 0;
   }

@@ -86,11 +86,12 @@ int oc_state(const ocache* c, int32_t* map, int32_t* slot_key, uint64_t* stamp,
 int oc_lru_order(const ocache* c, int pool, int32_t* out /* n_slots */);
 
 /* ---- expert math, fp64 ---- */
-enum { OFMT_BF16 = 0, OFMT_NVFP4 = 1, OFMT_MXFP4 = 2 };
+enum { OFMT_BF16 = 0, OFMT_NVFP4 = 1, OFMT_MXFP4 = 2, OFMT_Q4_0 = 3 };
 
 double om_e2m1(int code4);
 double om_e4m3(int byte);
 double om_e8m0(int byte);
+double om_f16(uint16_t bits);
 double om_bf16(uint16_t bits);
 /* Bytes of one expert blob in the fused six-bank layout. */
 uint64_t om_blob_bytes(int fmt, int hidden, int inter);

@@ -37,6 +37,7 @@ import numpy as np
 FMT_BF16 = 0
 FMT_NVFP4 = 1
 FMT_MXFP4 = 2
+FMT_Q4_0 = 3
 
 # stream ids of the seed sequence
 S_WEIGHTS, S_PERM, S_ROUTING, S_HIDDEN, S_PRED, S_RWEIGHTS, S_SHARED, S_PREFILL, S_ALIAS = range(1, 10)
@@ -189,11 +190,25 @@ def mxfp4_banks(hidden: int, inter: int) -> dict:
     return o
 
 
+def q4_banks(hidden: int, inter: int) -> dict:
+    """Byte offsets of a Q4_0 blob (banked): the code banks as NVFP4 (4-bit
+    unsigned codes q, weight = d * (q - 8)), then gate/up scales [I, H/32]
+    and down scales [H, I/32] as fp16 d, one per 32 consecutive row elements."""
+    ih = inter * hidden
+    o = {"code": [0, ih // 2, ih], "scale": [3 * ih // 2, 3 * ih // 2 + ih // 16,
+                                             3 * ih // 2 + 2 * (ih // 16)]}
+    o["end"] = 3 * ih // 2 + 3 * (ih // 16)
+    o["total"] = (o["end"] + 15) // 16 * 16
+    return o
+
+
 def blob_bytes(fmt: int, hidden: int, inter: int) -> int:
     if fmt == FMT_BF16:
         return 6 * hidden * inter
     if fmt == FMT_MXFP4:
         return mxfp4_banks(hidden, inter)["total"]
+    if fmt == FMT_Q4_0:
+        return q4_banks(hidden, inter)["total"]
     return nvfp4_banks(hidden, inter)["total"]
 
 
@@ -202,6 +217,15 @@ def fill_blob(out: np.ndarray, fmt: int, hidden: int, inter: int, rng: Rng) -> N
     if fmt == FMT_BF16:
         w = rng.normal(3 * hidden * inter) * 0.02
         out[:] = to_bf16_bits(w).view(np.uint8)
+        return
+    if fmt == FMT_Q4_0:  # random codes; fp16 block scales in [0.001, 0.005)
+        o = q4_banks(hidden, inter)
+        n_codes = o["scale"][0]
+        out[:n_codes] = rng.bytes(n_codes)
+        n_sc = (o["end"] - n_codes) // 2
+        d = (0.001 + 0.004 * rng.uniform(n_sc)).astype(np.float16)
+        out[n_codes:o["end"]] = d.view(np.uint8)
+        out[o["end"]:o["total"]] = 0
         return
     if fmt == FMT_MXFP4:  # random codes; block scales 2^-9 .. 2^-6 (E8M0 118..121)
         o = mxfp4_banks(hidden, inter)

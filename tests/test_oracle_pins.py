@@ -310,6 +310,16 @@ def test_e8m0_exhaustive_against_torch():
     assert oracle.e8m0(254) == 2.0 ** 127 and math.isnan(oracle.e8m0(255))
 
 
+def test_f16_exhaustive_against_numpy():
+    """IEEE binary16 (the Q4_0 block scale): every code against numpy's float16."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16(int(b)) for b in bits])
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.all(np.isnan(got[~fin]))
+
+
 def test_bf16_against_torch():
     bits = np.arange(0, 65536, 37, dtype=np.uint16)
     ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
@@ -366,6 +376,36 @@ def test_mxfp4_dequant_against_numpy(which):
     assert np.array_equal(d[0, :32], 2 * got[0, :32]) and np.array_equal(d[0, 32:], got[0, 32:])
 
 
+def _np_dequant_q4(blob: np.ndarray, H: int, I: int, which: int) -> np.ndarray:
+    """Independent numpy decode of one Q4_0 matrix (banked): d * (q - 8)."""
+    banks = synth.q4_banks(H, I)
+    rows, cols = (H, I) if which == 2 else (I, H)
+    codes = blob[banks["code"][which]:banks["code"][which] + rows * cols // 2]
+    q = np.empty(rows * cols, np.int64)
+    q[0::2] = codes & 15
+    q[1::2] = codes >> 4
+    sc = blob[banks["scale"][which]:banks["scale"][which] + rows * cols // 16]
+    d = sc.view(np.float16).astype(np.float64).reshape(rows, cols // 32)
+    return (q - 8).reshape(rows, cols) * np.repeat(d, 32, axis=1)
+
+
+@pytest.mark.parametrize("which", [0, 1, 2])
+def test_q4_0_dequant_against_numpy(which):
+    H, I = 64, 96
+    blob = np.empty(synth.blob_bytes(synth.FMT_Q4_0, H, I), np.uint8)
+    synth.fill_blob(blob, synth.FMT_Q4_0, H, I, synth.Rng(7, which))
+    assert oracle.blob_bytes(oracle.FMT_Q4_0, H, I) == len(blob) == 3 * H * I // 2 + 3 * H * I // 16
+    got = oracle.dequant(oracle.FMT_Q4_0, blob, H, I, which)
+    assert np.array_equal(got, _np_dequant_q4(blob, H, I, which))
+    # code 8 is zero whatever the scale; code 0 is -8 d
+    banks = synth.q4_banks(H, I)
+    b2 = blob.copy()
+    b2[banks["code"][which]] = 0x08  # element 0: q = 8, element 1: q = 0
+    d = oracle.dequant(oracle.FMT_Q4_0, b2, H, I, which)
+    d0 = float(blob[banks["scale"][which]:banks["scale"][which] + 2].view(np.float16)[0])
+    assert d[0, 0] == 0.0 and d[0, 1] == -8 * d0
+
+
 @pytest.mark.parametrize("which", [0, 1, 2])
 def test_nvfp4_dequant_against_numpy(which):
     H, I = 64, 96
@@ -382,7 +422,8 @@ def _np_ffn(Wg, Wu, Wd, x):
     return Wd @ (g / (1 + np.exp(-g)) * u)
 
 
-@pytest.mark.parametrize("fmt", [oracle.FMT_BF16, oracle.FMT_NVFP4, oracle.FMT_MXFP4])
+@pytest.mark.parametrize("fmt", [oracle.FMT_BF16, oracle.FMT_NVFP4, oracle.FMT_MXFP4,
+                                 oracle.FMT_Q4_0])
 def test_expert_ffn_against_numpy(fmt):
     H, I = 64, 128
     blob = np.empty(synth.blob_bytes(fmt, H, I), np.uint8)
