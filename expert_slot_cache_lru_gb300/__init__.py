@@ -35,6 +35,7 @@ MOE_NOALLOC_SCRATCH_BYTES = 1 << 20
 MOE_W_BF16 = 0
 MOE_W_NVFP4 = 1
 MOE_W_MXFP4 = 2
+MOE_W_Q4_0 = 3
 MOE_POOL_SHARED = 0
 MOE_POOL_PER_LAYER = 1
 MOE_PLAN_DEMAND = 0
@@ -274,6 +275,8 @@ def blob_bytes(wfmt: int, hidden: int, inter: int) -> int:
         return 6 * hidden * inter
     if wfmt == MOE_W_MXFP4:
         return 3 * hidden * inter // 2 + 3 * hidden * inter // 32
+    if wfmt == MOE_W_Q4_0:
+        return 3 * hidden * inter // 2 + 3 * hidden * inter // 16
     return 3 * hidden * inter // 2 + 3 * hidden * inter // 16 + 16
 
 

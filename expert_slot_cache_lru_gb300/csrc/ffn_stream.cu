@@ -211,6 +211,49 @@ __device__ __forceinline__ float dot8_fp4_f(uint32_t w, const float* h) {
   f = h2_f32(e2m1x2_h2<3>(w));
   return fmaf(f.x, h[6], fmaf(f.y, h[7], a));
 }
+// Q4_0 codes: the 8 unsigned 4-bit codes q of w (even element in the low
+// nibble) as four half2 of q - 8, exactly: each q goes into the mantissa of
+// an f16 1024 (byte 0x64 above it), then 1032 is subtracted.
+__device__ __forceinline__ void q4x8_h2(uint32_t w, uint32_t out[4]) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+  const uint32_t m0 = __byte_perm(lo, hi, 0x5140);  // codes 0 1 2 3
+  const uint32_t m1 = __byte_perm(lo, hi, 0x7362);  // codes 4 5 6 7
+  const uint32_t k = 0x64646464u;
+  uint32_t v[4] = {__byte_perm(m0, k, 0x4140), __byte_perm(m0, k, 0x4342),
+                   __byte_perm(m1, k, 0x4140), __byte_perm(m1, k, 0x4342)};
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&v[j]), bias);
+    out[j] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+// sum_{i<8} (q_i - 8) * x[i], x as four half2 words (exact products)
+__device__ __forceinline__ float dot8_q4_h(uint32_t w, uint4 x) {
+  uint32_t q[4];
+  q4x8_h2(w, q);
+  float a = fma2_h(q[0], x.x, 0.f);
+  a = fma2_h(q[1], x.y, a);
+  a = fma2_h(q[2], x.z, a);
+  return fma2_h(q[3], x.w, a);
+}
+// sum_{i<8} (q_i - 8) * h[i], h fp32
+__device__ __forceinline__ float dot8_q4_f(uint32_t w, const float* h) {
+  uint32_t q[4];
+  q4x8_h2(w, q);
+  float2 f = h2_f32(q[0]);
+  float a = fmaf(f.x, h[0], f.y * h[1]);
+  f = h2_f32(q[1]);
+  a = fmaf(f.x, h[2], fmaf(f.y, h[3], a));
+  f = h2_f32(q[2]);
+  a = fmaf(f.x, h[4], fmaf(f.y, h[5], a));
+  f = h2_f32(q[3]);
+  return fmaf(f.x, h[6], fmaf(f.y, h[7], a));
+}
+// an fp16 block scale (Q4_0) as fp32, exactly
+__device__ __forceinline__ float f16_f32(uint32_t bits16) {
+  return __half2float(__ushort_as_half((unsigned short)(bits16 & 0xffffu)));
+}
 // sum_{i<8} bf16 weights (uint4) * bf16 x (uint4), fp32
 __device__ __forceinline__ float dot8_bf16_bf(uint4 w, uint4 x, float a) {
   a = fma2_bf(w.x, x.x, a);
@@ -433,6 +476,49 @@ struct ItemA<MOE_W_MXFP4> {
   }
 };
 
+// Q4_0 (banked): chunks of 2048 elements; one fp16 scale d per 32 elements, so
+// each lane's 32-element block has one scale, weight = d * (q - 8):
+//   gate codes [1024 B] | up codes [1024 B] | gate scales [128 B] | up scales [128 B].
+template <>
+struct ItemA<MOE_W_Q4_0> {
+  static constexpr int CW = 2048;
+  static constexpr int BYTES = 2 * 1024 + 2 * 128;
+  static __device__ __forceinline__ uint32_t issue(uint8_t* slot, const uint8_t* blob,
+                                                   const BlobOff& o, int H, int i, int c,
+                                                   uint64_t* bar, uint64_t pol) {
+    const size_t cr = (size_t)i * (H / 2) + c * 1024, sr = (size_t)i * (H / 16) + c * 128;
+    bulk_g2s(slot, blob + o.code[0] + cr, 1024, bar, pol);
+    bulk_g2s(slot + 1024, blob + o.code[1] + cr, 1024, bar, pol);
+    bulk_g2s(slot + 2048, blob + o.scale[0] + sr, 128, bar, pol);
+    bulk_g2s(slot + 2176, blob + o.scale[1] + sr, 128, bar, pol);
+    return BYTES;
+  }
+  static __device__ __forceinline__ float2 glob(const uint8_t*, const BlobOff&) {
+    return make_float2(1.f, 1.f);
+  }
+  static __device__ __forceinline__ void dot(const uint8_t* slot, const uint4* xr, int c, int lane,
+                                             float& g, float& u) {
+    const uint4 g0 = *reinterpret_cast<const uint4*>(slot + lane * 16);
+    const uint4 g1 = *reinterpret_cast<const uint4*>(slot + 512 + lane * 16);
+    const uint4 u0 = *reinterpret_cast<const uint4*>(slot + 1024 + lane * 16);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(slot + 1536 + lane * 16);
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(slot + 2048);
+    const float sg0 = f16_f32(sc[lane]), sg1 = f16_f32(sc[32 + lane]);
+    const float su0 = f16_f32(sc[64 + lane]), su1 = f16_f32(sc[96 + lane]);
+    const int ua = c * 256 + lane * 4, ub = ua + 128;
+    uint4 x0 = xr[xswz(ua)], x1 = xr[xswz(ua + 1)], x2 = xr[xswz(ua + 2)], x3 = xr[xswz(ua + 3)];
+    g = fmaf((dot8_q4_h(g0.x, x0) + dot8_q4_h(g0.y, x1)) +
+             (dot8_q4_h(g0.z, x2) + dot8_q4_h(g0.w, x3)), sg0, g);
+    u = fmaf((dot8_q4_h(u0.x, x0) + dot8_q4_h(u0.y, x1)) +
+             (dot8_q4_h(u0.z, x2) + dot8_q4_h(u0.w, x3)), su0, u);
+    x0 = xr[xswz(ub)], x1 = xr[xswz(ub + 1)], x2 = xr[xswz(ub + 2)], x3 = xr[xswz(ub + 3)];
+    g = fmaf((dot8_q4_h(g1.x, x0) + dot8_q4_h(g1.y, x1)) +
+             (dot8_q4_h(g1.z, x2) + dot8_q4_h(g1.w, x3)), sg1, g);
+    u = fmaf((dot8_q4_h(u1.x, x0) + dot8_q4_h(u1.y, x1)) +
+             (dot8_q4_h(u1.z, x2) + dot8_q4_h(u1.w, x3)), su1, u);
+  }
+};
+
 constexpr int kSlotBytes = 2432;  // >= ItemA<*>::BYTES, a multiple of 128
 
 // ------------------------------------------------------------ phase B items
@@ -459,6 +545,16 @@ __device__ __forceinline__ void itemb_load(ItemB<FMT>& it, const uint8_t* codes,
       it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
       it.w[1].x = *reinterpret_cast<const uint16_t*>(scales + lane * 2);
     }
+  } else if (FMT == MOE_W_Q4_0) {  // the lane's 16 or 32 elements: one fp16 32-block scale
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(scales);
+    if (m == 1) {
+      const uint2 cw = *reinterpret_cast<const uint2*>(codes + lane * 8);
+      it.w[0] = make_uint4(cw.x, cw.y, 0u, 0u);
+      it.w[1].x = sc[lane >> 1];
+    } else {
+      it.w[0] = *reinterpret_cast<const uint4*>(codes + lane * 16);
+      it.w[1].x = sc[lane];
+    }
   } else if (FMT == MOE_W_MXFP4) {  // the lane's 16 (m = 1) or 32 elements: one 32-block scale
     if (m == 1) {
       const uint2 cw = *reinterpret_cast<const uint2*>(codes + lane * 8);
@@ -484,6 +580,10 @@ __device__ __forceinline__ float itemb_dot(const ItemB<FMT>& it, const float* hv
     float p = (dot8_fp4_f(it.w[0].x, hv) + dot8_fp4_f(it.w[0].y, hv + 8)) * sc.x;
     if (m == 2) p = fmaf(dot8_fp4_f(it.w[0].z, hv + 16) + dot8_fp4_f(it.w[0].w, hv + 24), sc.y, p);
     return p;
+  } else if (FMT == MOE_W_Q4_0) {
+    float p = dot8_q4_f(it.w[0].x, hv) + dot8_q4_f(it.w[0].y, hv + 8);
+    if (m == 2) p += dot8_q4_f(it.w[0].z, hv + 16) + dot8_q4_f(it.w[0].w, hv + 24);
+    return p * f16_f32(it.w[1].x);
   } else if (FMT == MOE_W_MXFP4) {
     float p = dot8_fp4_f(it.w[0].x, hv) + dot8_fp4_f(it.w[0].y, hv + 8);
     if (m == 2) p += dot8_fp4_f(it.w[0].z, hv + 16) + dot8_fp4_f(it.w[0].w, hv + 24);
@@ -630,7 +730,7 @@ template <int FMT, int MODE>
 __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) {
   constexpr bool SHARED = MODE == kShared, ADMIT = MODE == kLayerAdmit;
   constexpr bool LAYER = MODE == kLayer || ADMIT;
-  constexpr bool FP4 = FMT != MOE_W_BF16;  // NVFP4 or MXFP4 experts: e2m1 codes, f16 x
+  constexpr bool FP4 = FMT != MOE_W_BF16;  // 4-bit codes (NVFP4, MXFP4, Q4_0): f16 x
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ unsigned long long s_j;  // admission inside: this launch's index
   if (ADMIT) {  // every CTA of launch j adds one to a.epoch: j = old / gridDim.x
@@ -658,7 +758,7 @@ __global__ void __maxnreg__(kMaxReg) ffn_fused_kernel(DevState st, FusedArgs a) 
   const int H = a.H, I = a.I, k = a.k, n_rows = a.n_rows;
   const int m = I / 512;                                   // 16-element groups per lane (B)
   const int CB = FP4 ? I / 2 : I * 2;                      // down row: code bytes
-  const int SB = FMT == MOE_W_NVFP4 ? I / 16 : (FP4 ? I / 32 : 0);  // down row: scale bytes
+  const int SB = FMT == MOE_W_MXFP4 ? I / 32 : (FP4 ? I / 16 : 0);  // down row: scale bytes
   constexpr int CW = ItemA<FMT>::CW;
   const int KC = H / CW;                                   // phase-A chunks per row
   const BlobOff o(H, I, FMT);
@@ -1464,7 +1564,7 @@ struct Plan {
 Plan fused_plan(int wfmt, int H, int I, int n_rows, int k, int T, int G) {
   Plan p{};
   const int perB = (n_rows * H + G - 1) / G;
-  const int rowB = wfmt == MOE_W_NVFP4 ? I / 2 + I / 16 : (wfmt == MOE_W_MXFP4 ? I / 2 + I / 32 : I * 2);
+  const int rowB = wfmt == MOE_W_BF16 ? I * 2 : (wfmt == MOE_W_MXFP4 ? I / 2 + I / 32 : I / 2 + I / 16);
   p.htasks = std::min(T, 2 * k);
   const size_t fixed = round128((size_t)n_rows * H * 2) + round128((size_t)T * perB * 4) +
                        round128((size_t)p.htasks * I * 4) + (size_t)kW * 2 * kSlotBytes;
@@ -1527,6 +1627,7 @@ cudaError_t launch_format(int wfmt, int mode, size_t smem, cudaStream_t s, const
                           const FusedArgs& a) {
   if (wfmt == MOE_W_NVFP4) return launch_mode<MOE_W_NVFP4>(mode, smem, s, st, a);
   if (wfmt == MOE_W_MXFP4) return launch_mode<MOE_W_MXFP4>(mode, smem, s, st, a);
+  if (wfmt == MOE_W_Q4_0) return launch_mode<MOE_W_Q4_0>(mode, smem, s, st, a);
   return launch_mode<MOE_W_BF16>(mode, smem, s, st, a);
 }
 
@@ -1574,6 +1675,10 @@ cudaError_t ffn_stream_init(int wfmt, int H, int I, int Is, int max_rows, int ma
   set(ffn_fused_kernel<MOE_W_MXFP4, kRouted>);
   set(ffn_fused_kernel<MOE_W_MXFP4, kLayer>);
   set(ffn_fused_kernel<MOE_W_MXFP4, kLayerAdmit>);
+  set(ffn_fused_kernel<MOE_W_Q4_0, kShared>);
+  set(ffn_fused_kernel<MOE_W_Q4_0, kRouted>);
+  set(ffn_fused_kernel<MOE_W_Q4_0, kLayer>);
+  set(ffn_fused_kernel<MOE_W_Q4_0, kLayerAdmit>);
   (void)wfmt, (void)H, (void)I, (void)Is, (void)max_rows, (void)max_tasks;
   return e;
 }

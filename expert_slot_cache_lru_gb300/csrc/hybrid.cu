@@ -147,6 +147,38 @@ inline float dot_mx(const uint8_t* codes, const uint8_t* scales, const float* x,
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// IEEE binary16 bits -> fp32 (exact), from the bit fields
+inline float f16f(uint16_t v) {
+  const int s = v >> 15, e = (v >> 10) & 31, m = v & 1023;
+  float mag;
+  if (e == 31)
+    mag = m ? NAN : INFINITY;
+  else if (e == 0)
+    mag = std::ldexp((float)m, -24);
+  else
+    mag = std::ldexp(1.f + (float)m / 1024.f, e - 15);
+  return s ? -mag : mag;
+}
+
+// The same for one Q4_0 row (banked): per block of 32 elements the products
+// (q - 8) * x are summed, then scaled by the block's fp16 d; four sums.
+inline float dot_q4(const uint8_t* codes, const uint8_t* scales, const float* x, int n) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int blk = 0; blk < n / 32; ++blk) {
+    const uint8_t* c = codes + blk * 16;
+    const float* xb = x + blk * 32;
+    float s = 0.f;
+    for (int u = 0; u < 16; ++u) {
+      s += (float)((int)(c[u] & 15) - 8) * xb[2 * u];
+      s += (float)((int)(c[u] >> 4) - 8) * xb[2 * u + 1];
+    }
+    uint16_t d;
+    std::memcpy(&d, scales + 2 * blk, 2);
+    acc[blk & 3] += s * f16f(d);
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 // Row `r` of bank `which` (0 gate, 1 up: [I][H]; 2 down: [H][I]) dotted with x.
 inline float row_dot(int wfmt, const uint8_t* blob, const Banks& bk, int H, int I, int which,
                      int r, const float* x) {
@@ -155,6 +187,9 @@ inline float row_dot(int wfmt, const uint8_t* blob, const Banks& bk, int H, int 
     const uint16_t* m = reinterpret_cast<const uint16_t*>(blob) + (size_t)which * H * I;
     return dot_bf16(m + (size_t)r * n, x, n);
   }
+  if (wfmt == MOE_W_Q4_0)
+    return dot_q4(blob + bk.code[which] + (size_t)r * (n / 2),
+                  blob + bk.scale[which] + (size_t)r * (n / 16), x, n);
   if (wfmt == MOE_W_MXFP4)
     return dot_mx(blob + bk.code[which] + (size_t)r * (n / 2),
                   blob + bk.scale[which] + (size_t)r * (n / 32), x, n);
@@ -550,7 +585,7 @@ extern "C" {
 int moe_cpu_experts(int wfmt, int hidden, int inter, const void* const* h_blobs, int n_experts,
                     const uint16_t* h_x, const int32_t* h_ids, const int32_t* h_slot_ids,
                     const float* h_w, int n_rows, int k, int n_threads, float* h_out) {
-  if ((wfmt != MOE_W_BF16 && wfmt != MOE_W_NVFP4 && wfmt != MOE_W_MXFP4) || hidden <= 0 ||
+  if (wfmt < MOE_W_BF16 || wfmt > MOE_W_Q4_0 || hidden <= 0 ||
       inter <= 0 || hidden % 32 ||
       inter % 32 || n_experts <= 0 || !h_blobs || n_rows < 0 || k < 0 || n_threads < 1 ||
       n_threads > 256)

@@ -66,6 +66,7 @@ size_t blob_bytes(int fmt, int H, int I) {
   if (fmt == MOE_W_BF16) return 6 * ih;
   if (fmt == MOE_W_NVFP4) return 3 * ih / 2 + 3 * ih / 16 + 16;
   if (fmt == MOE_W_MXFP4) return 3 * ih / 2 + 3 * ih / 32;
+  if (fmt == MOE_W_Q4_0) return 3 * ih / 2 + 3 * ih / 16;
   return 0;
 }
 
@@ -125,7 +126,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   if (compute) {
     if (d.hidden <= 0 || d.inter <= 0 || d.hidden % 32 || d.inter % 32 || d.shared_inter < 0 ||
         d.shared_inter % 32 ||
-        (d.wfmt != MOE_W_BF16 && d.wfmt != MOE_W_NVFP4 && d.wfmt != MOE_W_MXFP4))
+        (d.wfmt < MOE_W_BF16 || d.wfmt > MOE_W_Q4_0))
       return MOE_ERR_CONFIG;
     if (d.slot_bytes != blob_bytes(d.wfmt, d.hidden, d.inter)) return MOE_ERR_CONFIG;
     if ((size_t)d.hidden * 4 > 200 * 1024) return MOE_ERR_UNSUPPORTED;
@@ -409,7 +410,8 @@ static int run_shared(moe_cache* c, const void* d_x, int n_rows, const void* blo
                                  static_cast<const uint8_t*>(blob), gate, c->sc, c->st.status, s));
     return MOE_OK;
   }
-  if (c->d.wfmt == MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;  // streaming kernels only
+  if (c->d.wfmt != MOE_W_BF16 && c->d.wfmt != MOE_W_NVFP4)  // streaming kernels only
+    return MOE_ERR_UNSUPPORTED;
   CK(moe::launch_shared_expert(c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows,
                                static_cast<const uint8_t*>(blob), gate, c->sc, s));
   return MOE_OK;
@@ -425,7 +427,7 @@ static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* s
                                  k, with_shared ? c->sc.ys : nullptr, d_out, c->sc, c->st.status, s));
     return MOE_OK;
   }
-  if (d.wfmt == MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;  // streaming kernels only
+  if (d.wfmt != MOE_W_BF16 && d.wfmt != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;  // streaming only
   if (k > 0 && moe::grouped_supported(d.wfmt, d.hidden, d.inter, d.n_experts)) {
     CK(moe::launch_routed_grouped(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w,
                                   n_rows, k, with_shared ? c->sc.ys : nullptr, d_out, c->sc,
@@ -457,7 +459,7 @@ int moe_routed_experts_noalloc(int wfmt, int hidden, int inter, const void* d_sl
                                size_t slot_stride, int n_slots, const void* d_x,
                                const int32_t* d_slot_ids, const float* d_w, int n_rows, int k,
                                void* d_out, unsigned long long* d_status, void* stream) {
-  if ((wfmt != MOE_W_BF16 && wfmt != MOE_W_NVFP4 && wfmt != MOE_W_MXFP4) || hidden <= 0 ||
+  if (wfmt < MOE_W_BF16 || wfmt > MOE_W_Q4_0 || hidden <= 0 ||
       inter <= 0 || hidden % 32 ||
       inter % 32 || n_slots <= 0 || n_rows < 0 || k < 0)
     return MOE_ERR_INVALID_ARG;

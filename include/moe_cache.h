@@ -79,6 +79,14 @@
  *                Decode-sized steps only (the streaming kernels, H a multiple
  *                of 2048, I of 512) and the hybrid CPU executor; wider steps
  *                return MOE_ERR_UNSUPPORTED.
+ *   MOE_W_Q4_0:  the arithmetic of Q4_0 (blocks of 32 weights, weight =
+ *                d * (q - 8) with q an unsigned 4-bit code and d an fp16
+ *                scale) in the same banked layout: the three code banks (q,
+ *                two per byte, even element in the low nibble), then gate
+ *                scales [I][H/32], up scales [I][H/32], down scales [H][I/32]
+ *                as fp16 d; 3*H*I/2 + 3*H*I/16 bytes [P1 section 7 lists
+ *                Q4_0].  Not the interleaved block bytes of other libraries.
+ *                Same shapes and paths as MOE_W_MXFP4.
  *   H, I and shared_inter must be multiples of 32 (checked at create).
  * Shared expert: a blob of the same format with I = shared_inter, plus a gate
  *   vector w_g bf16 [H]: shared(x) = sigmoid(x . w_g) * FFN_shared(x).
@@ -131,7 +139,7 @@ enum moe_err {
   MOE_ERR_SCRATCH = -8        /* request larger than MOE_NOALLOC_SCRATCH_BYTES allows */
 };
 
-typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_MXFP4 = 2 } moe_wfmt;
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1, MOE_W_MXFP4 = 2, MOE_W_Q4_0 = 3 } moe_wfmt;
 typedef enum { MOE_POOL_SHARED = 0, MOE_POOL_PER_LAYER = 1 } moe_pool_mode;
 typedef enum { MOE_PLAN_DEMAND = 0, MOE_PLAN_PREFETCH = 1 } moe_plan_kind;
 

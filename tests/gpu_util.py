@@ -8,8 +8,8 @@ import torch
 import oracle
 import synth
 
-TOL = {synth.FMT_NVFP4: (2e-2, 1e-2), synth.FMT_MXFP4: (2e-2, 1e-2),
-       synth.FMT_BF16: (5e-3, 1e-2)}  # (atol, rtol); MXFP4 takes the fp4 tolerance
+TOL = {synth.FMT_NVFP4: (2e-2, 1e-2), synth.FMT_MXFP4: (2e-2, 1e-2), synth.FMT_Q4_0: (2e-2, 1e-2),
+       synth.FMT_BF16: (5e-3, 1e-2)}  # (atol, rtol); the 4-bit formats take the fp4 tolerance
 
 
 class _Dev:

@@ -105,7 +105,7 @@ def test_host_side_validation(m):
 def test_blob_bytes_agree_with_header_layout(m):
     import synth
     for fmt, H, I in [(0, 64, 128), (1, 2048, 512), (1, 2048, 768), (0, 4096, 1024),
-                      (2, 2048, 512), (2, 64, 96)]:
+                      (2, 2048, 512), (2, 64, 96), (3, 2048, 512), (3, 64, 96)]:
         assert m.blob_bytes(fmt, H, I) == synth.blob_bytes(fmt, H, I)
 
 

@@ -15,7 +15,7 @@ import oracle
 import synth
 
 FMT = {synth.FMT_BF16: m.MOE_W_BF16, synth.FMT_NVFP4: m.MOE_W_NVFP4,
-       synth.FMT_MXFP4: m.MOE_W_MXFP4}
+       synth.FMT_MXFP4: m.MOE_W_MXFP4, synth.FMT_Q4_0: m.MOE_W_Q4_0}
 
 
 def _case(w, batch, seed, frac_cpu=0.5):
@@ -49,6 +49,8 @@ SHAPES = {
                                 hidden=256, inter=128, top_k=4),
     "mxfp4_small": synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=1, n_experts=8,
                                 hidden=256, inter=128, top_k=4, fmt=synth.FMT_MXFP4),
+    "q4_0_small": synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=1, n_experts=8,
+                               hidden=256, inter=128, top_k=4, fmt=synth.FMT_Q4_0),
 }
 
 

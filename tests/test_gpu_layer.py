@@ -413,14 +413,16 @@ def test_hybrid_graph_replay_equals_eager():
     assert ce["jobs"] == cg["jobs"] == w.steps * L and ce["cpu_routes"] == cg["cpu_routes"]
 
 
-def test_mxfp4_layer_fused_equals_four_launch_path_and_oracle():
-    """MXFP4 experts (e2m1 codes, one E8M0 scale per 32 row elements; the
-    formats of FreeToken PR #491, section 7, "What did not change", include
-    MXFP4): the one-launch layer equals the four-launch path byte for byte,
-    both match the fp64 oracle within the fp4 tolerance, and every resident
-    slot holds its expert's bytes.  The shared expert is MXFP4 as well."""
-    w = synth.scaled(synth.workloads()["qwen3moe_decode"], fmt=synth.FMT_MXFP4, n_layers=4,
-                     steps=8, n_slots=60)
+@pytest.mark.parametrize("fmt", [synth.FMT_MXFP4, synth.FMT_Q4_0])
+def test_4bit_formats_layer_fused_equals_four_launch_path_and_oracle(fmt):
+    """MXFP4 (e2m1 codes, one E8M0 scale per 32 row elements) and Q4_0 (fp16
+    d * (q - 8) per 32 row elements) experts -- formats listed in FreeToken PR
+    #491, section 7, "What did not change": the one-launch layer equals the
+    four-launch path byte for byte, both match the fp64 oracle within the fp4
+    tolerance, and every resident slot holds its expert's bytes.  The shared
+    expert has the routed experts' format."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], fmt=fmt, n_layers=4, steps=8,
+                     n_slots=60)
     blobs = synth.HostBlobs(w, pinned=True)
     a, b = Rig(w, blobs=blobs), Rig(w, blobs=blobs)
     sa, sb = Stepper(a, True, fused=True), Stepper(b, True)
