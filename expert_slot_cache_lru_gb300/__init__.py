@@ -45,6 +45,7 @@ MOE_FUSED = 2
 MOE_HYBRID = 4
 MOE_STATUS_INVALID_ID = 1
 MOE_STATUS_CAPACITY = 2
+MOE_STATUS_TIMEOUT = 4
 
 
 class moe_cache_desc(C.Structure):
@@ -98,6 +99,7 @@ _SIGS = {
     "moe_hybrid_start": [_vp, _i],
     "moe_hybrid_stop": [_vp],
     "moe_hybrid_counters": [_vp, _vp],
+    "moe_hybrid_pause": [_vp, _i],
     "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
     "moe_last_cuda_error": [],
@@ -240,6 +242,10 @@ def moe_hybrid_start(cache: int, n_threads: int) -> None:
 
 def moe_hybrid_stop(cache: int) -> None:
     _check("moe_hybrid_stop", _lib.moe_hybrid_stop(cache))
+
+
+def moe_hybrid_pause(cache: int, paused: bool) -> None:
+    _check("moe_hybrid_pause", _lib.moe_hybrid_pause(cache, int(paused)))
 
 
 def moe_hybrid_counters(cache: int) -> dict:

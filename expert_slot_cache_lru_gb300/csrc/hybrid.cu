@@ -347,6 +347,7 @@ struct moe_cpu_exec {
   std::atomic<unsigned long long> gen{0};  // jobs handed to the workers
   std::atomic<int> finished{0};            // worker passes over handed jobs
   std::atomic<bool> stop{false};
+  std::atomic<bool> paused{false};  // test hook: jobs are left unanswered while set
   std::atomic<unsigned long long> jobs{0}, routes{0}, busy_ns{0};
   std::vector<std::thread> threads;
 
@@ -383,7 +384,10 @@ void coordinator(moe_cpu_exec* x) {
   const int nw = x->n_threads - 1;
   for (;;) {
     unsigned long long seq = 0;
-    if (!wait_for([&] { return (seq = __atomic_load_n(&hd->job_seq, __ATOMIC_ACQUIRE)) != last; },
+    if (!wait_for([&] {
+          if (x->paused.load(std::memory_order_relaxed)) return false;
+          return (seq = __atomic_load_n(&hd->job_seq, __ATOMIC_ACQUIRE)) != last;
+        },
                   x->stop))
       return;
     if (!wait_for([&] { return x->finished.load(std::memory_order_acquire) >= (int)(handed * nw); },
@@ -571,6 +575,8 @@ int hybrid_start(const HybridConfig& c, moe_cpu_exec** out) {
   *out = x;
   return MOE_OK;
 }
+
+void hybrid_pause(moe_cpu_exec* x, bool paused) { x->paused.store(paused, std::memory_order_relaxed); }
 
 void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[3]) {
   out[0] = x->jobs.load(std::memory_order_relaxed);

@@ -595,6 +595,13 @@ int moe_hybrid_stop(moe_cache* c) {
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "hybrid stop sync");
 }
 
+int moe_hybrid_pause(moe_cache* c, int paused) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (!c->cpu) return MOE_ERR_STATE;
+  moe::hybrid_pause(c->cpu, paused != 0);
+  return MOE_OK;
+}
+
 int moe_hybrid_counters(moe_cache* c, uint64_t h_out[3]) {
   if (!c || !h_out) return MOE_ERR_INVALID_ARG;
   if (!c->cpu) return MOE_ERR_STATE;

@@ -364,6 +364,10 @@ MOE_API int moe_hybrid_start(moe_cache* c, int n_threads);
 MOE_API int moe_hybrid_stop(moe_cache* c);
 /* jobs done, CPU routes computed, nanoseconds the coordinator spent on jobs */
 MOE_API int moe_hybrid_counters(moe_cache* c, uint64_t h_out[3]);
+/* Test hook: while paused != 0 the executor leaves posted jobs unanswered, so
+ * the GPU's bounded wait runs out (MOE_STATUS_TIMEOUT, GPU partial kept);
+ * resuming answers the newest posted job. */
+MOE_API int moe_hybrid_pause(moe_cache* c, int paused);
 
 /* The CPU partial above as a plain host function (no GPU, no cache): h_blobs
  * [n_experts] host blob addresses of one layer; h_x bf16 [n_rows][H]; h_ids,

@@ -442,3 +442,38 @@ def test_4bit_formats_layer_fused_equals_four_launch_path_and_oracle(fmt):
     for s, key in enumerate(state["slot_key"]):
         if key >= 0:
             assert np.array_equal(a.slot_bytes(0, s), a.blobs.blob(int(key))), s
+
+
+def test_hybrid_wait_runs_out_and_reports_timeout():
+    """Failure detection without a fault: while the executor is paused nothing
+    answers the step's job, so the add kernel's bounded wait (1 s of
+    %globaltimer) runs out, sets MOE_STATUS_TIMEOUT and leaves the GPU
+    partial as the output; the context stays usable, and after resuming the
+    next step is whole again."""
+    w = synth.scaled(synth.workloads()["tiny"], steps=3, fetch_cap=1, batch=2)
+    rig = Rig(w)
+    m = rig.m
+    m.moe_hybrid_start(rig.sc.handle, 2)
+    st = Stepper(rig, hybrid=True)
+    ids, wts = synth.make_routing(w)
+
+    def run(t, whole):
+        x = synth.make_hidden(w, t)
+        refs = st.step(t, ids[t], wts[t], x, check_state=False)
+        gs, os_ = rig.sc.stats(0), rig.oc.stats(0)  # exact, but for the timeout bit
+        assert {**gs, "status_bits": 0} == {**os_, "status_bits": 0}, t
+        slots = refs[0]["slots"].reshape(w.batch, w.top_k)
+        mask = None if whole else (slots >= 0).astype(np.uint8)
+        ref = rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0], mask=mask)
+        assert_close(st.out[0], ref, w.fmt, f"step {t}")
+        return slots
+
+    run(0, whole=True)
+    assert not rig.sc.stats(0)["status_bits"] & m.MOE_STATUS_TIMEOUT
+    m.moe_hybrid_pause(rig.sc.handle, True)
+    slots = run(1, whole=False)
+    assert (slots < 0).any()  # the step had CPU routes, which the output now lacks
+    assert rig.sc.stats(0)["status_bits"] & m.MOE_STATUS_TIMEOUT
+    m.moe_hybrid_pause(rig.sc.handle, False)
+    run(2, whole=True)
+    m.moe_hybrid_stop(rig.sc.handle)
