@@ -521,6 +521,19 @@ def hybrid_step(dev: int, warm: int = 4, tokens: int = 8) -> dict:
     s = torch.cuda.Stream()
     n_threads = max(1, min(16, os.cpu_count() or 1))
     res = {"threads": n_threads, "tokens": tokens}
+    # the host-read reference for the executor: a plain multi-threaded read of
+    # the same pinned blobs (torch's fp32 sum over the bytes viewed as fp32,
+    # whatever values they hold), with as many threads as the pool, best of 3
+    prev = torch.get_num_threads()
+    torch.set_num_threads(n_threads)
+    flat = blobs.buf[:blobs.buf.numel() // 4 * 4].view(torch.float32)
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        flat.sum()
+        times.append(time.perf_counter() - t0)
+    torch.set_num_threads(prev)
+    host_gbs = flat.numel() * 4 / min(times) / 1e9
     for hybrid in (True, False):
         storage = torch.empty(w.n_slots * blobs.stride, dtype=torch.uint8, device="cuda")
         cache = m.SlotCache(n_layers=L, n_experts=w.n_experts, n_slots=w.n_slots,
@@ -583,11 +596,14 @@ def hybrid_step(dev: int, warm: int = 4, tokens: int = 8) -> dict:
             jobs = c1["jobs"] - c0["jobs"]
             routes = c1["cpu_routes"] - c0["cpu_routes"]
             busy = (c1["busy_ns"] - c0["busy_ns"]) * 1e-9
+            busy_r = (c1["busy_route_ns"] - c0["busy_route_ns"]) * 1e-9
+            gbs = routes * w.blob_bytes / max(busy_r, 1e-9) / 1e9
             res[key].update({"jobs": jobs, "cpu_routes": routes,
                              "cpu_routes_per_token": round(routes / tokens, 2),
                              "cpu_busy_us_per_job": round(busy / max(jobs, 1) * 1e6, 1),
-                             "cpu_expert_gbs": round(routes * w.blob_bytes / max(busy, 1e-9) / 1e9,
-                                                     1)})
+                             "cpu_expert_gbs": round(gbs, 1),
+                             "host_read_gbs": round(host_gbs, 1),
+                             "frac_of_host_read": round(gbs / host_gbs, 3)})
             m.moe_hybrid_stop(cache.handle)
         cache.close()
         del storage

@@ -250,9 +250,10 @@ def moe_hybrid_pause(cache: int, paused: bool) -> None:
 
 def moe_hybrid_counters(cache: int) -> dict:
     import numpy as np
-    out = np.zeros(3, np.uint64)
+    out = np.zeros(4, np.uint64)
     _check("moe_hybrid_counters", _lib.moe_hybrid_counters(cache, out.ctypes.data))
-    return {"jobs": int(out[0]), "cpu_routes": int(out[1]), "busy_ns": int(out[2])}
+    return {"jobs": int(out[0]), "cpu_routes": int(out[1]), "busy_ns": int(out[2]),
+            "busy_route_ns": int(out[3])}
 
 
 def moe_cpu_experts(wfmt: int, hidden: int, inter: int, blob_ptrs, x_bf16, ids, slot_ids, w,

@@ -237,7 +237,7 @@ struct HybridConfig {
 int hybrid_start(const HybridConfig& c, moe_cpu_exec** out);  // MOE_OK, MOE_ERR_*, or
                                                                // -1000 - cudaError_t
 void hybrid_stop(moe_cpu_exec* x);
-void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[3]);
+void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[4]);
 void hybrid_pause(moe_cpu_exec* x, bool paused);
 cudaError_t hybrid_post(moe_cpu_exec* x, int layer, const int32_t* ids, const int32_t* slots,
                         const float* w, const void* xin, int n_rows, int k, cudaStream_t s);

@@ -349,6 +349,7 @@ struct moe_cpu_exec {
   std::atomic<bool> stop{false};
   std::atomic<bool> paused{false};  // test hook: jobs are left unanswered while set
   std::atomic<unsigned long long> jobs{0}, routes{0}, busy_ns{0};
+  std::atomic<unsigned long long> busy_route_ns{0};  // ... of the jobs with -1 routes
   std::vector<std::thread> threads;
 
   moe::cpu::MailHeader* hdr() { return reinterpret_cast<moe::cpu::MailHeader*>(mb); }
@@ -414,11 +415,12 @@ void coordinator(moe_cpu_exec* x) {
     x->gen.store(++handed, std::memory_order_release);
     w.run();
     while (!w.complete()) std::this_thread::yield();
+    const auto dt = (unsigned long long)std::chrono::duration_cast<std::chrono::nanoseconds>(
+                        std::chrono::steady_clock::now() - t0).count();
     x->routes.fetch_add(w.routes.size(), std::memory_order_relaxed);
     x->jobs.fetch_add(1, std::memory_order_relaxed);
-    x->busy_ns.fetch_add((unsigned long long)std::chrono::duration_cast<std::chrono::nanoseconds>(
-                             std::chrono::steady_clock::now() - t0).count(),
-                         std::memory_order_relaxed);
+    x->busy_ns.fetch_add(dt, std::memory_order_relaxed);
+    if (!w.routes.empty()) x->busy_route_ns.fetch_add(dt, std::memory_order_relaxed);
     __atomic_store_n(&hd->done_seq, seq, __ATOMIC_RELEASE);
     last = seq;
   }
@@ -578,10 +580,11 @@ int hybrid_start(const HybridConfig& c, moe_cpu_exec** out) {
 
 void hybrid_pause(moe_cpu_exec* x, bool paused) { x->paused.store(paused, std::memory_order_relaxed); }
 
-void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[3]) {
+void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[4]) {
   out[0] = x->jobs.load(std::memory_order_relaxed);
   out[1] = x->routes.load(std::memory_order_relaxed);
   out[2] = x->busy_ns.load(std::memory_order_relaxed);
+  out[3] = x->busy_route_ns.load(std::memory_order_relaxed);
 }
 
 }  // namespace moe

@@ -602,12 +602,12 @@ int moe_hybrid_pause(moe_cache* c, int paused) {
   return MOE_OK;
 }
 
-int moe_hybrid_counters(moe_cache* c, uint64_t h_out[3]) {
+int moe_hybrid_counters(moe_cache* c, uint64_t h_out[4]) {
   if (!c || !h_out) return MOE_ERR_INVALID_ARG;
   if (!c->cpu) return MOE_ERR_STATE;
-  unsigned long long v[3];
+  unsigned long long v[4];
   moe::hybrid_counters(c->cpu, v);
-  for (int i = 0; i < 3; ++i) h_out[i] = v[i];
+  for (int i = 0; i < 4; ++i) h_out[i] = v[i];
   return MOE_OK;
 }
 

@@ -362,8 +362,9 @@ MOE_API int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int
  * the one-launch gather + experts kernel.  MOE_ERR_STATE if no executor runs. */
 MOE_API int moe_hybrid_start(moe_cache* c, int n_threads);
 MOE_API int moe_hybrid_stop(moe_cache* c);
-/* jobs done, CPU routes computed, nanoseconds the coordinator spent on jobs */
-MOE_API int moe_hybrid_counters(moe_cache* c, uint64_t h_out[3]);
+/* jobs done, CPU routes computed, nanoseconds the coordinator spent on jobs,
+ * and on the jobs that had at least one -1 route */
+MOE_API int moe_hybrid_counters(moe_cache* c, uint64_t h_out[4]);
 /* Test hook: while paused != 0 the executor leaves posted jobs unanswered, so
  * the GPU's bounded wait runs out (MOE_STATUS_TIMEOUT, GPU partial kept);
  * resuming answers the newest posted job. */
