@@ -359,7 +359,10 @@ MOE_API int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int
  * Every step posts a job, even one without -1 routes, so a captured graph
  * does not depend on the hit pattern; both kernels are capturable.  With
  * MOE_FUSED the admission runs as its own launch, followed by the post and
- * the one-launch gather + experts kernel.  MOE_ERR_STATE if no executor runs. */
+ * the one-launch gather + experts kernel.  MOE_ERR_STATE if no executor runs.
+ * A graph captured with MOE_HYBRID holds the executor's mailbox and counter
+ * addresses: replay it only while that executor runs (not after
+ * moe_hybrid_stop, a later moe_hybrid_start or moe_cache_destroy). */
 MOE_API int moe_hybrid_start(moe_cache* c, int n_threads);
 MOE_API int moe_hybrid_stop(moe_cache* c);
 /* jobs done, CPU routes computed, nanoseconds the coordinator spent on jobs,
