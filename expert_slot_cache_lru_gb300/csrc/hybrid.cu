@@ -345,7 +345,7 @@ struct moe_cpu_exec {
   std::vector<float> xf, h;
   moe::cpu::Work work;
   std::atomic<unsigned long long> gen{0};  // jobs handed to the workers
-  std::atomic<int> finished{0};            // worker passes over handed jobs
+  std::atomic<unsigned long long> finished{0};  // worker passes over handed jobs
   std::atomic<bool> stop{false};
   std::atomic<bool> paused{false};  // test hook: jobs are left unanswered while set
   std::atomic<unsigned long long> jobs{0}, routes{0}, busy_ns{0};
@@ -382,7 +382,7 @@ bool wait_for(F ready, const std::atomic<bool>& stop) {
 void coordinator(moe_cpu_exec* x) {
   MailHeader* hd = x->hdr();
   unsigned long long last = 0, handed = 0;
-  const int nw = x->n_threads - 1;
+  const unsigned long long nw = (unsigned long long)x->n_threads - 1;
   for (;;) {
     unsigned long long seq = 0;
     if (!wait_for([&] {
@@ -391,7 +391,7 @@ void coordinator(moe_cpu_exec* x) {
         },
                   x->stop))
       return;
-    if (!wait_for([&] { return x->finished.load(std::memory_order_acquire) >= (int)(handed * nw); },
+    if (!wait_for([&] { return x->finished.load(std::memory_order_acquire) >= handed * nw; },
                   x->stop))
       return;
     const auto t0 = std::chrono::steady_clock::now();
