@@ -100,6 +100,7 @@ _SIGS = {
     "moe_hybrid_stop": [_vp],
     "moe_hybrid_counters": [_vp, _vp],
     "moe_hybrid_pause": [_vp, _i],
+    "moe_hybrid_selftest": [_i, _i, _i, _vp, _i, _i, _i, _i, _i, _u, _vp],
     "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
     "moe_last_cuda_error": [],
@@ -246,6 +247,19 @@ def moe_hybrid_stop(cache: int) -> None:
 
 def moe_hybrid_pause(cache: int, paused: bool) -> None:
     _check("moe_hybrid_pause", _lib.moe_hybrid_pause(cache, int(paused)))
+
+
+def moe_hybrid_selftest(wfmt: int, hidden: int, inter: int, blob_ptrs, max_rows: int, k: int,
+                        n_threads: int, n_jobs: int, seed: int = 0) -> int:
+    """Host-only stress test of the executor's job protocol; returns the number
+    of jobs whose answer differed from moe_cpu_experts (see moe_cache.h)."""
+    import numpy as np
+    ptrs = np.ascontiguousarray(np.asarray(blob_ptrs, dtype=np.uint64))
+    bad = C.c_longlong(0)
+    _check("moe_hybrid_selftest", _lib.moe_hybrid_selftest(
+        wfmt, hidden, inter, ptrs.ctypes.data, len(ptrs), max_rows, k, n_threads, n_jobs, seed,
+        C.byref(bad)))
+    return bad.value
 
 
 def moe_hybrid_counters(cache: int) -> dict:

@@ -234,7 +234,7 @@ struct HybridConfig {
   int wfmt, H, I, E, L, max_rows, max_routes, n_threads;
   const void* const* host_blobs;  // [L*E] host addresses of the expert blobs
 };
-int hybrid_start(const HybridConfig& c, moe_cpu_exec** out);  // MOE_OK, MOE_ERR_*, or
+int hybrid_start(const HybridConfig& c, moe_cpu_exec** out, bool host_only = false);  // MOE_OK, MOE_ERR_*, or
                                                                // -1000 - cudaError_t
 void hybrid_stop(moe_cpu_exec* x);
 void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[4]);

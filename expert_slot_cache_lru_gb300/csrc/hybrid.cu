@@ -21,6 +21,7 @@
 // count.
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 #include <chrono>
 #include <cmath>
 #include <cstring>
@@ -339,6 +340,7 @@ struct moe_cpu_exec {
   int wfmt = 0, H = 0, I = 0, E = 0, L = 0, max_rows = 0, max_routes = 0, n_threads = 0;
   std::vector<const uint8_t*> blobs;  // [L*E] host blob addresses
   uint8_t* mb = nullptr;              // mailbox, host address (mapped, pinned)
+  bool host_only = false;             // self-test pool: mailbox in plain host memory, no GPU
   uint8_t* mb_dev = nullptr;          // the same, device address
   moe::MailOff off;
   unsigned long long* d_seq = nullptr;  // device: jobs posted so far
@@ -538,29 +540,40 @@ void hybrid_stop(moe_cpu_exec* x) {
   x->stop.store(true, std::memory_order_relaxed);
   for (std::thread& t : x->threads)
     if (t.joinable()) t.join();
-  if (x->mb) cudaFreeHost(x->mb);
+  if (x->mb && x->host_only) std::free(x->mb);
+  if (x->mb && !x->host_only) cudaFreeHost(x->mb);
   if (x->d_seq) cudaFree(x->d_seq);
   delete x;
 }
 
-int hybrid_start(const HybridConfig& c, moe_cpu_exec** out) {
+int hybrid_start(const HybridConfig& c, moe_cpu_exec** out, bool host_only) {
   moe_cpu_exec* x = new (std::nothrow) moe_cpu_exec();
   if (!x) return MOE_ERR_STATE;
+  x->host_only = host_only;
   x->wfmt = c.wfmt, x->H = c.H, x->I = c.I, x->E = c.E, x->L = c.L;
   x->max_rows = c.max_rows, x->max_routes = c.max_routes, x->n_threads = c.n_threads;
   x->blobs.resize((size_t)c.L * c.E);
   for (size_t i = 0; i < x->blobs.size(); ++i)
     x->blobs[i] = static_cast<const uint8_t*>(c.host_blobs[i]);
   x->off = MailOff(c.max_routes, c.max_rows, c.H);
-  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&x->mb), x->off.bytes, cudaHostAllocMapped);
-  if (e == cudaSuccess) {
+  cudaError_t e = cudaSuccess;
+  if (host_only) {  // no device: the caller plays the GPU's part of the protocol
+    x->mb = static_cast<uint8_t*>(std::aligned_alloc(4096, (x->off.bytes + 4095) / 4096 * 4096));
+    if (!x->mb) {
+      hybrid_stop(x);
+      return MOE_ERR_STATE;
+    }
+    std::memset(x->mb, 0, x->off.bytes);
+  } else if ((e = cudaHostAlloc(reinterpret_cast<void**>(&x->mb), x->off.bytes,
+                                cudaHostAllocMapped)) == cudaSuccess) {
     std::memset(x->mb, 0, x->off.bytes);
     e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&x->mb_dev), x->mb, 0);
   } else {
     x->mb = nullptr;
   }
-  if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&x->d_seq), sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaMemset(x->d_seq, 0, sizeof(unsigned long long));
+  if (e == cudaSuccess && !host_only)
+    e = cudaMalloc(reinterpret_cast<void**>(&x->d_seq), sizeof(unsigned long long));
+  if (e == cudaSuccess && !host_only) e = cudaMemset(x->d_seq, 0, sizeof(unsigned long long));
   if (e != cudaSuccess) {
     hybrid_stop(x);
     return -1000 - (int)e;  // the caller maps this to MOE_ERR_CUDA
@@ -617,6 +630,73 @@ int moe_cpu_experts(int wfmt, int hidden, int inter, const void* const* h_blobs,
   w.run();
   for (std::thread& t : pool) t.join();
   return MOE_OK;
+}
+
+// Host-only self-test of the executor's job protocol: a pool over a mailbox in
+// plain host memory, fed n_jobs random steps (rows, ids with some invalid,
+// slots with about half at -1, weights, x) the way the post kernel feeds it,
+// with a pause now and then; every answer is compared bit for bit with
+// moe_cpu_experts on the same step.  *h_mismatches receives the number of
+// differing output values; MOE_ERR_STATE if a job is not answered in 10 s.
+int moe_hybrid_selftest(int wfmt, int hidden, int inter, const void* const* h_blobs,
+                        int n_experts, int max_rows, int k, int n_threads, int n_jobs,
+                        unsigned seed, long long* h_mismatches) {
+  if (wfmt < MOE_W_BF16 || wfmt > MOE_W_Q4_0 || hidden <= 0 || inter <= 0 || hidden % 32 ||
+      inter % 32 || n_experts <= 0 || !h_blobs || max_rows < 1 || k < 1 || n_threads < 1 ||
+      n_threads > 256 || n_jobs < 0 || !h_mismatches)
+    return MOE_ERR_INVALID_ARG;
+  moe::HybridConfig hc{wfmt, hidden, inter, n_experts, 1, max_rows, max_rows * k, n_threads,
+                       h_blobs};
+  moe_cpu_exec* x = nullptr;
+  int rc = moe::hybrid_start(hc, &x, true);
+  if (rc != MOE_OK) return rc;
+  moe::cpu::MailHeader* hd = x->hdr();
+  auto* ids = reinterpret_cast<int32_t*>(x->mb + x->off.ids);
+  auto* slots = reinterpret_cast<int32_t*>(x->mb + x->off.slots);
+  auto* wts = reinterpret_cast<float*>(x->mb + x->off.w);
+  auto* xin = reinterpret_cast<uint16_t*>(x->mb + x->off.x);
+  const auto* y = reinterpret_cast<const float*>(x->mb + x->off.y);
+  uint64_t r = 0x9E3779B97F4A7C15ull ^ seed;
+  auto rnd = [&] {  // xorshift64*
+    r ^= r >> 12, r ^= r << 25, r ^= r >> 27;
+    return (uint32_t)((r * 0x2545F4914F6CDD1Dull) >> 32);
+  };
+  std::vector<float> ref((size_t)max_rows * hidden);
+  long long bad = 0;
+  for (int j = 1; j <= n_jobs && rc == MOE_OK; ++j) {
+    const int rows = 1 + (int)(rnd() % (unsigned)max_rows);
+    for (int q = 0; q < rows * k; ++q) {
+      ids[q] = rnd() % 16 == 0 ? n_experts + (int)(rnd() % 3) : (int)(rnd() % (unsigned)n_experts);
+      slots[q] = rnd() % 2 ? -1 : (int)(rnd() % 100);
+      wts[q] = (float)(rnd() % 1000) / 1000.f;
+    }
+    for (int i = 0; i < rows * hidden; ++i)  // bf16 values in about [-2, 2)
+      xin[i] = (uint16_t)((rnd() % 2 ? 0xC000u : 0x4000u) - 0x100u + (rnd() % 0x200u));
+    hd->layer = 0, hd->n_rows = rows, hd->k = k;
+    const bool pause = j % 97 == 0;
+    if (pause) moe::hybrid_pause(x, true);
+    __atomic_store_n(&hd->job_seq, (unsigned long long)j, __ATOMIC_RELEASE);
+    if (pause) {
+      std::this_thread::sleep_for(std::chrono::milliseconds(2));
+      if (__atomic_load_n(&hd->done_seq, __ATOMIC_ACQUIRE) == (unsigned long long)j) ++bad;
+      moe::hybrid_pause(x, false);
+    }
+    const auto t0 = std::chrono::steady_clock::now();
+    while (__atomic_load_n(&hd->done_seq, __ATOMIC_ACQUIRE) != (unsigned long long)j) {
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10)) {
+        rc = MOE_ERR_STATE;
+        break;
+      }
+      std::this_thread::yield();
+    }
+    if (rc != MOE_OK) break;
+    moe_cpu_experts(wfmt, hidden, inter, h_blobs, n_experts, xin, ids, slots, wts, rows, k, 1,
+                    ref.data());
+    bad += std::memcmp(ref.data(), y, (size_t)rows * hidden * 4) != 0;
+  }
+  moe::hybrid_stop(x);
+  *h_mismatches = bad;
+  return rc;
 }
 
 }  // extern "C"

@@ -373,6 +373,17 @@ MOE_API int moe_hybrid_counters(moe_cache* c, uint64_t h_out[4]);
  * resuming answers the newest posted job. */
 MOE_API int moe_hybrid_pause(moe_cache* c, int paused);
 
+/* Test hook, host only (no GPU, no cache): the executor's job protocol over a
+ * mailbox in plain host memory.  n_jobs random steps of up to max_rows rows
+ * (some ids invalid, about half the routes at -1, a pause every 97th job) are
+ * posted the way the GPU posts them, and each answer is compared bit for bit
+ * with moe_cpu_experts; *h_mismatches receives the number of differing jobs
+ * (a job answered while paused counts as one).  MOE_ERR_STATE if a job goes
+ * unanswered for 10 s. */
+MOE_API int moe_hybrid_selftest(int wfmt, int hidden, int inter, const void* const* h_blobs,
+                                int n_experts, int max_rows, int k, int n_threads, int n_jobs,
+                                unsigned seed, long long* h_mismatches);
+
 /* The CPU partial above as a plain host function (no GPU, no cache): h_blobs
  * [n_experts] host blob addresses of one layer; h_x bf16 [n_rows][H]; h_ids,
  * h_slot_ids int32 and h_w float [n_rows][k]; h_out float [n_rows][H].  Uses

@@ -108,3 +108,17 @@ def test_argument_checks():
         m.moe_cpu_experts(FMT[w.fmt], w.hidden + 1, w.inter, ptrs, x, ids, slots, wts)
     with pytest.raises(m.MoeError):
         m.moe_cpu_experts(FMT[w.fmt], w.hidden, w.inter, ptrs, x, ids, slots, wts, n_threads=0)
+
+
+@pytest.mark.parametrize("name,threads,jobs", [("bf16_tiny", 4, 3000), ("bf16_tiny", 1, 300),
+                                               ("nvfp4_small", 8, 400), ("q4_0_small", 3, 200)])
+def test_job_protocol_over_host_mailbox(name, threads, jobs):
+    """The executor's coordinator and workers over a mailbox in plain host
+    memory, fed thousands of random steps the way the GPU posts them (a pause
+    every 97th job, which must stay unanswered while paused): every answer
+    equals the direct host math bit for bit and no job is lost."""
+    w = SHAPES[name]
+    blobs = synth.HostBlobs(w, pinned=False)
+    ptrs = [blobs.addr(e) for e in range(w.n_experts)]
+    assert m.moe_hybrid_selftest(FMT[w.fmt], w.hidden, w.inter, ptrs, max_rows=3, k=w.top_k,
+                                 n_threads=threads, n_jobs=jobs, seed=jobs) == 0
