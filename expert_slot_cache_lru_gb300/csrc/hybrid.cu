@@ -387,9 +387,11 @@ void coordinator(moe_cpu_exec* x) {
   const unsigned long long nw = (unsigned long long)x->n_threads - 1;
   for (;;) {
     unsigned long long seq = 0;
+    // the job number first, then the pause flag: a pause set before a job was
+    // posted is then always seen with that job
     if (!wait_for([&] {
-          if (x->paused.load(std::memory_order_relaxed)) return false;
-          return (seq = __atomic_load_n(&hd->job_seq, __ATOMIC_ACQUIRE)) != last;
+          seq = __atomic_load_n(&hd->job_seq, __ATOMIC_ACQUIRE);
+          return seq != last && !x->paused.load(std::memory_order_acquire);
         },
                   x->stop))
       return;
@@ -591,7 +593,7 @@ int hybrid_start(const HybridConfig& c, moe_cpu_exec** out, bool host_only) {
   return MOE_OK;
 }
 
-void hybrid_pause(moe_cpu_exec* x, bool paused) { x->paused.store(paused, std::memory_order_relaxed); }
+void hybrid_pause(moe_cpu_exec* x, bool paused) { x->paused.store(paused, std::memory_order_release); }
 
 void hybrid_counters(const moe_cpu_exec* x, unsigned long long out[4]) {
   out[0] = x->jobs.load(std::memory_order_relaxed);
