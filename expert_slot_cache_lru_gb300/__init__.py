@@ -100,6 +100,7 @@ _SIGS = {
     "moe_hybrid_stop": [_vp],
     "moe_hybrid_counters": [_vp, _vp],
     "moe_hybrid_pause": [_vp, _i],
+    "moe_schedule_trace": [_i, _i, _i, _i, _i, _i, _i, _vp, _i],
     "moe_hybrid_selftest": [_i, _i, _i, _vp, _i, _i, _i, _i, _i, _u, _vp],
     "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
@@ -260,6 +261,16 @@ def moe_hybrid_selftest(wfmt: int, hidden: int, inter: int, blob_ptrs, max_rows:
         wfmt, hidden, inter, ptrs.ctypes.data, len(ptrs), max_rows, k, n_threads, n_jobs, seed,
         C.byref(bad)))
     return bad.value
+
+
+def moe_schedule_trace(one_launch: bool = False, fused: bool = False, overlap: bool = True,
+                       pf: bool = False, shared: bool = False, hybrid: bool = False,
+                       fail_at: int = -1) -> tuple[int, list[str]]:
+    """(return code, ["c:admit", "s:gather_demand", ...]) of a layer plan (see moe_cache.h)."""
+    buf = C.create_string_buffer(4096)
+    rc = _lib.moe_schedule_trace(int(one_launch), int(fused), int(overlap), int(pf), int(shared),
+                                 int(hybrid), fail_at, buf, len(buf))
+    return rc, buf.value.decode().split()
 
 
 def moe_hybrid_counters(cache: int) -> dict:

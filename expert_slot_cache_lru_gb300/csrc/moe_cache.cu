@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <string>
 #include <vector>
 
 #include "common.cuh"
@@ -481,6 +482,164 @@ int moe_routed_experts_noalloc(int wfmt, int hidden, int inter, const void* d_sl
   return MOE_OK;
 }
 
+namespace {
+
+// ---------------------------------------------------------------- layer schedule
+// The work of one decode layer as operations on two streams, and the order
+// they are enqueued in [P2 What we changed, "order inside one layer"; P1
+// section 4 for the hybrid post and add].  The same function drives the CUDA
+// calls (CudaOps) and, for the host-only schedule test, a recorder
+// (moe_schedule_trace).
+enum Op {
+  kOpAdmit, kOpPost, kOpPrefetch, kOpGatherDemand, kOpGatherPrefetch, kOpShared, kOpRouted,
+  kOpAddCpu, kOpLayerAdmit, kOpLayerStream, kOpRecordReady, kOpWaitReady, kOpRecordDone,
+  kOpWaitDone, kOpCount
+};
+const char* const kOpName[kOpCount] = {
+    "admit", "post", "prefetch", "gather_demand", "gather_prefetch", "shared", "routed",
+    "add_cpu", "layer_admit", "layer_stream", "record_ready", "wait_ready", "record_done",
+    "wait_done"};
+enum Str { kCompute = 0, kSide = 1 };
+
+struct LayerOps {
+  virtual int run(Op op, Str s) = 0;  // MOE_OK or an error code
+  virtual ~LayerOps() = default;
+};
+
+struct LayerPlan {
+  bool one_launch;  // the whole layer, admission included, in one launch
+  bool fused;       // the admission, then one launch for the rest
+  bool overlap;     // the gather on the side stream, forked and joined by events
+  bool pf, shared, hybrid;
+};
+
+int schedule_layer(const LayerPlan& p, LayerOps& ops) {
+  int rc;
+  if (p.one_launch) return ops.run(kOpLayerAdmit, kCompute);
+  if ((rc = ops.run(kOpAdmit, kCompute))) return rc;
+  if (p.hybrid && (rc = ops.run(kOpPost, kCompute))) return rc;
+  if (p.pf && (rc = ops.run(kOpPrefetch, kCompute))) return rc;
+  if (p.fused) {
+    if ((rc = ops.run(kOpLayerStream, kCompute))) return rc;
+    return p.hybrid ? ops.run(kOpAddCpu, kCompute) : MOE_OK;
+  }
+  if (!p.overlap) {
+    if ((rc = ops.run(kOpGatherDemand, kCompute))) return rc;
+    if (p.shared && (rc = ops.run(kOpShared, kCompute))) return rc;
+    if ((rc = ops.run(kOpRouted, kCompute))) return rc;
+    if (p.pf && (rc = ops.run(kOpGatherPrefetch, kCompute))) return rc;
+    return p.hybrid ? ops.run(kOpAddCpu, kCompute) : MOE_OK;
+  }
+  // fork: the side stream waits for the admission, gathers, and records done
+  if ((rc = ops.run(kOpRecordReady, kCompute))) return rc;
+  if ((rc = ops.run(kOpWaitReady, kSide))) return rc;
+  int side = ops.run(kOpGatherDemand, kSide);
+  const int rec = ops.run(kOpRecordDone, kSide);
+  if (side == MOE_OK && p.pf) side = ops.run(kOpGatherPrefetch, kSide);
+  int shared = MOE_OK;
+  if (side == MOE_OK && rec == MOE_OK && p.shared) shared = ops.run(kOpShared, kCompute);
+  // join, on every path once forked (a capture must not end with an unjoined fork)
+  const int join = rec == MOE_OK ? ops.run(kOpWaitDone, kCompute) : rec;
+  if (side != MOE_OK) return side;
+  if (join != MOE_OK) return join;
+  if (shared != MOE_OK) return shared;
+  if ((rc = ops.run(kOpRouted, kCompute))) return rc;
+  return p.hybrid ? ops.run(kOpAddCpu, kCompute) : MOE_OK;
+}
+
+// The operations as CUDA work on the two streams.
+struct CudaOps : LayerOps {
+  moe_cache* c;
+  int layer;
+  const void* d_x;
+  const int32_t* d_ids;
+  const float* d_w;
+  int32_t* d_slot_ids;
+  int n_rows, k, fetch_cap;
+  const int32_t* d_pred;
+  int n_pred;
+  const void* d_shared_blob;
+  const void* d_shared_gate;
+  void* d_out;
+  cudaStream_t cs, ss;
+  int32_t* pf_plan;
+
+  int run(Op op, Str s) override {
+    const cudaStream_t st = s == kSide ? ss : cs;
+    const moe_cache_desc& dd = c->d;
+    const bool pf = d_pred && n_pred > 0;
+    switch (op) {
+      case kOpAdmit:
+        CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, n_rows * k, fetch_cap, st));
+        return MOE_OK;
+      case kOpPost:
+        CK(moe::hybrid_post(c->cpu, layer, d_ids, d_slot_ids, d_w, d_x, n_rows, k, st));
+        return MOE_OK;
+      case kOpPrefetch:
+        CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, st));
+        c->last_pf_layer = layer + 1;
+        return MOE_OK;
+      case kOpGatherDemand:
+        CK(moe::launch_gather(c->st, c->st.plan_demand, c->gather_grid, st));
+        return MOE_OK;
+      case kOpGatherPrefetch:
+        CK(moe::launch_gather(c->st, pf_plan, c->gather_grid, st));
+        return MOE_OK;
+      case kOpShared:
+        return run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, st);
+      case kOpRouted:
+        return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr,
+                          d_out, st);
+      case kOpAddCpu:
+        CK(moe::hybrid_add(c->cpu, d_out, n_rows, c->st.status, st));
+        return MOE_OK;
+      case kOpLayerAdmit:
+        CK(moe::launch_layer_admit(c->st, dd.wfmt, dd.hidden, dd.inter, layer, d_x, d_ids,
+                                   d_slot_ids, d_w, n_rows, k, fetch_cap, pf ? d_pred : nullptr,
+                                   n_pred, static_cast<const uint8_t*>(d_shared_blob),
+                                   d_shared_gate, pf ? pf_plan : nullptr, d_out, c->sc,
+                                   c->st.status, st));
+        if (pf) c->last_pf_layer = layer + 1;
+        return MOE_OK;
+      case kOpLayerStream:
+        CK(moe::launch_layer_stream(c->st, dd.wfmt, dd.hidden, dd.inter, layer, d_x, d_slot_ids,
+                                    d_w, n_rows, k, static_cast<const uint8_t*>(d_shared_blob),
+                                    d_shared_gate, c->st.plan_demand, pf ? pf_plan : nullptr,
+                                    d_out, c->sc, c->st.status, st));
+        return MOE_OK;
+      case kOpRecordReady:
+        CK(cudaEventRecord(c->ev_ready, st));
+        return MOE_OK;
+      case kOpWaitReady:
+        CK(cudaStreamWaitEvent(st, c->ev_ready, 0));
+        return MOE_OK;
+      case kOpRecordDone:
+        CK(cudaEventRecord(c->ev_done, st));
+        return MOE_OK;
+      case kOpWaitDone:
+        CK(cudaStreamWaitEvent(st, c->ev_done, 0));
+        return MOE_OK;
+      default:
+        return MOE_ERR_INVALID_ARG;
+    }
+  }
+};
+
+// The recorder of the host-only schedule test: "c:op" / "s:op" tokens, and an
+// optional operation index that fails.
+struct TraceOps : LayerOps {
+  std::string out;
+  int n = 0, fail_at = -1;
+  int run(Op op, Str s) override {
+    out += (s == kSide ? "s:" : "c:");
+    out += kOpName[op];
+    out += ' ';
+    return n++ == fail_at ? MOE_ERR_CUDA : MOE_OK;
+  }
+};
+
+}  // namespace
+
 int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,
                      const float* d_w, int32_t* d_slot_ids, int n_rows, int k, int fetch_cap,
                      const int32_t* d_pred, int n_pred, const void* d_shared_blob,
@@ -494,86 +653,41 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
   const bool pf = d_pred && n_pred > 0;
   if (pf && (layer + 1 >= c->d.n_layers || c->d.max_pred == 0)) return MOE_ERR_INVALID_ARG;
   if (pf && n_pred > c->d.max_pred) return MOE_ERR_CAPACITY;
-  const bool overlap = (flags & MOE_OVERLAP) != 0;
-  const bool hybrid = (flags & MOE_HYBRID) != 0;
-  if (hybrid && !c->cpu) return MOE_ERR_STATE;
-  cudaStream_t cs = as_stream(compute_stream), ss = as_stream(side_stream);
-  // hybrid [P1 section 4]: the step goes to the host right after the
-  // admission, and the host's partial is added after the GPU's combine
-  auto post = [&]() -> cudaError_t {
-    return hybrid ? moe::hybrid_post(c->cpu, layer, d_ids, d_slot_ids, d_w, d_x, n_rows, k, cs)
-                  : cudaSuccess;
-  };
-  auto add_cpu = [&]() -> int {
-    if (hybrid) CK(moe::hybrid_add(c->cpu, d_out, n_rows, c->st.status, cs));
-    return MOE_OK;
-  };
+  LayerPlan p{};
+  p.overlap = (flags & MOE_OVERLAP) != 0;
+  p.hybrid = (flags & MOE_HYBRID) != 0;
+  p.pf = pf;
+  p.shared = d_shared_blob != nullptr;
+  if (p.hybrid && !c->cpu) return MOE_ERR_STATE;
   const moe_cache_desc& dd = c->d;
-  const bool fused = (flags & MOE_FUSED) && c->stream_ffn && dd.slot_bytes > 0 &&
-                     (!d_shared_blob || dd.shared_inter == dd.inter) &&
-                     moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k,
-                                                 d_shared_blob != nullptr);
-  if (fused && !hybrid && moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k,
-                                         d_shared_blob != nullptr)) {
-    // one launch for the whole layer: admission (and prefetch admission) in
-    // CTA 0, gathers + shared expert + routed experts in the others
-    int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
-    CK(moe::launch_layer_admit(c->st, dd.wfmt, dd.hidden, dd.inter, layer, d_x, d_ids, d_slot_ids,
-                               d_w, n_rows, k, fetch_cap, pf ? d_pred : nullptr, n_pred,
-                               static_cast<const uint8_t*>(d_shared_blob), d_shared_gate,
-                               pf ? pf_plan : nullptr, d_out, c->sc, c->st.status, cs));
-    if (pf) c->last_pf_layer = layer + 1;
-    return MOE_OK;
-  }
-  if (fused) {  // admission, then one launch: gathers + shared expert + routed experts
-    CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
-    CK(post());
-    int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
-    if (pf) {
-      CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, cs));
-      c->last_pf_layer = layer + 1;
-    }
-    CK(moe::launch_layer_stream(c->st, dd.wfmt, dd.hidden, dd.inter, layer, d_x, d_slot_ids, d_w,
-                                n_rows, k, static_cast<const uint8_t*>(d_shared_blob),
-                                d_shared_gate, c->st.plan_demand, pf ? pf_plan : nullptr, d_out,
-                                c->sc, c->st.status, cs));
-    return add_cpu();
-  }
-  if (overlap && !side_stream) return MOE_ERR_INVALID_ARG;
+  p.fused = (flags & MOE_FUSED) && c->stream_ffn && dd.slot_bytes > 0 &&
+            (!d_shared_blob || dd.shared_inter == dd.inter) &&
+            moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k, p.shared);
+  // the hybrid post must follow the admission, so a hybrid layer keeps it as
+  // its own launch
+  p.one_launch = p.fused && !p.hybrid &&
+                 moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k, p.shared);
+  if (!p.fused && p.overlap && !side_stream) return MOE_ERR_INVALID_ARG;
+  CudaOps ops;
+  ops.c = c, ops.layer = layer, ops.d_x = d_x, ops.d_ids = d_ids, ops.d_w = d_w;
+  ops.d_slot_ids = d_slot_ids, ops.n_rows = n_rows, ops.k = k, ops.fetch_cap = fetch_cap;
+  ops.d_pred = d_pred, ops.n_pred = n_pred, ops.d_shared_blob = d_shared_blob;
+  ops.d_shared_gate = d_shared_gate, ops.d_out = d_out;
+  ops.cs = as_stream(compute_stream), ops.ss = as_stream(side_stream);
+  ops.pf_plan = c->st.plan_pf[(layer + 1) & 1];
+  return schedule_layer(p, ops);
+}
 
-  CK(moe::launch_admit(c->st, layer, d_ids, d_slot_ids, R, fetch_cap, cs));
-  CK(post());
-  int32_t* pf_plan = c->st.plan_pf[(layer + 1) & 1];
-  if (pf) {
-    CK(moe::launch_prefetch(c->st, layer + 1, d_pred, n_pred, pf_plan, cs));
-    c->last_pf_layer = layer + 1;
-  }
-  if (!overlap) {
-    CK(moe::launch_gather(c->st, c->st.plan_demand, c->gather_grid, cs));
-    if (d_shared_blob && (rc = run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, cs))) return rc;
-    if ((rc = run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out, cs)))
-      return rc;
-    if (pf) CK(moe::launch_gather(c->st, pf_plan, c->gather_grid, cs));
-    return add_cpu();
-  }
-  // fork
-  CK(cudaEventRecord(c->ev_ready, cs));
-  CK(cudaStreamWaitEvent(ss, c->ev_ready, 0));
-  cudaError_t side_err = moe::launch_gather(c->st, c->st.plan_demand, c->gather_grid, ss);
-  cudaError_t rec = cudaEventRecord(c->ev_done, ss);
-  if (side_err == cudaSuccess && pf) side_err = moe::launch_gather(c->st, pf_plan, c->gather_grid, ss);
-  int shared_rc = MOE_OK;
-  if (side_err == cudaSuccess && rec == cudaSuccess && d_shared_blob)
-    shared_rc = run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, cs);
-  // join, on every path once forked
-  cudaError_t join = rec == cudaSuccess ? cudaStreamWaitEvent(cs, c->ev_done, 0) : rec;
-  if (side_err != cudaSuccess) return cuda_fail(side_err, "gather (side stream)");
-  if (join != cudaSuccess) return cuda_fail(join, "join");
-  if (shared_rc != MOE_OK) return shared_rc;
-  if ((rc = run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out,
-                       cs)))
-    return rc;
-  return add_cpu();
+int moe_schedule_trace(int one_launch, int fused, int overlap, int pf, int shared, int hybrid,
+                       int fail_at, char* h_out, int cap) {
+  if (!h_out || cap < 1) return MOE_ERR_INVALID_ARG;
+  LayerPlan p{one_launch != 0, fused != 0, overlap != 0, pf != 0, shared != 0, hybrid != 0};
+  TraceOps ops;
+  ops.fail_at = fail_at;
+  const int rc = schedule_layer(p, ops);
+  if ((int)ops.out.size() >= cap) return MOE_ERR_CAPACITY;
+  std::memcpy(h_out, ops.out.c_str(), ops.out.size() + 1);
+  return rc;
 }
 
 int moe_hybrid_start(moe_cache* c, int n_threads) {

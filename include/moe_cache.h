@@ -393,6 +393,17 @@ MOE_API int moe_cpu_experts(int wfmt, int hidden, int inter, const void* const* 
                             const int32_t* h_slot_ids, const float* h_w, int n_rows, int k,
                             int n_threads, float* h_out);
 
+/* Test hook, host only: the operations moe_decode_layer enqueues for a layer
+ * plan, in order, as "c:op" (compute stream) / "s:op" (side stream) tokens
+ * separated by spaces, written to h_out (cap bytes).  The ops are admit, post,
+ * prefetch, gather_demand, gather_prefetch, shared, routed, add_cpu,
+ * layer_admit, layer_stream, record_ready, wait_ready, record_done and
+ * wait_done.  The fork/join events are ready and done.  fail_at >= 0 makes the
+ * fail_at-th operation fail with MOE_ERR_CUDA, and the call returns the code
+ * the layer would.  MOE_ERR_CAPACITY if the trace does not fit. */
+MOE_API int moe_schedule_trace(int one_launch, int fused, int overlap, int pf, int shared,
+                               int hybrid, int fail_at, char* h_out, int cap);
+
 /* Copy one layer's counters to the host.  Synchronises the device. */
 MOE_API int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out);
 
