@@ -459,6 +459,45 @@ def test_one_weight_expert_closed_form():
     assert np.count_nonzero(y) == 1
 
 
+def _set_code(blob, bank_off, row, k, cols, code):
+    """Put a 4-bit code at element (row, k) of a code bank (even element in the low nibble)."""
+    i = bank_off + row * (cols // 2) + k // 2
+    blob[i] = (blob[i] & 0xF0) | code if k % 2 == 0 else (blob[i] & 0x0F) | (code << 4)
+
+
+@pytest.mark.parametrize("fmt", [synth.FMT_MXFP4, synth.FMT_Q4_0])
+def test_one_weight_expert_closed_form_4bit_formats(fmt):
+    """Only Wg[2,5] = 0.75, Wu[2,5] = -1.5 and Wd[7,2] = 2 are nonzero, spelled
+    in the format's own codes and block scales: y[7] = 2 silu(0.75 x5) (-1.5 x5)."""
+    H, I = 64, 64
+    blob = np.zeros(synth.blob_bytes(fmt, H, I), np.uint8)
+    if fmt == synth.FMT_MXFP4:
+        o = synth.mxfp4_banks(H, I)  # codes 0 are +0; scales E8M0
+        blob[o["scale"][0]:o["end"]] = 127
+        _set_code(blob, o["code"][0], 2, 5, H, 0x3)        # e2m1 1.5, block scale 2^-1
+        blob[o["scale"][0] + 2 * (H // 32) + 0] = 126
+        _set_code(blob, o["code"][1], 2, 5, H, 0x8 | 0x3)  # -1.5, scale 1
+        _set_code(blob, o["code"][2], 7, 2, I, 0x4)        # 2.0, scale 1
+    else:
+        o = synth.q4_banks(H, I)  # code 8 is zero; scales fp16 d
+        blob[:o["scale"][0]] = 0x88
+        d = np.full((o["end"] - o["scale"][0]) // 2, 0.5, np.float16)
+        blob[o["scale"][0]:o["end"]] = d.view(np.uint8)
+        _set_code(blob, o["code"][0], 2, 5, H, 8 + 3)      # 0.25 * 3 below
+        blob[o["scale"][0] + 2 * (2 * (H // 32)):][:2] = np.array([0.25], np.float16).view(np.uint8)
+        _set_code(blob, o["code"][1], 2, 5, H, 8 - 3)      # 0.5 * -3
+        _set_code(blob, o["code"][2], 7, 2, I, 8 + 4)      # 0.5 * 4
+    W = [oracle.dequant(fmt, blob, H, I, m_) for m_ in range(3)]
+    assert W[0][2, 5] == 0.75 and W[1][2, 5] == -1.5 and W[2][7, 2] == 2.0
+    assert [np.count_nonzero(w_) for w_ in W] == [1, 1, 1]
+    x = np.zeros(H, np.float32)
+    x[5] = 1.25
+    y = oracle.expert_ffn(fmt, blob, H, I, synth.to_bf16_bits(x))
+    g = 0.75 * 1.25
+    assert y[7] == pytest.approx(2.0 * (g / (1 + math.exp(-g))) * (-1.5 * 1.25), rel=1e-15)
+    assert np.count_nonzero(y) == 1
+
+
 def test_layer_zero_input_and_masks():
     w = synth.scaled(synth.workloads()["tiny"], shared_inter=64)
     blobs = synth.HostBlobs(w, pinned=False)
