@@ -41,3 +41,26 @@ def test_blob_sizes():
     assert synth.blob_bytes(synth.FMT_BF16, 4096, 1024) == 25165824
     for fmt, H, I in [(0, 64, 128), (1, 2048, 512), (1, 2048, 768), (0, 4096, 1024)]:
         assert oracle.blob_bytes(fmt, H, I) == synth.blob_bytes(fmt, H, I)
+
+
+def test_4bit_format_blobs_are_deterministic_and_in_range():
+    """MXFP4 and Q4_0 blobs: sizes agree with the oracle, the same key gives the
+    same bytes, and the scales stay in the recipe's ranges (E8M0 118..121;
+    fp16 d in [0.001, 0.005))."""
+    H, I = 2048, 512
+    assert synth.blob_bytes(synth.FMT_MXFP4, H, I) == 3 * H * I // 2 + 3 * H * I // 32
+    assert synth.blob_bytes(synth.FMT_Q4_0, H, I) == 3 * H * I // 2 + 3 * H * I // 16
+    for fmt, banks in ((synth.FMT_MXFP4, synth.mxfp4_banks), (synth.FMT_Q4_0, synth.q4_banks)):
+        assert oracle.blob_bytes(fmt, H, I) == synth.blob_bytes(fmt, H, I)
+        a = np.empty(synth.blob_bytes(fmt, H, I), np.uint8)
+        b = np.empty_like(a)
+        synth.fill_blob(a, fmt, H, I, synth.Rng(3, 7))
+        synth.fill_blob(b, fmt, H, I, synth.Rng(3, 7))
+        assert np.array_equal(a, b)
+        o = banks(H, I)
+        sc = a[o["scale"][0]:o["end"]]
+        if fmt == synth.FMT_MXFP4:
+            assert sc.min() >= 118 and sc.max() <= 121
+        else:
+            d = sc.view(np.float16).astype(np.float64)
+            assert d.min() >= 0.001 * (1 - 2 ** -10) and d.max() < 0.005 * (1 + 2 ** -10)
