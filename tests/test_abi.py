@@ -83,7 +83,7 @@ def test_host_side_validation(m):
         dict(max_pred=4, n_slots=0),                      # prefetch needs a cache
         dict(hidden=48, inter=64, slot_bytes=6 * 48 * 64),  # H not a multiple of 32
         dict(hidden=64, inter=64, slot_bytes=123),         # slot_bytes != blob size
-        dict(hidden=64, inter=64, wfmt=3, slot_bytes=6 * 64 * 64),
+        dict(hidden=64, inter=64, wfmt=7, slot_bytes=6 * 64 * 64),  # no such format
         dict(slot_bytes=64),                               # storage without pointers
     ]
     for kw in bad:
