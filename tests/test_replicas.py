@@ -79,3 +79,27 @@ def test_reference_arm_rank0_prints_one_line():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 1
+
+
+def test_routed_traffic_only_for_the_captured_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu record that carries the hash
+    of the kernel source it was captured from; once the source changes the
+    figure must be withheld (None), not reused."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "kernel.cu"
+    src.write_text("// one version of the kernel\n")
+    rec = tmp_path / "traffic.txt"
+    rec.write_text("# comment\ndram_bytes_per_launch=1234\n"
+                   f"source_sha256_16={bench.source_hash(str(src))}\n")
+    monkeypatch.setattr(bench, "FFN_SOURCE", str(src))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(rec))
+    got = bench.routed_traffic()
+    assert got is not None and got["bytes_per_launch"] == 1234.0
+    src.write_text("// another version of the kernel\n")
+    assert bench.routed_traffic() is None
+    rec.unlink()
+    assert bench.routed_traffic() is None
+    # the committed record matches the committed kernel source
+    monkeypatch.undo()
+    assert bench.routed_traffic() is not None
