@@ -516,14 +516,16 @@ namespace {
 // three fp32 per-matrix global scales padded to 16 bytes.  Gate and up are
 // [I, H], down is [H, I].  bf16: gate, up, down, row-major.
 // MXFP4 (OCP Microscaling: MXFP4 blocks of 32 e2m1 elements sharing one
-// E8M0 scale): the same three code banks, then the gate, up, down E8M0 scales
+// E8M0 scale; FreeToken PR #491, section 7, names MXFP4 among the expert
+// formats): the same three code banks, then the gate, up, down E8M0 scales
 // (one per 32 consecutive elements of a row); no global scale.
 struct Layout {
   uint64_t code[3], scale[3], glob, total;
 };
 // Q4_0 arithmetic (blocks of 32 weights sharing an fp16 scale d, weight =
-// d * (q - 8) for the 4-bit unsigned code q), laid out in banks like the fp4
-// formats: gate, up, down codes (two per byte, the even element in the low
+// d * (q - 8) for the 4-bit unsigned code q) -- FreeToken PR #491, section 7
+// ("What did not change"), names Q4_0 among the expert formats -- laid out in
+// banks like the fp4 formats: gate, up, down codes (two per byte, the even element in the low
 // nibble), then gate, up, down fp16 scales (one per 32 consecutive elements
 // of a row), padded to 16 bytes.
 Layout q4_layout(int H, int I) {
