@@ -96,6 +96,36 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "_source": "fallback"}
 
 
+def host_numa(addr: int, dev: int) -> dict:
+    """Where the pinned host blobs live and which node the GPU hangs off:
+    the NUMA nodes the host shows, the GPU's PCI numa_node, and the per-node
+    page counts of the memory mapping that holds `addr` (/proc/self/numa_maps)."""
+    out = {}
+    try:
+        out["host_nodes"] = sorted(n for n in os.listdir("/sys/devices/system/node")
+                                   if n.startswith("node"))
+    except OSError:
+        out["host_nodes"] = None
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        bus = (f"{getattr(p, 'pci_domain_id', 0):04x}:{getattr(p, 'pci_bus_id', 0):02x}:"
+               f"{getattr(p, 'pci_device_id', 0):02x}.0")
+        out["gpu_numa_node"] = int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read())
+    except Exception:
+        out["gpu_numa_node"] = None
+    try:
+        for line in open("/proc/self/numa_maps"):
+            f = line.split()
+            if f and int(f[0], 16) <= addr:
+                best = f
+        out["blob_mapping"] = " ".join(x for x in best[1:] if x.startswith(("N", "default", "bind",
+                                                                            "interleave", "prefer")))
+    except Exception:
+        out["blob_mapping"] = None
+    return out
+
+
 class ClockSampler:
     """SM clock and clock-event reasons sampled through NVML (read-only)."""
 
@@ -263,6 +293,47 @@ class Decode:
         self.cs.synchronize()
         self.t += 1
 
+    def totals(self) -> dict:
+        """Statistics summed over the layers (synchronises the device)."""
+        tot = {}
+        for layer in range(self.w.n_layers):
+            for k, v in self.cache.stats(layer).items():
+                tot[k] = tot.get(k, 0) + v
+        return tot
+
+    def layer_kernel_roofline(self, t_first: int, steps: int, ms: float, timed: dict,
+                              hbm_gbs: float, gather_peak=None) -> dict:
+        """The decode's own kernel (one launch per layer: admission, miss
+        staging, shared and routed experts, combine), from the timed region:
+        its average launch time is the timed region over steps x layers (the
+        graph holds nothing else).  HBM algorithmic bytes per launch: each
+        step's distinct experts' blobs (the misses read back from staging),
+        the shared expert's blob, activations and ids; host-link bytes: the
+        misses' blobs."""
+        w = self.w
+        L = w.n_layers
+        ids = self.d_ids.cpu().numpy()
+        hbm_bytes = 0
+        for i in range(steps):
+            t = (t_first + i) % self.T
+            for layer in range(L):
+                nd = len(set(int(v) for v in ids[t, layer] if 0 <= v < w.n_experts))
+                hbm_bytes += ((nd + (1 if w.shared_inter else 0)) * w.blob_bytes +
+                              w.batch * w.hidden * 2 * 2 + w.routes * 12)
+        launches = steps * L
+        per_launch_s = ms * 1e-3 / launches
+        hbm_per = hbm_bytes / launches
+        host_per = timed["fetched"] / L * w.blob_bytes
+        return {"kernel": "ffn_fused_kernel<NVFP4, layerAdmit> (moe_decode_layer, MOE_FUSED: "
+                          "the whole layer in one launch)",
+                "bound": "hbm", "launches": launches, "avg_launch_us": round(per_launch_s * 1e6, 3),
+                "bytes_per_launch": round(hbm_per), "achieved": round(hbm_per / per_launch_s / 1e9, 1),
+                "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(hbm_per / per_launch_s / 1e9 / hbm_gbs, 4),
+                "host_link": {"bytes_per_launch": round(host_per),
+                              "achieved": round(host_per / per_launch_s / 1e9, 1),
+                              "unit": "GB/s", "peak": gather_peak, "frac": None}}
+
     def h2d_bytes(self) -> int:
         return (self.b_ids.numel() * 4 + self.b_w.numel() * 4 + self.b_x.numel() * 2)
 
@@ -382,7 +453,31 @@ class Decode:
             self.cs.synchronize()
             ce.append(e0.elapsed_time(e1))
         res["copy_engine_gbs_1GiB"] = big / (min(ce) * 1e-3) / 1e9
+        # four 256 MiB copies on four streams at once, from four regions of the blobs
+        streams = [torch.cuda.Stream() for _ in range(4)]
+        part = big // 4
+        ce = []
+        for _ in range(3):
+            self.cs.synchronize()
+            with torch.cuda.stream(self.cs):
+                e0.record(self.cs)
+            for i, st in enumerate(streams):
+                st.wait_event(e0)
+                with torch.cuda.stream(st):
+                    self.storage[i * part:(i + 1) * part].copy_(
+                        self.blobs.buf[(2 * i + 1) * part:(2 * i + 2) * part], non_blocking=True)
+            for st in streams:
+                ev = torch.cuda.Event()
+                ev.record(st)
+                self.cs.wait_event(ev)
+            with torch.cuda.stream(self.cs):
+                e1.record(self.cs)
+            self.cs.synchronize()
+            ce.append(e0.elapsed_time(e1))
+        res["copy_engine_gbs_4_streams_1GiB"] = big / (min(ce) * 1e-3) / 1e9
+        res["numa"] = host_numa(self.blobs.buf.data_ptr(), self.torch.cuda.current_device())
         res["host_link_peak_gbs"] = max(res["copy_engine_gbs_1GiB"],
+                                        res["copy_engine_gbs_4_streams_1GiB"],
                                         res["sm_gather_gbs_28_experts"])
         res["frac_of_host_link_peak"] = res["sm_gather_gbs_28_experts"] / res["host_link_peak_gbs"]
         return res
@@ -431,6 +526,108 @@ def admission_sweep(dev: int) -> dict:
             meds.append(e0.elapsed_time(e1) * 1e3 / (48 * 40))
         res[str(R)] = round(statistics.median(meds), 3)
     cache.close()
+    return res
+
+
+def _admission_inputs(name: str, tokens: int):
+    """(workload, ids [T, L, R], predictions [T, L, n_pred] or None) of a
+    workload's first tokens."""
+    import synth
+    w = synth.workloads()[name]
+    ids, _ = synth.make_routing(w, steps=tokens)
+    ids = ids.reshape(tokens, w.n_layers, -1).astype(np.int32)
+    pred = None
+    if w.n_pred:
+        pred = np.zeros((tokens, w.n_layers, w.n_pred), np.int32)
+        for t in range(tokens):
+            for l in range(w.n_layers - 1):
+                pred[t, l] = synth.make_predictions(w, ids[t, l + 1], t, l)
+    return w, ids, pred
+
+
+ADMISSION_CASES = {"tiny": 64, "hybrid_prefetch": 8}  # workload -> tokens timed
+
+
+def admission_small(dev: int) -> dict:
+    """GPU admission on the tiny workload (1 layer, 16 experts, 6 slots, top-2,
+    64 steps) and the hybrid one (48 layers, 1,024 slots, fetch cap 4, plus the
+    look-ahead prefetch of 8 ids for the next layer), as the workloads' first
+    tokens captured in one CUDA graph of admissions (and prefetches) on an
+    admission-only cache.  The graph is replayed 5 times (the cache state
+    carries over), each replay timed with CUDA events; median µs per call."""
+    import torch
+
+    import expert_slot_cache_lru_gb300 as m
+    res = {}
+    for name, tokens in ADMISSION_CASES.items():
+        w, ids, pred = _admission_inputs(name, tokens)
+        L, R = w.n_layers, ids.shape[2]
+        cache = m.SlotCache(n_layers=L, n_experts=w.n_experts, n_slots=w.n_slots,
+                            pool_mode=m.MOE_POOL_SHARED, max_routes=R, max_rows=w.batch,
+                            max_pred=w.n_pred)
+        d_ids = torch.from_numpy(ids).cuda()
+        d_out = torch.empty_like(d_ids)
+        d_pred = torch.from_numpy(pred).cuda() if pred is not None else None
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        calls = 0
+        with torch.cuda.graph(g, stream=s):
+            for t in range(tokens):
+                for l in range(L):
+                    m.moe_admit(cache.handle, l, d_ids[t, l], d_out[t, l], R, w.fetch_cap, s)
+                    calls += 1
+                    if d_pred is not None and l + 1 < L:
+                        m.moe_prefetch(cache.handle, l + 1, d_pred[t, l], w.n_pred, s)
+                        calls += 1
+        times = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+            s.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / calls)
+        res[name] = {"calls_per_graph": calls, "us_per_call": round(statistics.median(times), 3)}
+        del g
+        cache.close()
+    return res
+
+
+def admission_oracle(seconds: float = 6.0) -> dict:
+    """The oracle's admission (single-threaded, the caller's thread) on the
+    same inputs as admission_small and admission_sweep: µs per call."""
+    import oracle
+    import synth
+    res = {}
+    for name, tokens in ADMISSION_CASES.items():
+        w, ids, pred = _admission_inputs(name, tokens)
+        oc = oracle.OracleCache(w.n_layers, w.n_experts, w.n_slots)
+        calls, t0 = 0, time.perf_counter()
+        for t in range(tokens):
+            for l in range(w.n_layers):
+                oc.admit(l, ids[t, l], w.fetch_cap)
+                calls += 1
+                if pred is not None and l + 1 < w.n_layers:
+                    oc.prefetch(l + 1, pred[t, l])
+                    calls += 1
+        res[name] = {"calls": calls, "us_per_call": round((time.perf_counter() - t0) * 1e6 / calls, 2)}
+    w = synth.workloads()["wide_admission"]
+    pre = synth.prefill_ids(w)
+    for batch in (1, 128):
+        oc = oracle.OracleCache(w.n_layers, w.n_experts, w.n_slots, per_layer=True)
+        for layer in range(w.n_layers):
+            oc.prefill(layer, pre)
+        ids = synth.uniform_ids(w, batch, salt=batch)
+        calls, t0 = 0, time.perf_counter()
+        while True:
+            for layer in range(w.n_layers):
+                oc.admit(layer, ids[layer])
+                calls += 1
+            if time.perf_counter() - t0 > seconds / 4:
+                break
+        res[f"wide_admission_{ids.shape[1]}_routes"] = {
+            "calls": calls, "us_per_call": round((time.perf_counter() - t0) * 1e6 / calls, 2)}
     return res
 
 
@@ -612,9 +809,27 @@ def hybrid_step(dev: int, warm: int = 4, tokens: int = 8) -> dict:
 
 
 def cpu_baseline(seconds: float = 15.0) -> dict:
-    """The oracle as it stands, single-threaded on this host: admission plus
+    """The oracle as it stands, single-threaded on one host core (the process
+    is pinned to one CPU with sched_setaffinity while it runs): admission plus
     fp64 layer math for as many layers of the benchmark's tokens as fit in
-    ~`seconds`, extrapolated to tokens/s (40 layers per token)."""
+    ~`seconds`, extrapolated to tokens/s (40 layers per token); then the
+    oracle's µs per admission on the tiny, hybrid and wide-admission inputs.
+    Reports the host's core count beside it."""
+    prev = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    cpu = min(prev) if prev else None
+    if prev:
+        os.sched_setaffinity(0, {cpu})
+    try:
+        res = _cpu_baseline(seconds)
+    finally:
+        if prev:
+            os.sched_setaffinity(0, prev)
+    res["pinned_cpu"] = cpu
+    res["host_cores"] = os.cpu_count()
+    return res
+
+
+def _cpu_baseline(seconds: float) -> dict:
     import oracle
     import synth
     w = synth.workloads()[WORKLOAD]
@@ -654,10 +869,12 @@ def cpu_baseline(seconds: float = 15.0) -> dict:
                 break
         t += 1
     tok_s = layers_done / w.n_layers / elapsed
+    adm = admission_oracle()
     return {"value": tok_s, "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": f"{layers_done} layers (admission + fp64 dequantised layer math, "
                       f"shared expert included) of the first tokens, {elapsed:.1f} s of CPU, "
-                      f"extrapolated at 40 layers per token"}
+                      f"extrapolated at 40 layers per token",
+            "admission_us_per_call": adm}
 
 
 def run_native(args) -> None:
@@ -668,6 +885,7 @@ def run_native(args) -> None:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo",
                                 device_id=torch.device("cuda", local))
     peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
     if args.wide_only:  # profiler runs: the wide decode step alone
         if rank == 0:
             print(json.dumps({"wide_only": True, **wide_step(local)}), flush=True)
@@ -701,6 +919,8 @@ def run_native(args) -> None:
 
     barrier()
     torch.cuda.synchronize()
+    st0 = dec.totals()
+    t_first = dec.t
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     bus = (f"{getattr(props, 'pci_domain_id', 0):08x}:{getattr(props, 'pci_bus_id', 0):02x}:"
            f"{getattr(props, 'pci_device_id', 0):02x}.0")
@@ -714,7 +934,10 @@ def run_native(args) -> None:
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
     barrier()
-    tok_s, max_s = replica_rate(e0.elapsed_time(e1) * 1e-3, args.steps, ws, "cuda")
+    st1 = dec.totals()
+    timed = {k: (st1[k] - st0[k]) / args.steps for k in st0}
+    local_ms = e0.elapsed_time(e1)
+    tok_s, max_s = replica_rate(local_ms * 1e-3, args.steps, ws, "cuda")
     ms = max_s * 1e3
     if args.routed_only:  # profiler runs: the routed FFN kernel's roofline graph only
         if rank == 0:
@@ -725,6 +948,7 @@ def run_native(args) -> None:
         if rank == 0:
             print(json.dumps({"decode_only": True, "layers": L, "slots": dec.w.n_slots,
                               "settle_tokens": settle_tokens,
+                              "misses_per_token": round(timed["misses"], 2),
                               "tok_s": round(tok_s, 2), "ms_per_step": round(ms / args.steps, 4)}),
                   flush=True)
         return
@@ -739,12 +963,17 @@ def run_native(args) -> None:
     e2e = {"value": e2e_rate, "unit": "tok/s",
            "h2d_bytes_per_step": dec.h2d_bytes(), "d2h_bytes_per_step": dec.d2h_bytes()}
 
+    layer_roof = dec.layer_kernel_roofline(t_first, args.steps, local_ms, timed, hbm,
+                                           gather_peak=None)
     roof = dec.routed_gemv_roofline(steps=8)
     gather = dec.gather_bandwidth()
+    layer_roof["host_link"]["peak"] = round(gather["host_link_peak_gbs"], 1)
+    layer_roof["host_link"]["frac"] = round(layer_roof["host_link"]["achieved"] /
+                                            gather["host_link_peak_gbs"], 4)
     adm = admission_sweep(local)
+    adm_small = admission_small(local)
     wide = wide_step(local)
     hyb = hybrid_step(local) if not args.no_hybrid else None
-    hbm = peaks.get("hbm_gbs", 6800.0)
     tr = routed_traffic()
     line = {
         "metric": METRIC,
@@ -788,7 +1017,13 @@ def run_native(args) -> None:
                      "kernel": roof["kernel"], "avg_launch_us": round(roof["avg_launch_us"], 3),
                      "bytes_per_launch": round(roof["bytes_per_launch"]),
                      "peak_source": f"{peaks['_source']} (MEASURED_PEAKS.json hbm_gbs)"},
+        "timed_tokens": {"misses_per_token": round(timed["misses"], 2),
+                         "fetched_per_token": round(timed["fetched"], 2),
+                         "lookups_per_token": round(timed["lookups"], 2),
+                         "hits_per_token": round(timed["hits"], 2)},
+        "roofline_layer_kernel": layer_roof,
         "admission_us_per_layer": adm,
+        "admission_us_per_call_small": adm_small,
         "wide_decode_step": wide,
         "hybrid_decode": hyb,
         "gather": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in gather.items()},

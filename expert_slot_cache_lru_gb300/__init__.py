@@ -101,6 +101,7 @@ _SIGS = {
     "moe_hybrid_counters": [_vp, _vp],
     "moe_hybrid_pause": [_vp, _i],
     "moe_schedule_trace": [_i, _i, _i, _i, _i, _i, _i, _vp, _i],
+    "moe_decode_layer_plan": [_vp, _i, _i, _i, _i, _u, _vp, _i],
     "moe_hybrid_selftest": [_i, _i, _i, _vp, _i, _i, _i, _i, _i, _u, _vp],
     "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
@@ -271,6 +272,16 @@ def moe_schedule_trace(one_launch: bool = False, fused: bool = False, overlap: b
     rc = _lib.moe_schedule_trace(int(one_launch), int(fused), int(overlap), int(pf), int(shared),
                                  int(hybrid), fail_at, buf, len(buf))
     return rc, buf.value.decode().split()
+
+
+def moe_decode_layer_plan(cache: int, n_rows: int, k: int, shared: bool = False,
+                          pf: bool = False, flags: int = 0) -> list[str]:
+    """The operations moe_decode_layer would enqueue on this cache for the
+    shape and flags, as moe_schedule_trace tokens (see moe_cache.h)."""
+    buf = C.create_string_buffer(4096)
+    _check("moe_decode_layer_plan", _lib.moe_decode_layer_plan(
+        cache, n_rows, k, int(shared), int(pf), flags, buf, len(buf)))
+    return buf.value.decode().split()
 
 
 def moe_hybrid_counters(cache: int) -> dict:

@@ -638,6 +638,24 @@ struct TraceOps : LayerOps {
   }
 };
 
+// The plan moe_decode_layer runs for a step of this shape on this cache.
+LayerPlan plan_of(const moe_cache* c, int n_rows, int k, bool shared, bool pf, unsigned flags) {
+  LayerPlan p{};
+  p.overlap = (flags & MOE_OVERLAP) != 0;
+  p.hybrid = (flags & MOE_HYBRID) != 0;
+  p.pf = pf;
+  p.shared = shared;
+  const moe_cache_desc& dd = c->d;
+  p.fused = (flags & MOE_FUSED) && c->stream_ffn && dd.slot_bytes > 0 &&
+            (!shared || dd.shared_inter == dd.inter) &&
+            moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k, p.shared);
+  // the hybrid post must follow the admission, so a hybrid layer keeps it as
+  // its own launch
+  p.one_launch = p.fused && !p.hybrid &&
+                 moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k, p.shared);
+  return p;
+}
+
 }  // namespace
 
 int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_ids,
@@ -653,20 +671,8 @@ int moe_decode_layer(moe_cache* c, int layer, const void* d_x, const int32_t* d_
   const bool pf = d_pred && n_pred > 0;
   if (pf && (layer + 1 >= c->d.n_layers || c->d.max_pred == 0)) return MOE_ERR_INVALID_ARG;
   if (pf && n_pred > c->d.max_pred) return MOE_ERR_CAPACITY;
-  LayerPlan p{};
-  p.overlap = (flags & MOE_OVERLAP) != 0;
-  p.hybrid = (flags & MOE_HYBRID) != 0;
-  p.pf = pf;
-  p.shared = d_shared_blob != nullptr;
+  const LayerPlan p = plan_of(c, n_rows, k, d_shared_blob != nullptr, pf, flags);
   if (p.hybrid && !c->cpu) return MOE_ERR_STATE;
-  const moe_cache_desc& dd = c->d;
-  p.fused = (flags & MOE_FUSED) && c->stream_ffn && dd.slot_bytes > 0 &&
-            (!d_shared_blob || dd.shared_inter == dd.inter) &&
-            moe::layer_stream_supported(dd.wfmt, dd.hidden, dd.inter, n_rows, k, p.shared);
-  // the hybrid post must follow the admission, so a hybrid layer keeps it as
-  // its own launch
-  p.one_launch = p.fused && !p.hybrid &&
-                 moe::layer_admit_supported(c->st, dd.wfmt, dd.hidden, dd.inter, n_rows, k, p.shared);
   if (!p.fused && p.overlap && !side_stream) return MOE_ERR_INVALID_ARG;
   CudaOps ops;
   ops.c = c, ops.layer = layer, ops.d_x = d_x, ops.d_ids = d_ids, ops.d_w = d_w;
@@ -684,6 +690,17 @@ int moe_schedule_trace(int one_launch, int fused, int overlap, int pf, int share
   LayerPlan p{one_launch != 0, fused != 0, overlap != 0, pf != 0, shared != 0, hybrid != 0};
   TraceOps ops;
   ops.fail_at = fail_at;
+  const int rc = schedule_layer(p, ops);
+  if ((int)ops.out.size() >= cap) return MOE_ERR_CAPACITY;
+  std::memcpy(h_out, ops.out.c_str(), ops.out.size() + 1);
+  return rc;
+}
+
+int moe_decode_layer_plan(moe_cache* c, int n_rows, int k, int shared, int pf, unsigned flags,
+                          char* h_out, int cap) {
+  if (!c || !h_out || cap < 1 || n_rows < 0 || k < 0) return MOE_ERR_INVALID_ARG;
+  const LayerPlan p = plan_of(c, n_rows, k, shared != 0, pf != 0, flags);
+  TraceOps ops;
   const int rc = schedule_layer(p, ops);
   if ((int)ops.out.size() >= cap) return MOE_ERR_CAPACITY;
   std::memcpy(h_out, ops.out.c_str(), ops.out.size() + 1);

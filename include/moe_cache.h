@@ -404,6 +404,15 @@ MOE_API int moe_cpu_experts(int wfmt, int hidden, int inter, const void* const* 
 MOE_API int moe_schedule_trace(int one_launch, int fused, int overlap, int pf, int shared,
                                int hybrid, int fail_at, char* h_out, int cap);
 
+/* Host only, no device work: the operations moe_decode_layer would enqueue on
+ * cache c for a step of n_rows x k routes, with (shared != 0) or without a
+ * shared expert, with (pf != 0) or without predictions, under `flags` -- the
+ * same tokens as moe_schedule_trace ("c:layer_admit" alone is the one-launch
+ * layer).  Lets a caller (and the tests) confirm which path a shape takes.
+ * MOE_ERR_CAPACITY if the trace does not fit in cap bytes. */
+MOE_API int moe_decode_layer_plan(moe_cache* c, int n_rows, int k, int shared, int pf,
+                                  unsigned flags, char* h_out, int cap);
+
 /* Copy one layer's counters to the host.  Synchronises the device. */
 MOE_API int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out);
 
@@ -439,7 +448,11 @@ MOE_API int moe_cache_fail_next_gather(moe_cache* c, int n);
  * Set-up: the first call on each device (that device current) looks up the
  * array's address with cudaGetSymbolAddress and sets the kernel's shared
  * memory limit; a failure returns MOE_ERR_CUDA.  If the first call is the
- * one doing this set-up, make it before any stream capture.
+ * one doing this set-up, make it before any stream capture.  The address is
+ * kept per device ordinal for the life of the process and belongs to that
+ * device's primary CUDA context: after a cudaDeviceReset of the device it is
+ * stale (the context and its array are gone), so do not call this entry point
+ * on a device that was reset after its first call.
  *
  * Races: there is one scratch array per device, so calls whose executions
  * overlap on a device (different streams, or threads without ordering) race

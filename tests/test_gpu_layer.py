@@ -208,13 +208,20 @@ def test_slot_placement_does_not_change_bits():
 
 
 @pytest.mark.slow
-def test_qwen3moe_full_size():
+@pytest.mark.parametrize("fused", [False, True])
+def test_qwen3moe_full_size(fused):
     """The decode benchmark's workload at full size (40 layers x 256 NVFP4
-    experts, 3,164 slots, shared expert), overlapped as benchmarked: state
-    exact every token, outputs of sampled tokens on every layer vs fp64."""
+    experts, 3,164 slots, shared expert), eagerly, on the four-launch
+    overlapped path and on the one-launch layer (MOE_FUSED) the benchmark
+    captures: state exact every token, outputs of two tokens on every layer vs
+    fp64."""
     w = synth.scaled(synth.workloads()["qwen3moe_decode"], steps=20)
     rig = Rig(w)
-    st = Stepper(rig)
+    st = Stepper(rig, fused=fused)
+    if fused:
+        plan = rig.m.moe_decode_layer_plan(rig.sc.handle, w.batch, w.top_k, shared=True,
+                                           flags=rig.m.MOE_FUSED | rig.m.MOE_OVERLAP)
+        assert plan == ["c:layer_admit"], plan
     ids, wts = synth.make_routing(w)
     for t in range(w.steps):
         x = synth.make_hidden(w, t)
@@ -225,6 +232,74 @@ def test_qwen3moe_full_size():
                 assert_close(st.out[layer], ref, w.fmt, f"token {t} layer {layer}")
     misses = sum(rig.sc.stats(l)["misses"] for l in range(w.n_layers))
     assert misses > 300
+
+
+@pytest.mark.slow
+def test_qwen3moe_benchmark_graph_full_size():
+    """The path bench.py times, as it times it: bench.Decode (40 layers x 256
+    NVFP4 experts, 3,164 slots, shared expert, MOE_FUSED: one launch per
+    layer with the admission inside) captured as one CUDA graph per token and
+    replayed for 14 tokens with each token's inputs written into the graph's
+    fixed buffers [FreeToken issue #753, What we changed: fixed addresses,
+    device-side miss counts, no host sync].  After every token the slot ids,
+    the whole cache state and every layer's statistics equal the oracle's;
+    at two tokens all 40 layers' outputs are within the NVFP4 tolerance of
+    fp64; at the end every resident slot holds its expert's bytes."""
+    import oracle
+
+    import bench
+    from tests.gpu_util import assert_close, assert_state_equal
+    dec = bench.Decode(0, warm_tokens=2, total_tokens=16)
+    w, m = dec.w, dec.m
+    plan = m.moe_decode_layer_plan(dec.cache.handle, w.batch, w.top_k, shared=True,
+                                   flags=m.MOE_FUSED | m.MOE_OVERLAP)
+    assert plan == ["c:layer_admit"], plan  # the one-launch layer at the full size
+    ids = dec.d_ids.cpu().numpy()           # [T, L, R], as the graph's inputs
+    wts = dec.d_w.cpu().numpy()
+    oc = oracle.OracleCache(w.n_layers, w.n_experts, w.n_slots)
+    for t in range(2):                      # the eager warm-up tokens
+        for layer in range(w.n_layers):
+            oc.admit(layer, ids[t, layer])
+    assert_state_equal(dec.cache, oc, what="after the eager tokens")
+    shared = [synth.make_shared(w, l) for l in range(w.n_layers)]
+    misses = 0
+    for t in range(2, dec.T):
+        before = sum(dec.cache.stats(l)["misses"] for l in range(w.n_layers))
+        assert dec.t == t
+        dec.step()
+        torch.cuda.synchronize()
+        got = dec.b_slots.cpu().numpy()
+        for layer in range(w.n_layers):
+            ref = oc.admit(layer, ids[t, layer])
+            assert np.array_equal(got[layer], ref["slots"]), f"token {t} layer {layer}"
+        assert_state_equal(dec.cache, oc, what=f"token {t}")
+        misses += sum(dec.cache.stats(l)["misses"] for l in range(w.n_layers)) - before
+        if t in (2, dec.T - 1):
+            x = dec.d_x[t].cpu().numpy().view(np.uint16)
+            for layer in range(w.n_layers):
+                ref = oracle.layer(w.fmt, [dec.blobs.addr(layer * w.n_experts + e)
+                                           for e in range(w.n_experts)],
+                                   w.n_experts, w.hidden, w.inter, x[layer],
+                                   ids[t, layer].reshape(w.batch, w.top_k),
+                                   wts[t, layer].reshape(w.batch, w.top_k),
+                                   shared_blob=shared[layer][0], shared_inter=w.shared_inter,
+                                   shared_gate_w=shared[layer][1])
+                assert_close(dec.b_out[layer], ref, w.fmt, f"token {t} layer {layer}")
+    assert misses > 100  # the replayed tokens really gather (about 28 per token at steady state)
+    for l in range(w.n_layers):
+        assert dec.cache.stats(l)["status_bits"] == 0
+    # every resident slot holds its expert's bytes, compared on the device in chunks
+    state = oc.state()
+    keys = state["slot_key"]
+    res = np.nonzero(keys >= 0)[0]
+    host = dec.blobs.buf.view(-1, dec.blobs.stride)
+    dev = dec.storage.view(w.n_slots, dec.blobs.stride)
+    nb = dec.blobs.nbytes
+    for c0 in range(0, len(res), 128):
+        sl = res[c0:c0 + 128]
+        rows = torch.from_numpy(dec.blobs.key_to_blob[keys[sl]])
+        want = host.index_select(0, rows)[:, :nb].cuda()
+        assert torch.equal(dev[torch.from_numpy(sl).cuda()][:, :nb], want), f"slots {sl[:4]}"
 
 
 @pytest.mark.slow
@@ -280,21 +355,51 @@ def test_qwen3moe_graph_replay_equals_eager():
         assert graphed.sc.stats(layer) == eager.sc.stats(layer)
 
 
+def _gpu_groups(sc, max_routes: int) -> list[tuple[int, list[int]]]:
+    """The route groups moe_routed_experts wrote on the grouped path:
+    [G, slot[max_routes], start[max_routes + 1], route[max_routes]]."""
+    from tests.gpu_util import dev_copy
+    n = 1 + max_routes + (max_routes + 1) + max_routes
+    a = dev_copy(sc.views().groups, n, np.int32)
+    G = int(a[0])
+    slot = a[1:1 + G]
+    start = a[1 + max_routes:1 + max_routes + G + 1]
+    route = a[2 + 2 * max_routes:]
+    return [(int(slot[g]), [int(r) for r in route[start[g]:start[g + 1]]]) for g in range(G)]
+
+
+def wide_layer_oracle(rig, x, ids, wts, experts_per_call: int = 64) -> np.ndarray:
+    """The fp64 layer over every row, computed as a sum of partial layers over
+    disjoint sets of experts (ascending id, `experts_per_call` at a time), so
+    that one oracle call dequantises at most that many experts."""
+    w = rig.w
+    used = np.unique(ids[(ids >= 0) & (ids < w.n_experts)])
+    full = np.zeros((x.shape[0], w.hidden), np.float64)
+    for c0 in range(0, len(used), experts_per_call):
+        part = used[c0:c0 + experts_per_call]
+        mask = np.isin(ids, part).astype(np.uint8)
+        full += rig.oracle_layer(0, x, ids, wts, mask=mask)
+    return full
+
+
 @pytest.mark.slow
 def test_wide_decode_step():
-    """600 rows x top-2 = 1,200 routes over 1,024 NVFP4 experts with 1,100
-    slots, 30% pre-resident: admission + gather + routed FFNs; every row's
-    slot ids exact, sampled rows' outputs vs fp64."""
+    """[FreeToken PR #680, Tests]: 600 rows x top-2 = 1,200 routes over 1,024
+    NVFP4 experts with 1,100 slots, 30% pre-resident: admission + gather +
+    grouped routed FFNs.  Every slot id exact; the route groups the GPU built
+    equal the oracle's; every one of the 600 rows' outputs within the NVFP4
+    tolerance of the fp64 layer."""
     w = synth.workloads()["wide_decode"]
     rig = Rig(w)
     rig.prefill(0, synth.prefill_ids(w))
     st = Stepper(rig)
     ids, wts = synth.make_routing(w, steps=1)
     x = synth.make_hidden(w, 0)
-    st.step(0, ids[0], wts[0], x)
-    rows = np.random.default_rng(0).choice(w.batch, 12, replace=False)
-    ref = rig.oracle_layer(0, x[0][rows], ids[0, 0][rows], wts[0, 0][rows])
-    assert_close(st.out[0][torch.from_numpy(rows).cuda()], ref, w.fmt, "wide step rows")
+    refs = st.step(0, ids[0], wts[0], x)
+    assert _gpu_groups(rig.sc, rig.sc.desc.max_routes) == refs[0]["groups"]
+    ref = wide_layer_oracle(rig, x[0], ids[0, 0], wts[0, 0])
+    info = assert_close(st.out[0], ref, w.fmt, "wide step, all rows")
+    assert info["max_abs"] > 0
     s = rig.sc.stats(0)
     assert s["fetched"] == s["misses"] > 400 and s["evictions"] == 0
 

@@ -528,6 +528,51 @@ def test_layer_zero_input_and_masks():
     assert np.allclose(s_only[0], 0.5 * ffn_s, rtol=1e-14, atol=1e-16)
 
 
+def _one_weight_bf16_blob(H, I, a, b, c):
+    """bf16 expert whose only nonzero weights are Wg[2,5] = a, Wu[2,5] = b, Wd[7,2] = c."""
+    w = np.zeros(3 * H * I, np.float32)
+    w[2 * H + 5] = a
+    w[H * I + 2 * H + 5] = b
+    w[2 * H * I + 7 * I + 2] = c
+    return synth.to_bf16_bits(w).view(np.uint8)
+
+
+@pytest.mark.parametrize("wg", [0.75, -0.75])
+def test_shared_gate_one_hot_closed_form(wg):
+    """The shared expert's gate sigmoid(x . w_g) with a one-hot w_g (only
+    w_g[9] = wg) and x nonzero at 5 and 9: z = x9 * wg exactly, and the layer
+    output is the routed sum plus sigmoid(z) times the shared FFN's closed form,
+    at both signs of z.  A sigma(-z), a z taken over the wrong vector or element,
+    or the gate applied to the routed part fails here."""
+    H, I, E = 32, 32, 4
+    x = np.zeros(H, np.float32)
+    x[5], x[9] = 1.25, 2.0
+    xb = synth.to_bf16_bits(x)
+    sblob = _one_weight_bf16_blob(H, I, 0.75, -1.5, 2.0)      # shared: y[7] only
+    rblob = _one_weight_bf16_blob(H, I, 0.5, 1.0, -1.0)       # routed expert 1: y[7] only
+    gate = np.zeros(H, np.float32)
+    gate[9] = wg
+    gw = synth.to_bf16_bits(gate)
+    z = 2.0 * wg
+    sig = 1.0 / (1.0 + math.exp(-z))
+    g_s = 0.75 * 1.25
+    ffn_s = 2.0 * (g_s / (1 + math.exp(-g_s))) * (-1.5 * 1.25)
+    g_r = 0.5 * 1.25
+    ffn_r = -1.0 * (g_r / (1 + math.exp(-g_r))) * (1.0 * 1.25)
+    blobs = [None, rblob, None, None]
+    ids = np.array([[1, 1]], np.int32)             # expert 1 twice: weights 0.25 + 0.5
+    wts = np.array([[0.25, 0.5]], np.float32)
+    out = oracle.layer(oracle.FMT_BF16, blobs, E, H, I, xb[None, :], ids, wts,
+                       shared_blob=sblob, shared_inter=I, shared_gate_w=gw)
+    assert out[0, 7] == pytest.approx(0.75 * ffn_r + sig * ffn_s, rel=1e-14)
+    assert np.count_nonzero(out[0]) == 1
+    # the shared term alone (zero routing weights): exactly the gated closed form
+    s_only = oracle.layer(oracle.FMT_BF16, blobs, E, H, I, xb[None, :], ids, np.zeros_like(wts),
+                          shared_blob=sblob, shared_inter=I, shared_gate_w=gw)
+    assert s_only[0, 7] == pytest.approx(sig * ffn_s, rel=1e-14)
+    assert (s_only[0, 7] / ffn_s > 0.5) == (wg > 0)
+
+
 @pytest.mark.parametrize("age,protected", [(1, True), (254, True), (255, False), (300, False)])
 def test_guard_recency_byte_boundary(age, protected):
     """Score (4 << 8) | rec against a never-seen prediction: protected iff

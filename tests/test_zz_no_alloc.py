@@ -92,6 +92,43 @@ def test_noalloc_matches_routed_experts_on_two_calls_in_a_row():
 
 
 @pytest.mark.gpu
+def test_noalloc_skips_slot_ids_outside_the_pool():
+    """Routes whose slot id lies outside [0, n_slots) (-1, n_slots, a large id)
+    contribute nothing: the output equals moe_routed_experts' for the same slot
+    ids byte for byte, and the oracle's layer with those routes masked out."""
+    w = _workload()
+    rig = Rig(w, max_rows=w.batch)
+    m = rig.m
+    ids, wts = synth.make_routing(w)
+    d_slots, ref = _resident_step(rig, 0, ids)
+    s = d_slots.cpu().numpy().reshape(w.batch, w.top_k).copy()
+    bad = np.zeros_like(s, dtype=bool)
+    for (b, j), v in zip([(0, 1), (1, 7), (2, 0), (3, 3), (3, 4)],
+                         [-1, w.n_slots, 1 << 20, -7, w.n_slots + 1]):
+        s[b, j] = v
+        bad[b, j] = True
+    d_s = torch.from_numpy(s.ravel().copy()).cuda()
+    x = synth.make_hidden(w, 0)[0]
+    d_x = torch.from_numpy(x.view(np.int16)).cuda()
+    d_w = torch.from_numpy(np.ascontiguousarray(wts[0, 0], np.float32)).cuda()
+    want = torch.empty(w.batch, w.hidden, dtype=torch.bfloat16, device="cuda")
+    m.moe_routed_experts(rig.sc.handle, 0, d_x, d_s, d_w, w.batch, w.top_k, None, None, want)
+    status = torch.zeros(1, dtype=torch.int64, device="cuda")
+    got = [torch.full((w.batch, w.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+           for _ in range(2)]
+    for t in range(2):
+        m.moe_routed_experts_noalloc(w.fmt, w.hidden, w.inter, rig.storage, rig.blobs.stride,
+                                     w.n_slots, d_x, d_s, d_w, w.batch, w.top_k, got[t], status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    b = want.view(torch.int16).cpu().numpy()
+    for t in range(2):
+        assert np.array_equal(got[t].view(torch.int16).cpu().numpy(), b), f"call {t}"
+    masked = rig.oracle_layer(0, x, ids[0, 0], wts[0, 0], mask=(~bad).astype(np.uint8))
+    assert_close(got[1], masked, w.fmt, "skipped routes against the masked oracle layer")
+
+
+@pytest.mark.gpu
 def test_noalloc_rejects_unsupported_shape():
     import expert_slot_cache_lru_gb300 as m
     w = _workload()
