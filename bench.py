@@ -631,7 +631,7 @@ def admission_oracle(seconds: float = 6.0) -> dict:
     return res
 
 
-def wide_step(dev: int, reps: int = 5) -> dict:
+def wide_step(dev: int, reps: int = 5, routing: str = "uniform") -> dict:
     """The wide decode step: 600 rows x top-2 = 1,200 routes over 1,024 NVFP4
     experts (H 2048, I 768) with a 1,100-slot cache, 30% of the experts
     pre-resident.  The first step admits ~495 misses; its admission, gather and
@@ -644,6 +644,8 @@ def wide_step(dev: int, reps: int = 5) -> dict:
     import expert_slot_cache_lru_gb300 as m
     import synth
     w = synth.workloads()["wide_decode"]
+    if routing != w.routing:
+        w = synth.scaled(w, routing=routing)
     blobs = synth.HostBlobs(w, pinned=True)
     storage = torch.empty(w.n_slots * blobs.stride, dtype=torch.uint8, device="cuda")
     cache = m.SlotCache(n_layers=1, n_experts=w.n_experts, n_slots=w.n_slots,
@@ -675,6 +677,8 @@ def wide_step(dev: int, reps: int = 5) -> dict:
     t_adm, t_gat, t_ffn = (ev[i].elapsed_time(ev[i + 1]) for i in range(3))
     slots = d_slots.cpu().numpy()
     distinct = len(set(int(v) for v in slots if v >= 0))
+    _, counts = np.unique(slots[slots >= 0], return_counts=True)
+    dense_groups = int((counts >= 8).sum())
     ffn_bytes = distinct * w.blob_bytes + w.batch * w.hidden * 2 * 2 + R * 8
     times = []
     for _ in range(reps):
@@ -687,13 +691,67 @@ def wide_step(dev: int, reps: int = 5) -> dict:
         s.synchronize()
         times.append(e0.elapsed_time(e1))
     t_ffn_hot = statistics.median(times)
+    # the same FFN with every group forced onto one kernel family, for comparison
+    forced = {}
+    for name, mode in (("cuda_cores", m.MOE_WIDE_CUDA_CORES), ("tensor_cores", m.MOE_WIDE_TENSOR_CORES)):
+        m.moe_cache_set_wide_path(cache.handle, mode)
+        tt = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                e0.record(s)
+                m.moe_routed_experts(cache.handle, 0, d_x, d_slots, d_w, w.batch, w.top_k, None,
+                                     None, out, s)
+                e1.record(s)
+            s.synchronize()
+            tt.append(e0.elapsed_time(e1))
+        forced[name] = statistics.median(tt)
+    m.moe_cache_set_wide_path(cache.handle, m.MOE_WIDE_AUTO)
+    # the admission again in a graph, repeated: the same 1,200 routes each time
+    # on a fresh cache holding the same 307 experts (so every replay admits the
+    # ~479 misses into empty slots, as the first step did)
+    adm_graph = None
+    try:
+        caches = []
+        g = torch.cuda.CUDAGraph()
+        n_rep = 8
+        for _ in range(n_rep):
+            c2 = m.SlotCache(n_layers=1, n_experts=w.n_experts, n_slots=w.n_slots,
+                             pool_mode=m.MOE_POOL_SHARED, max_routes=w.routes, max_rows=w.batch)
+            m.moe_cache_prefill(c2.handle, 0, pre, len(pre))
+            caches.append(c2)
+        outs = [torch.empty_like(d_ids) for _ in range(n_rep)]
+        with torch.cuda.graph(g, stream=s):
+            for c2, o2 in zip(caches, outs):
+                m.moe_admit(c2.handle, 0, d_ids, o2, R, -1, s)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        s.synchronize()
+        assert all(torch.equal(o2, d_slots) for o2 in outs)
+        adm_graph = round(e0.elapsed_time(e1) * 1e3 / n_rep, 2)
+        del g
+        for c2 in caches:
+            c2.close()
+    except Exception as ex:  # reported, never fatal to the bench line
+        adm_graph = f"failed: {ex}"
     cache.close()
-    return {"routes": R, "distinct_experts": distinct, "misses": int(st["misses"]),
+    return {"routing": routing, "routes": R, "distinct_experts": distinct,
+            "misses": int(st["misses"]),
             "admission_us": round(t_adm * 1e3, 2),
             "gather_ms": round(t_gat, 3),
             "gather_gbs": round(st["fetched"] * w.blob_bytes / (t_gat * 1e-3) / 1e9, 1),
+            "admission_us_graph": adm_graph,
+            "ffn_path": "automatic: expert groups of >= 8 routes on the tensor cores (tcgen05), "
+                        "the rest on the CUDA cores",
+            "groups_ge_8_routes": dense_groups,
             "ffn_ms_first": round(t_ffn, 3), "ffn_ms": round(t_ffn_hot, 3),
             "ffn_bytes": ffn_bytes, "ffn_gbs": round(ffn_bytes / (t_ffn_hot * 1e-3) / 1e9, 1),
+            "ffn_ms_all_cuda_cores": round(forced["cuda_cores"], 3),
+            "ffn_ms_all_tensor_cores": round(forced["tensor_cores"], 3),
+            "ffn_gbs_all_tensor_cores": round(ffn_bytes / (forced["tensor_cores"] * 1e-3) / 1e9, 1),
             "step_ms": round(t_adm + t_gat + t_ffn, 3)}
 
 
@@ -888,7 +946,8 @@ def run_native(args) -> None:
     hbm = peaks.get("hbm_gbs", 6800.0)
     if args.wide_only:  # profiler runs: the wide decode step alone
         if rank == 0:
-            print(json.dumps({"wide_only": True, **wide_step(local)}), flush=True)
+            print(json.dumps({"wide_only": True, **wide_step(local, routing=args.wide_routing)}),
+                  flush=True)
         return
     if args.hybrid_only:
         if rank == 0:
@@ -973,6 +1032,7 @@ def run_native(args) -> None:
     adm = admission_sweep(local)
     adm_small = admission_small(local)
     wide = wide_step(local)
+    wide_zipf = wide_step(local, reps=3, routing="zipf")
     hyb = hybrid_step(local) if not args.no_hybrid else None
     tr = routed_traffic()
     line = {
@@ -1025,6 +1085,7 @@ def run_native(args) -> None:
         "admission_us_per_layer": adm,
         "admission_us_per_call_small": adm_small,
         "wide_decode_step": wide,
+        "wide_decode_step_zipf": wide_zipf,
         "hybrid_decode": hyb,
         "gather": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in gather.items()},
         "setup_s": {k: round(v, 1) for k, v in dec.setup_s.items()},
@@ -1114,6 +1175,8 @@ def main():
                     help="time the decode only and print a short line (profiler runs)")
     ap.add_argument("--wide-only", action="store_true",
                     help="run only the wide decode step sub-measurement (profiler runs)")
+    ap.add_argument("--wide-routing", choices=["uniform", "zipf"], default="uniform",
+                    help="routing of the --wide-only step")
     ap.add_argument("--routed-only", action="store_true",
                     help="after the decode, run only the routed FFN kernel's roofline graph "
                          "(profiler runs)")

@@ -46,6 +46,9 @@ MOE_HYBRID = 4
 MOE_STATUS_INVALID_ID = 1
 MOE_STATUS_CAPACITY = 2
 MOE_STATUS_TIMEOUT = 4
+MOE_WIDE_AUTO = 0
+MOE_WIDE_CUDA_CORES = 1
+MOE_WIDE_TENSOR_CORES = 2
 
 
 class moe_cache_desc(C.Structure):
@@ -96,6 +99,7 @@ _SIGS = {
     "moe_read_stats": [_vp, _i, C.POINTER(moe_stats)],
     "moe_device_views": [_vp, C.POINTER(moe_views)],
     "moe_cache_fail_next_gather": [_vp, _i],
+    "moe_cache_set_wide_path": [_vp, _i],
     "moe_hybrid_start": [_vp, _i],
     "moe_hybrid_stop": [_vp],
     "moe_hybrid_counters": [_vp, _vp],
@@ -237,6 +241,12 @@ def moe_device_views(cache: int) -> moe_views:
 
 def moe_cache_fail_next_gather(cache: int, n: int = 1) -> None:
     _check("moe_cache_fail_next_gather", _lib.moe_cache_fail_next_gather(cache, n))
+
+
+def moe_cache_set_wide_path(cache: int, mode: int) -> None:
+    """MOE_WIDE_AUTO, MOE_WIDE_CUDA_CORES or MOE_WIDE_TENSOR_CORES: which
+    kernels run wide steps' routed experts (see moe_cache.h)."""
+    _check("moe_cache_set_wide_path", _lib.moe_cache_set_wide_path(cache, int(mode)))
 
 
 def moe_hybrid_start(cache: int, n_threads: int) -> None:

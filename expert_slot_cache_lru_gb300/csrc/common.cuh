@@ -158,6 +158,9 @@ struct FfnScratch {
   uint16_t* x16;    // [max_rows * H] x prepared for the grouped kernels
   float* xinv;      // [max_rows] inverse of the per-row x scale
   float* y;         // [max_routes * H] per-route down projections (grouped path)
+  uint16_t* h16;    // [max_routes * I] h as f16 for the tensor-core down GEMM
+  float* hinv;      // [max_routes] inverse of each route's h scale
+  int32_t* dense;   // [1 + max_routes] the groups the tensor-core kernels take: count, ids
   int* gdone;       // [max_routes] pieces of each demand-plan expert copied by a fused layer
   // a fused layer with the admission inside the launch (three counters that only grow)
   unsigned long long* epoch;   // launches (each CTA adds one)
@@ -218,7 +221,22 @@ cudaError_t grouped_init(int E, int H, int I);
 cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, int layer,
                                   const void* x, const int32_t* slot_ids, const float* w,
                                   int n_rows, int k, const float* shared_y, void* out,
-                                  FfnScratch sc, int max_routes, cudaStream_t s);
+                                  FfnScratch sc, int max_routes, int wide_mode,
+                                  cudaStream_t s);
+
+// The gate/up and down GEMMs of the grouped path on the tensor cores
+// (grouped_tc.cu): NVFP4 experts with H and I multiples of 128, for the groups
+// group_kernel lists (FfnScratch::dense).  One tcgen05.mma (M 128, K 16) takes about
+// 100 cycles to issue whatever its N, i.e. ~20 fp4 weights per cycle per SM,
+// half of what HBM delivers to an SM; the CUDA-core kernels reread nothing and
+// win while a group has few routes.  In the automatic mode groups of at least
+// kTcMinRoutes routes go to the tensor cores and the rest to the CUDA cores.
+constexpr int kTcMinRoutes = 8;
+bool grouped_tc_supported(int wfmt, int H, int I);
+cudaError_t grouped_tc_init();
+cudaError_t launch_grouped_tc(const DevState& st, int H, int I, int layer, int k, int n_routes,
+                              int max_routes, FfnScratch sc, unsigned long long* status,
+                              cudaStream_t s);
 
 // Allocation-free routed FFN (ffn_stream.cu): the scratch is a file-scope
 // device array whose address noalloc_scratch looks up once per device.

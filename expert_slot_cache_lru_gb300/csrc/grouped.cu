@@ -119,13 +119,13 @@ struct Groups {
 // routes scattered by an atomic cursor, then each group's (few) routes sorted.
 __global__ void __launch_bounds__(kGT) group_kernel(DevState st, int layer,
                                                     const int32_t* __restrict__ slot_ids, int R,
-                                                    Groups gr) {
+                                                    Groups gr, int dense_from,
+                                                    int32_t* __restrict__ dense) {
   extern __shared__ int gsm[];
   const int E = st.E;
   int* off = gsm;          // [E] routes, then start offset, of expert e
   int* cur = gsm + E;      // [E] scatter cursor
   int* eslot = gsm + 2 * E;  // [E] the slot of expert e
-  int* gid = gsm + 3 * E;    // [E] group index of expert e (-1 = none)
   __shared__ BlockScratch bs;
   const int tid = threadIdx.x;
   const size_t pbase = (size_t)pool_of(st, layer) * st.S;
@@ -145,18 +145,20 @@ __global__ void __launch_bounds__(kGT) group_kernel(DevState st, int layer,
   __syncthreads();
   const int ept = (E + kGT - 1) / kGT;
   const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
-  int nr = 0, ng = 0;
+  int nr = 0, ng = 0, nd = 0;
   for (int e = e0; e < e1; ++e) {
     nr += off[e];
     ng += off[e] > 0;
+    nd += dense_from > 0 && off[e] >= dense_from;
   }
-  int totR, totG;
+  int totR, totG, totD;
   int r0 = block_excl_scan(nr, bs, &totR);
   int g0 = block_excl_scan(ng, bs, &totG);
+  int d0 = block_excl_scan(nd, bs, &totD);
   for (int e = e0; e < e1; ++e) {
     const int c = off[e];
-    gid[e] = c > 0 ? g0 : -1;
     if (c > 0) {
+      if (dense && dense_from > 0 && c >= dense_from) dense[1 + d0++] = g0;
       gr.slot()[g0] = eslot[e];
       gr.start()[g0] = r0;
       ++g0;
@@ -167,27 +169,30 @@ __global__ void __launch_bounds__(kGT) group_kernel(DevState st, int layer,
   if (tid == 0) {
     gr.G() = totG;
     gr.start()[totG] = totR;
+    if (dense) dense[0] = totD;
   }
   __syncthreads();
-  for (int r = tid; r < R; r += kGT) {
-    const int s = slot_ids[r];
-    if ((unsigned)s >= (unsigned)st.S) continue;
-    const int e = st.slot_key[pbase + s] - layer * E;
-    if ((unsigned)e >= (unsigned)E) continue;
-    gr.route()[off[e] + atomicAdd(&cur[e], 1)] = r;
-  }
-  __syncthreads();
-  for (int g = tid; g < totG; g += kGT) {  // ascending route index within the group
-    int32_t* rt = gr.route();
-    const int a = gr.start()[g], b = gr.start()[g + 1];
-    for (int i = a + 1; i < b; ++i) {
-      const int v = rt[i];
-      int j = i - 1;
-      while (j >= a && rt[j] > v) {
-        rt[j + 1] = rt[j];
-        --j;
+  // scatter in ascending route order, 32 routes at a time by warp 0: lanes of
+  // the same expert take consecutive places in lane order
+  if (tid < 32) {
+    for (int b = 0; b < R; b += 32) {
+      const int r = b + tid;
+      int e = -1;
+      if (r < R) {
+        const int s = slot_ids[r];
+        if ((unsigned)s < (unsigned)st.S) {
+          e = st.slot_key[pbase + s] - layer * E;
+          if ((unsigned)e >= (unsigned)E) e = -1;
+        }
       }
-      rt[j + 1] = v;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const int rank = __popc(same & ((1u << tid) - 1u));
+        gr.route()[off[e] + cur[e] + rank] = r;
+      }
+      __syncwarp();
+      if (e >= 0 && tid == 31 - __clz(same)) cur[e] += __popc(same);  // the set's last lane
+      __syncwarp();
     }
   }
 }
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(kWT, 2) gup_staged_kernel(DevState st, int H, 
                                                             const uint16_t* __restrict__ x16,
                                                             const float* __restrict__ xinv,
                                                             int k, Groups gr,
-                                                            float* __restrict__ h) {
+                                                            float* __restrict__ h, int skip_from) {
   extern __shared__ __align__(16) uint8_t dsm[];
   uint4* xs = reinterpret_cast<uint4*>(dsm);  // [kNR][H / 8]
   uint8_t* stg = dsm + (size_t)kNR * H * 2;   // [kNS][gate codes | up codes | gate sc | up sc]
@@ -415,6 +420,7 @@ __global__ void __launch_bounds__(kWT, 2) gup_staged_kernel(DevState st, int H, 
   for (int item = blockIdx.x; item < G * nch; item += gridDim.x) {
     const int g = item / nch, ch = item - g * nch;
     const int ra = gr.start()[g], rb = gr.start()[g + 1];
+    if (skip_from > 0 && rb - ra >= skip_from) continue;  // a dense group: the tensor cores take it
     const uint8_t* blob = st.slots + (pbase + gr.slot()[g]) * st.stride;
     const int i0 = ch * kRowsItem, i = i0 + t;
     const float gs0 = reinterpret_cast<const float*>(blob + o.glob)[0];
@@ -611,7 +617,7 @@ __global__ void __launch_bounds__(kWT) gdown_kernel(DevState st, int H, int I, i
 __global__ void __launch_bounds__(kWT, 2) gdown_staged_kernel(DevState st, int H, int I,
                                                               int layer, Groups gr,
                                                               const float* __restrict__ h,
-                                                              float* __restrict__ y) {
+                                                              float* __restrict__ y, int skip_from) {
   extern __shared__ __align__(16) uint8_t dsm[];
   float* hsm = reinterpret_cast<float*>(dsm);  // [kNR][I]
   uint8_t* stg = dsm + (size_t)kNR * I * 4;    // [kNS][codes | scales]
@@ -625,6 +631,7 @@ __global__ void __launch_bounds__(kWT, 2) gdown_staged_kernel(DevState st, int H
   for (int item = blockIdx.x; item < G * nch; item += gridDim.x) {
     const int g = item / nch, ch = item - g * nch;
     const int ra = gr.start()[g], rb = gr.start()[g + 1];
+    if (skip_from > 0 && rb - ra >= skip_from) continue;  // a dense group: the tensor cores take it
     const uint8_t* blob = st.slots + (pbase + gr.slot()[g]) * st.stride;
     const float gs2 = reinterpret_cast<const float*>(blob + o.glob)[2];
     const int n0 = ch * kRowsItem, n = n0 + t;
@@ -744,9 +751,9 @@ cudaError_t grouped_init(int E, int H, int I) {
   int dev;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess && (size_t)E * 16 > 48 * 1024)
+  if (e == cudaSuccess && (size_t)E * 12 > 48 * 1024)
     e = cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)E * 16));
+                             (int)((size_t)E * 12));
   auto lim = [&](auto kern, size_t bytes) {
     if (e == cudaSuccess && bytes > 48 * 1024)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -770,26 +777,46 @@ cudaError_t grouped_init(int E, int H, int I) {
     occ(gup_staged_kernel, gup_staged_smem(H), &g_occ_staged[0]);
     occ(gdown_staged_kernel, gdown_staged_smem(I), &g_occ_staged[1]);
   }
+  if (e == cudaSuccess && grouped_tc_supported(MOE_W_NVFP4, H, I)) e = grouped_tc_init();
   return e;
 }
 
 cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, int layer,
                                   const void* x, const int32_t* slot_ids, const float* w,
                                   int n_rows, int k, const float* shared_y, void* out,
-                                  FfnScratch sc, int max_routes, cudaStream_t s) {
+                                  FfnScratch sc, int max_routes, int wide_mode,
+                                  cudaStream_t s) {
   const int R = n_rows * k;
   Groups gr{st.groups, max_routes};
-  group_kernel<<<1, kGT, (size_t)st.E * 16, s>>>(st, layer, slot_ids, R, gr);
+  const bool tc_any = wide_mode != MOE_WIDE_CUDA_CORES && grouped_tc_supported(wfmt, H, I);
+  const bool tc_split = tc_any && wide_mode != MOE_WIDE_TENSOR_CORES && staged_ok(H, I);
+  // the tensor cores' groups: those of at least kTcMinRoutes routes (every group
+  // when they take them all)
+  group_kernel<<<1, kGT, (size_t)st.E * 12, s>>>(st, layer, slot_ids, R, gr,
+                                                 tc_any ? (tc_split ? kTcMinRoutes : 1) : 0,
+                                                 tc_any ? sc.dense : nullptr);
   const uint16_t* xx = static_cast<const uint16_t*>(x);
   const int sms = g_sms > 0 ? g_sms : 1;
   const int fi = wfmt == MOE_W_NVFP4 ? MOE_W_NVFP4 : MOE_W_BF16;
   const int grid_u = sms * g_occ[fi][0], grid_d = sms * g_occ[fi][1];
-  if (wfmt == MOE_W_NVFP4 && staged_ok(H, I)) {
+  // NVFP4 with both kernel families available: per group by its route count
+  // (auto), or all groups on one family (a forced mode)
+  const bool tc = tc_any;
+  const bool cc = wide_mode != MOE_WIDE_TENSOR_CORES || !tc;
+  if (wfmt == MOE_W_NVFP4 && (tc || staged_ok(H, I))) {
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
-    gup_staged_kernel<<<sms * g_occ_staged[0], kWT, gup_staged_smem(H), s>>>(
-        st, H, I, layer, sc.x16, sc.xinv, k, gr, sc.h);
-    gdown_staged_kernel<<<sms * g_occ_staged[1], kWT, gdown_staged_smem(I), s>>>(
-        st, H, I, layer, gr, sc.h, sc.y);
+    const bool split = tc && cc && staged_ok(H, I);
+    const int tc_from = !tc ? 0 : (split ? kTcMinRoutes : 1);  // tensor cores: groups >= this
+    if (cc && staged_ok(H, I))
+      gup_staged_kernel<<<sms * g_occ_staged[0], kWT, gup_staged_smem(H), s>>>(
+          st, H, I, layer, sc.x16, sc.xinv, k, gr, sc.h, tc_from);
+    if (tc) {
+      cudaError_t e = launch_grouped_tc(st, H, I, layer, k, R, max_routes, sc, st.status, s);
+      if (e != cudaSuccess) return e;
+    }
+    if (cc && staged_ok(H, I))
+      gdown_staged_kernel<<<sms * g_occ_staged[1], kWT, gdown_staged_smem(I), s>>>(
+          st, H, I, layer, gr, sc.h, sc.y, tc_from);
   } else if (wfmt == MOE_W_NVFP4) {
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
     gup_kernel<MOE_W_NVFP4><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,

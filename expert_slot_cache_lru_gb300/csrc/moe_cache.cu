@@ -41,6 +41,7 @@ struct moe_cache {
   int down_k_max = 0;        // largest k the down kernel's shared memory was sized for
   int last_pf_layer = 0;     // target layer of the last prefetch enqueued (selects its plan)
   bool stream_ffn = true;    // decode-sized steps use the streaming FFN kernels
+  int wide_mode = MOE_WIDE_AUTO;  // which kernels run wide steps (moe_cache_set_wide_path)
   std::vector<const void*> host_ptrs;  // [L*E] host blob addresses, copied at create
   moe_cpu_exec* cpu = nullptr;         // hybrid CPU executor, when started
 };
@@ -176,6 +177,9 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_x16 = cv.take<uint16_t>((size_t)d.max_rows * std::max(H, 1)),
                o_xinv = cv.take<float>(d.max_rows),
                o_y = cv.take<float>((size_t)d.max_routes * std::max(H, 1)),
+               o_h16 = cv.take<uint16_t>((size_t)d.max_routes * std::max(I, 1)),
+               o_hinv = cv.take<float>(d.max_routes),
+               o_dense = cv.take<int32_t>(1 + (size_t)d.max_routes),
                o_status = cv.take<unsigned long long>(1),
                o_bar = cv.take<unsigned long long>(1),
                o_ep = cv.take<unsigned long long>(1), o_pseq = cv.take<unsigned long long>(1),
@@ -227,6 +231,9 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.x16 = reinterpret_cast<uint16_t*>(m + o_x16);
   c->sc.xinv = reinterpret_cast<float*>(m + o_xinv);
   c->sc.y = reinterpret_cast<float*>(m + o_y);
+  c->sc.h16 = reinterpret_cast<uint16_t*>(m + o_h16);
+  c->sc.hinv = reinterpret_cast<float*>(m + o_hinv);
+  c->sc.dense = reinterpret_cast<int32_t*>(m + o_dense);
   c->sc.gdone = reinterpret_cast<int*>(m + o_gdone);
 
   // initial state: nothing resident, every clock at 1
@@ -432,7 +439,7 @@ static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* s
   if (k > 0 && moe::grouped_supported(d.wfmt, d.hidden, d.inter, d.n_experts)) {
     CK(moe::launch_routed_grouped(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w,
                                   n_rows, k, with_shared ? c->sc.ys : nullptr, d_out, c->sc,
-                                  d.max_routes, s));
+                                  d.max_routes, c->wide_mode, s));
     return MOE_OK;
   }
   if (k > 0)
@@ -768,6 +775,12 @@ int moe_device_views(moe_cache* c, moe_views* v) {
   v->plan_prefetch = st.plan_pf[c->last_pf_layer & 1];
   v->groups = st.groups;
   v->n_pools = c->P;
+  return MOE_OK;
+}
+
+int moe_cache_set_wide_path(moe_cache* c, int mode) {
+  if (!c || mode < MOE_WIDE_AUTO || mode > MOE_WIDE_TENSOR_CORES) return MOE_ERR_INVALID_ARG;
+  c->wide_mode = mode;
   return MOE_OK;
 }
 

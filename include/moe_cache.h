@@ -419,6 +419,23 @@ MOE_API int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out);
 /* Device pointers into the state (valid until moe_cache_destroy). */
 MOE_API int moe_device_views(moe_cache* c, moe_views* out);
 
+/* Which kernels run the routed experts of wide steps (the grouped path: more
+ * than 16 rows or 64 routes; the route groups hold each distinct expert's
+ * routes).  NVFP4 experts with H and I multiples of 128 have two kernel
+ * families: the tensor cores (tcgen05 kind::f16 MMAs of 128 weight rows x up
+ * to 32 routes, fp32 accumulators in tensor memory; h is rounded to f16 with a
+ * per-route power-of-two scale before the down GEMM) and the CUDA cores (fp32
+ * h).  A tensor-core MMA costs the same whatever its route count, so:
+ *   MOE_WIDE_AUTO (the default): groups of at least 8 routes on the tensor
+ *     cores, smaller groups on the CUDA cores -- the tensor cores only where
+ *     the group is a real dense contraction;
+ *   MOE_WIDE_CUDA_CORES: every group on the CUDA cores;
+ *   MOE_WIDE_TENSOR_CORES: every group on the tensor cores.
+ * Other shapes and formats always use the CUDA-core kernels.  Host only;
+ * affects calls enqueued afterwards.  MOE_ERR_INVALID_ARG for another mode. */
+enum { MOE_WIDE_AUTO = 0, MOE_WIDE_CUDA_CORES = 1, MOE_WIDE_TENSOR_CORES = 2 };
+MOE_API int moe_cache_set_wide_path(moe_cache* c, int mode);
+
 /* Test hook: make the next moe_gather_missing call fail with MOE_ERR_INJECTED
  * before it enqueues anything (the plan's bookings stay; the caller is
  * expected to call moe_rollback_plan).  n = 0 clears the request. */

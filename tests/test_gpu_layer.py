@@ -404,6 +404,40 @@ def test_wide_decode_step():
     assert s["fetched"] == s["misses"] > 400 and s["evictions"] == 0
 
 
+@pytest.mark.parametrize("routing,batch", [("zipf", 200), ("uniform", 40)])
+def test_wide_step_tensor_cores_and_cuda_cores(routing, batch):
+    """A wide step small enough to check whole on every grouped path: 64 NVFP4
+    experts (H 256, I 128), top-4.  Zipf routing over 200 rows gives hot
+    experts more than 32 routes (several route chunks per tile, MMA N of 16 and
+    32) and cold ones a single route, so the automatic mode splits the groups
+    between the two kernel families; uniform routing over 40 rows gives groups
+    of one to a few routes.  The tensor-core mode (tcgen05 for every group),
+    the CUDA-core mode and the automatic mode each match the fp64 layer on
+    every row; slot ids, route groups and state are identical."""
+    import expert_slot_cache_lru_gb300 as m
+    w = synth.scaled(synth.workloads()["wide_decode"], n_experts=64, top_k=4, hidden=256,
+                     inter=128, n_slots=64, batch=batch, routing=routing, prefill_frac=0.0)
+    blobs = synth.HostBlobs(w, pinned=True)
+    modes = [m.MOE_WIDE_TENSOR_CORES, m.MOE_WIDE_CUDA_CORES, m.MOE_WIDE_AUTO]
+    rigs = [Rig(w, blobs=blobs) for _ in modes]
+    ids, wts = synth.make_routing(w, steps=2)
+    for rig, mode in zip(rigs, modes):
+        m.moe_cache_set_wide_path(rig.sc.handle, mode)
+        st = Stepper(rig)
+        for t in range(2):
+            x = synth.make_hidden(w, t)
+            refs = st.step(t, ids[t], wts[t], x)
+            assert _gpu_groups(rig.sc, rig.sc.desc.max_routes) == refs[0]["groups"]
+            ref = rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0])
+            assert_close(st.out[0], ref, w.fmt, f"step {t}, mode {mode}")
+        if routing == "zipf":
+            sizes = [len(r) for _, r in refs[0]["groups"]]
+            assert max(sizes) > 32 and min(sizes) < 8, sizes
+    assert_state_equal(rigs[0].sc, rigs[1].oc)
+    with pytest.raises(m.MoeError):
+        m.moe_cache_set_wide_path(rigs[0].sc.handle, 3)
+
+
 @pytest.mark.slow
 def test_hybrid_capped_prefetch_partial_plus_cpu():
     """Capped fetch (4 per layer) + look-ahead prefetch over 48 bf16 layers:
