@@ -118,7 +118,7 @@ __device__ int select_victims_small(const DevState& st, const PoolKeys<CACHED>& 
     }
     if (lane == 0) sm.wk[w][i] = m;
   }
-  __syncthreads();
+  sync_nt<NT>();
   if (w == 0) {
     constexpr int NW = NT / 32;  // one list per warp, lanes past NW hold none
     int h = 0, n = 0;
@@ -135,7 +135,7 @@ __device__ int select_victims_small(const DevState& st, const PoolKeys<CACHED>& 
     }
     if (lane == 0) sm.nvict = n;
   }
-  __syncthreads();
+  sync_nt<NT>();
   return sm.nvict;
 }
 
@@ -180,7 +180,7 @@ __device__ int select_victims(const DevState& st, const PoolKeys<CACHED>& key, i
     const int nbits = 64 - __clzll((long long)range);
     for (int shift = ((nbits - 1) / 10) * 10; shift >= 0; shift -= 10) {
       for (int i = tid; i < kRadixBins; i += NT) sm.bins[i] = 0;
-      __syncthreads();
+      sync_nt<NT>();
       for (int s = s0; s < s1; ++s) {
         const unsigned long long t = key(s);
         if (t == ~0ull) continue;
@@ -188,7 +188,7 @@ __device__ int select_victims(const DevState& st, const PoolKeys<CACHED>& key, i
         const bool match = (shift + 10 >= 64) || ((rel >> (shift + 10)) == (prefix >> (shift + 10)));
         if (match) atomicAdd(&sm.bins[(rel >> shift) & 1023], 1);
       }
-      __syncthreads();
+      sync_nt<NT>();
       // bins [tid * BPT, tid * BPT + BPT) belong to this thread, in order
       constexpr int BPT = kRadixBins / NT;
       int cb[BPT], c = 0;
@@ -204,10 +204,10 @@ __device__ int select_victims(const DevState& st, const PoolKeys<CACHED>& key, i
         }
         ex += cb[j];
       }
-      __syncthreads();
+      sync_nt<NT>();
       prefix |= (unsigned long long)sm.digit << shift;
       k = sm.krem;
-      __syncthreads();
+      sync_nt<NT>();
     }
   }
   // k is in [1, n] by construction; the clamp keeps every index below in
@@ -244,7 +244,7 @@ __device__ int select_victims(const DevState& st, const PoolKeys<CACHED>& key, i
       ++q;
     }
   }
-  __syncthreads();
+  sync_nt<NT>();
   // order the (few) older victims by (stamp, slot)
   for (int i = tid; i < below; i += NT) {
     const unsigned long long ti = lo_t[i];
@@ -256,7 +256,7 @@ __device__ int select_victims(const DevState& st, const PoolKeys<CACHED>& key, i
     }
     vict[rank] = si;
   }
-  __syncthreads();
+  sync_nt<NT>();
   return n;
 }
 
@@ -330,7 +330,7 @@ __device__ void admit_body(const DevState& st, int layer, const int32_t* ids, in
   }
   if (tid < 6) s_acc[tid] = 0;
   for (int e = tid; e < E; e += NT) cnt[e] = 0;
-  __syncthreads();
+  sync_nt<NT>();
 
   // histogram of the valid ids; ids outside [0, E) are counted and dropped
   int inv = 0;
@@ -347,7 +347,7 @@ __device__ void admit_body(const DevState& st, int layer, const int32_t* ids, in
     if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
     else ++inv;
   }
-  __syncthreads();
+  sync_nt<NT>();
 
   // distinct experts (contiguous chunk per thread): counters, lookup, hits
   int nd = 0, nh = 0, nm = 0;
@@ -407,7 +407,7 @@ __device__ void admit_body(const DevState& st, int layer, const int32_t* ids, in
     st.plan_demand[1 + 3 * i + 1] = layer;
     st.plan_demand[1 + 3 * i + 2] = e;
   }
-  __syncthreads();
+  sync_nt<NT>();
 
   // rewrite routes to slots (in place allowed: each thread reads then writes its own r)
   int ov = 0;
@@ -437,7 +437,7 @@ __device__ void admit_body(const DevState& st, int layer, const int32_t* ids, in
   if (nh) atomicAdd(&s_acc[2], nh);
   if (nev) atomicAdd(&s_acc[3], nev);
   if (ov) atomicAdd(&s_acc[4], ov);
-  __syncthreads();
+  sync_nt<NT>();
   if (tid == 0) {  // the counters as loaded at entry, plus this call
     moe_stats v;
     memcpy(&v, s_st, sizeof v);
@@ -489,14 +489,14 @@ __device__ void prefetch_body(const DevState& st, int layer, const int32_t* pred
 
   if (tid < 3) s_acc[tid] = 0;
   for (int e = tid; e < E; e += NT) cnt[e] = 0;
-  __syncthreads();
+  sync_nt<NT>();
   int inv = 0;
   for (int i = tid; i < n; i += NT) {
     const int e = pred[i];
     if ((unsigned)e < (unsigned)E) cnt[e] = 1;
     else ++inv;
   }
-  __syncthreads();
+  sync_nt<NT>();
   const int ept = (E + NT - 1) / NT;
   const int e0 = min(E, tid * ept), e1 = min(E, e0 + ept);
   int nreq = 0, nres = 0, nq = 0;

@@ -152,9 +152,9 @@ __global__ void __launch_bounds__(kGT) group_kernel(DevState st, int layer,
     nd += dense_from > 0 && off[e] >= dense_from;
   }
   int totR, totG, totD;
-  int r0 = block_excl_scan(nr, bs, &totR);
-  int g0 = block_excl_scan(ng, bs, &totG);
-  int d0 = block_excl_scan(nd, bs, &totD);
+  int r0 = block_excl_scan<kGT>(nr, bs, &totR);
+  int g0 = block_excl_scan<kGT>(ng, bs, &totG);
+  int d0 = block_excl_scan<kGT>(nd, bs, &totD);
   for (int e = e0; e < e1; ++e) {
     const int c = off[e];
     if (c > 0) {
