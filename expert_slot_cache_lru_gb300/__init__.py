@@ -106,7 +106,6 @@ _SIGS = {
     "moe_hybrid_pause": [_vp, _i],
     "moe_schedule_trace": [_i, _i, _i, _i, _i, _i, _i, _vp, _i],
     "moe_decode_layer_plan": [_vp, _i, _i, _i, _i, _u, _vp, _i],
-    "moe_stream_split": [_vp, _i, _i, _i, _i, _vp],
     "moe_hybrid_selftest": [_i, _i, _i, _vp, _i, _i, _i, _i, _i, _u, _vp],
     "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
@@ -293,18 +292,6 @@ def moe_decode_layer_plan(cache: int, n_rows: int, k: int, shared: bool = False,
     _check("moe_decode_layer_plan", _lib.moe_decode_layer_plan(
         cache, n_rows, k, int(shared), int(pf), flags, buf, len(buf)))
     return buf.value.decode().split()
-
-
-def moe_stream_split(cache: int, n_rows: int, k: int, shared: bool = False,
-                     one_launch: bool = False) -> dict:
-    """The decode-sized expert kernel's work split on this GPU (see moe_cache.h)."""
-    import numpy as np
-    out = np.zeros(6, np.int32)
-    _check("moe_stream_split", _lib.moe_stream_split(cache, n_rows, k, int(shared),
-                                                     int(one_launch), out.ctypes.data))
-    return {"routed_parts": int(out[0]), "shared_parts": int(out[1]), "units": int(out[2]),
-            "clusters": int(out[3]), "one_round": bool(out[4]),
-            "resident_clusters": int(out[5])}
 
 
 def moe_hybrid_counters(cache: int) -> dict:

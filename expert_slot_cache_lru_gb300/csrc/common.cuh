@@ -167,9 +167,6 @@ struct FfnScratch {
   uint16_t* h16;    // [max_routes * I] h as f16 for the tensor-core down GEMM
   float* hinv;      // [max_routes] inverse of each route's h scale
   int32_t* dense;   // [1 + max_routes] the groups the tensor-core kernels take: count, ids
-  unsigned long long* acc;  // [max_rows][H] the streaming kernel's fixed-point layer sums (zero
-                            // between launches)
-  unsigned* slice_cnt;  // [4] its units done per output slice (zero between launches)
   int* gdone;       // [max_routes] pieces of each demand-plan expert copied by a fused layer
   // a fused layer with the admission inside the launch (three counters that only grow)
   unsigned long long* epoch;   // launches (each CTA adds one)
@@ -193,24 +190,14 @@ cudaError_t launch_routed_down_combine(const DevState& st, int wfmt, int H, int 
 
 // Streaming expert FFNs for decode-sized steps (ffn_stream.cu).
 bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks);
-cudaError_t ffn_stream_init();  // once per device: kernel limits, resident clusters
-int ffn_stream_max_parts(int I);  // parts of I a task is cut into, at most
-bool ffn_stream_split(int mode_layer, int admit, int wfmt, int H, int I, int n_rows, int k,
-                      bool shared, int out[6]);
-// to_ys: write the gated shared expert into sc.ys (float); else leave it in
-// the layer's fixed-point sums for the streaming routed launch to add on
+cudaError_t ffn_stream_init();
 cudaError_t launch_shared_stream(const DevState& st, int wfmt, int H, int Is, const void* x,
-                                 int n_rows, int k_layer, bool to_ys, const uint8_t* blob,
-                                 const void* gate_w, FfnScratch sc, unsigned long long* status,
-                                 cudaStream_t s);
-// layer_shared: the layer has a shared expert (the tasks are split as in its
-// one-launch form); shared_y: the gated shared expert in float, added to the
-// output (null: none, or already in the fixed-point sums)
+                                 int n_rows, const uint8_t* blob, const void* gate_w,
+                                 FfnScratch sc, unsigned long long* status, cudaStream_t s);
 cudaError_t launch_routed_stream(const DevState& st, int wfmt, int H, int I, int layer,
                                  const void* x, const int32_t* slot_ids, const float* w,
-                                 int n_rows, int k, bool layer_shared, const float* shared_y,
-                                 void* out, FfnScratch sc, unsigned long long* status,
-                                 cudaStream_t s);
+                                 int n_rows, int k, const float* shared_y, void* out,
+                                 FfnScratch sc, unsigned long long* status, cudaStream_t s);
 
 // One launch for a whole decode-sized layer after its admission: the demand
 // (and prefetch) gather, the shared expert and the routed experts (ffn_stream.cu).
@@ -260,7 +247,6 @@ cudaError_t launch_grouped_tc(const DevState& st, int H, int I, int layer, int k
 // Allocation-free routed FFN (ffn_stream.cu): the scratch is a file-scope
 // device array whose address noalloc_scratch looks up once per device.
 cudaError_t noalloc_scratch(void** out);
-size_t noalloc_scratch_bytes(int wfmt, int H, int I, int n_rows, int k);  // 0: shape not taken
 cudaError_t launch_routed_noalloc(int wfmt, int H, int I, const uint8_t* slots, size_t stride,
                                   int n_slots, const void* x, const int32_t* slot_ids,
                                   const float* w, int n_rows, int k, void* out,

@@ -180,8 +180,6 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_h16 = cv.take<uint16_t>((size_t)d.max_routes * std::max(I, 1)),
                o_hinv = cv.take<float>(d.max_routes),
                o_dense = cv.take<int32_t>(1 + (size_t)d.max_routes),
-               o_acc = cv.take<unsigned long long>((size_t)d.max_rows * std::max(H, 1)),
-               o_slice = cv.take<unsigned>(64),
                o_status = cv.take<unsigned long long>(1),
                o_bar = cv.take<unsigned long long>(1),
                o_ep = cv.take<unsigned long long>(1), o_pseq = cv.take<unsigned long long>(1),
@@ -236,8 +234,6 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.h16 = reinterpret_cast<uint16_t*>(m + o_h16);
   c->sc.hinv = reinterpret_cast<float*>(m + o_hinv);
   c->sc.dense = reinterpret_cast<int32_t*>(m + o_dense);
-  c->sc.acc = reinterpret_cast<unsigned long long*>(m + o_acc);
-  c->sc.slice_cnt = reinterpret_cast<unsigned*>(m + o_slice);
   c->sc.gdone = reinterpret_cast<int*>(m + o_gdone);
 
   // initial state: nothing resident, every clock at 1
@@ -413,26 +409,13 @@ static int check_compute(moe_cache* c, int layer, int n_rows, int k, const void*
   return MOE_OK;
 }
 
-// k: the layer's top-k (the streaming kernel splits the shared expert as the
-// layer's one-launch form would)
-// The streaming kernel takes the shared expert / the routed experts of this shape.
-static bool shared_streams(const moe_cache* c, int n_rows) {
-  return c->stream_ffn &&
-         moe::ffn_stream_supported(c->d.wfmt, c->d.hidden, c->d.shared_inter, n_rows, n_rows);
-}
-static bool routed_streams(const moe_cache* c, int n_rows, int k) {
-  return c->stream_ffn && moe::ffn_stream_supported(c->d.wfmt, c->d.hidden, c->d.inter, n_rows, n_rows * k);
-}
-
-static int run_shared(moe_cache* c, const void* d_x, int n_rows, int k, const void* blob,
-                      const void* gate, cudaStream_t s) {
+static int run_shared(moe_cache* c, const void* d_x, int n_rows, const void* blob, const void* gate,
+                      cudaStream_t s) {
   if (n_rows == 0) return MOE_OK;
-  if (shared_streams(c, n_rows)) {
-    // into the layer's fixed-point sums when the routed experts stream too
-    // (the routed launch adds on and converts), else into ys
-    CK(moe::launch_shared_stream(c->st, c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows, k,
-                                 !routed_streams(c, n_rows, k), static_cast<const uint8_t*>(blob),
-                                 gate, c->sc, c->st.status, s));
+  if (c->stream_ffn &&
+      moe::ffn_stream_supported(c->d.wfmt, c->d.hidden, c->d.shared_inter, n_rows, n_rows)) {
+    CK(moe::launch_shared_stream(c->st, c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows,
+                                 static_cast<const uint8_t*>(blob), gate, c->sc, c->st.status, s));
     return MOE_OK;
   }
   if (c->d.wfmt != MOE_W_BF16 && c->d.wfmt != MOE_W_NVFP4)  // streaming kernels only
@@ -447,13 +430,9 @@ static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* s
                       cudaStream_t s) {
   const moe_cache_desc& d = c->d;
   if (n_rows == 0) return MOE_OK;
-  if (routed_streams(c, n_rows, k)) {
-    // a shared expert that streamed is in the fixed-point sums already; one
-    // from the other kernels is in ys
-    const bool ys = with_shared && !shared_streams(c, n_rows);
+  if (c->stream_ffn && moe::ffn_stream_supported(d.wfmt, d.hidden, d.inter, n_rows, n_rows * k)) {
     CK(moe::launch_routed_stream(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w, n_rows,
-                                 k, with_shared, ys ? c->sc.ys : nullptr, d_out, c->sc,
-                                 c->st.status, s));
+                                 k, with_shared ? c->sc.ys : nullptr, d_out, c->sc, c->st.status, s));
     return MOE_OK;
   }
   if (d.wfmt != MOE_W_BF16 && d.wfmt != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;  // streaming only
@@ -478,7 +457,7 @@ int moe_routed_experts(moe_cache* c, int layer, const void* d_x, const int32_t* 
   if (rc != MOE_OK) return rc;
   if (n_rows == 0) return MOE_OK;
   if (!d_x || !d_out || (k > 0 && (!d_slot_ids || !d_w)) || d_out == d_x) return MOE_ERR_INVALID_ARG;
-  if (d_shared_blob && (rc = run_shared(c, d_x, n_rows, k, d_shared_blob, d_shared_gate, as_stream(stream))))
+  if (d_shared_blob && (rc = run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, as_stream(stream))))
     return rc;
   return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr, d_out,
                     as_stream(stream));
@@ -499,8 +478,8 @@ int moe_routed_experts_noalloc(int wfmt, int hidden, int inter, const void* d_sl
   if (!d_x || !d_out || d_out == d_x || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
       (k > 0 && (!d_slot_ids || !d_w)))
     return MOE_ERR_INVALID_ARG;
-  // the counters and one int64 sum per output element (checked before any CUDA call)
-  if (256 + (size_t)n_rows * (size_t)hidden * 8 > MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_SCRATCH;
+  if (256 + (size_t)n_rows * (size_t)k * (size_t)inter * sizeof(float) > MOE_NOALLOC_SCRATCH_BYTES)
+    return MOE_ERR_SCRATCH;
   void* scratch = nullptr;
   CK(moe::noalloc_scratch(&scratch));
   if (!moe::ffn_stream_supported(wfmt, hidden, inter, n_rows, n_rows * k)) return MOE_ERR_UNSUPPORTED;
@@ -614,7 +593,7 @@ struct CudaOps : LayerOps {
         CK(moe::launch_gather(c->st, pf_plan, c->gather_grid, st));
         return MOE_OK;
       case kOpShared:
-        return run_shared(c, d_x, n_rows, k, d_shared_blob, d_shared_gate, st);
+        return run_shared(c, d_x, n_rows, d_shared_blob, d_shared_gate, st);
       case kOpRouted:
         return run_routed(c, layer, d_x, d_slot_ids, d_w, n_rows, k, d_shared_blob != nullptr,
                           d_out, st);
@@ -722,16 +701,6 @@ int moe_schedule_trace(int one_launch, int fused, int overlap, int pf, int share
   if ((int)ops.out.size() >= cap) return MOE_ERR_CAPACITY;
   std::memcpy(h_out, ops.out.c_str(), ops.out.size() + 1);
   return rc;
-}
-
-int moe_stream_split(moe_cache* c, int n_rows, int k, int shared, int one_launch, int h_out[6]) {
-  if (!c || !h_out || n_rows < 1 || k < 0) return MOE_ERR_INVALID_ARG;
-  const moe_cache_desc& d = c->d;
-  const int layer = shared || one_launch;
-  if (!moe::ffn_stream_split(layer, one_launch, d.wfmt, d.hidden, d.inter, n_rows, k,
-                             shared != 0, h_out))
-    return MOE_ERR_UNSUPPORTED;
-  return MOE_OK;
 }
 
 int moe_decode_layer_plan(moe_cache* c, int n_rows, int k, int shared, int pf, unsigned flags,

@@ -413,18 +413,6 @@ MOE_API int moe_schedule_trace(int one_launch, int fused, int overlap, int pf, i
 MOE_API int moe_decode_layer_plan(moe_cache* c, int n_rows, int k, int shared, int pf,
                                   unsigned flags, char* h_out, int cap);
 
-/* Host only, for tests and profiling: the work split of the decode-sized
- * expert kernel on this cache's GPU for n_rows x k routes, with (shared != 0)
- * or without the shared expert, as the one-launch layer (one_launch != 0) or
- * the routed launch.  h_out = {parts a routed expert's intermediate is cut
- * into, parts of the shared expert's, units of the launch, its clusters, 1 if
- * every unit has a cluster of its own, clusters of 4 CTAs resident on the GPU
- * at once}.  The parts depend on the layer's shape only, so every launch mode
- * sums a task alike.  MOE_ERR_UNSUPPORTED if the kernel does not take the
- * shape. */
-MOE_API int moe_stream_split(moe_cache* c, int n_rows, int k, int shared, int one_launch,
-                             int h_out[6]);
-
 /* Copy one layer's counters to the host.  Synchronises the device. */
 MOE_API int moe_read_stats(moe_cache* c, int layer, moe_stats* h_out);
 
@@ -467,12 +455,12 @@ MOE_API int moe_cache_fail_next_gather(moe_cache* c, int n);
  * and scratch, and a cudaFree synchronises the device, so neither fits there.
  *
  * Scratch: a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES (1 MiB).
- * Bytes [0, 256) hold the kernel's output-slice counters and the bytes after
- * them its fixed-point layer sums, one int64 per output element
- * [n_rows][hidden].  A request needs 256 + 8 * n_rows * hidden bytes; a
- * larger one returns MOE_ERR_SCRATCH before anything is enqueued (before any
- * CUDA call).  Each call clears the counters and the sums with one
- * cudaMemsetAsync on `stream` before the kernel.
+ * Bytes [0, 256) hold the kernel's grid-barrier counter and bytes [256, 1 MiB)
+ * hold the fp32 intermediate h [n_rows*k][inter].  A request needs
+ * 256 + 4*n_rows*k*inter bytes; a larger one returns MOE_ERR_SCRATCH before
+ * anything is enqueued.  Each call clears the counter with a cudaMemsetAsync
+ * on `stream` before the kernel; h needs no clearing (every element read is
+ * written first in the same launch).
  *
  * Set-up: the first call on each device (that device current) looks up the
  * array's address with cudaGetSymbolAddress and sets the kernel's shared

@@ -159,12 +159,11 @@ def test_noalloc_host_checks_without_a_device():
             m.moe_routed_experts_noalloc(**a)
         return e.value.code
 
-    # 256 bytes of counters + one int64 sum per output element: 16 rows x 16384 x 8 > 1 MiB
-    big = dict(hidden=16384, slot_stride=(synth.blob_bytes(fmt, 16384, I) + 255) // 256 * 256)
-    assert call(n_rows=16, k=4, **big) == m.MOE_ERR_SCRATCH
-    limit = (m.MOE_NOALLOC_SCRATCH_BYTES - 256) // 8
-    big_h = (limit // 32 + 1) * 32  # one row's sums alone are over the limit
-    assert call(n_rows=1, k=1, hidden=big_h, slot_stride=1 << 30) == m.MOE_ERR_SCRATCH
+    # 16 rows x 64 routes x 512 x 4 bytes = 2 MiB > 1 MiB of scratch
+    assert call(n_rows=16, k=64) == m.MOE_ERR_SCRATCH
+    limit = (m.MOE_NOALLOC_SCRATCH_BYTES - 256) // 4
+    assert call(n_rows=1, k=1, inter=(limit // 32 + 1) * 32,
+                slot_stride=1 << 30) == m.MOE_ERR_SCRATCH
     assert "1 MiB" in m.moe_strerror(m.MOE_ERR_SCRATCH)
     assert call(slot_stride=stride - 256) == m.MOE_ERR_INVALID_ARG
     assert call(slot_stride=stride + 16) == m.MOE_ERR_INVALID_ARG
