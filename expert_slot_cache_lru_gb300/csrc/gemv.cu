@@ -10,13 +10,17 @@
 // section 5]: a route whose slot id is -1 contributes nothing on the GPU.
 //
 // Work split: one warp per output row.  Weights stream through 128-bit loads
-// (NVFP4: 32 e2m1 codes and their two e4m3 scales per lane per step; bf16:
-// 32 elements per lane per step), the activation vector sits in shared memory
-// as fp32, and each warp reduces its row with shuffles.  Accumulation is fp32;
-// the e2m1 x e4m3 x bf16 products are exact in fp32.
+// (4-bit formats: 32 codes and their scales per lane per step; bf16: 32
+// elements per lane per step), the activation vector sits in shared memory
+// as fp32, and each warp reduces its row with shuffles.  Accumulation is fp32.
+// NVFP4 blocks are 16 codes with an e4m3 scale and a global scale per matrix;
+// MXFP4 blocks 32 e2m1 codes with an E8M0 power of two; Q4_0 blocks 32
+// unsigned codes q with an fp16 scale d (weight d (q - 8)).
 #include <cuda_bf16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -51,6 +55,20 @@ __device__ __forceinline__ float dot8_e2m1(uint32_t w, const float* xs) {
   return acc;
 }
 
+// sum_{i<8} (q_i - 8) * xs[i], q_i = nibble i of the word (element i)
+__device__ __forceinline__ float dot8_q4(uint32_t w, const float* xs) {
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc = fmaf((float)((int)((w >> (4 * i)) & 0xFu) - 8), xs[i], acc);
+  return acc;
+}
+// an E8M0 scale: 2^(e - 127); 0xFF is NaN
+__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
+  return e == 0 ? __uint_as_float(0x00400000u)
+                : (e == 255 ? __uint_as_float(0x7fffffffu) : __uint_as_float(e << 23));
+}
+__device__ __forceinline__ float f16_bits_to_f32(uint16_t v) { return __half2float(__ushort_as_half(v)); }
+
 // sum_{i<8} bf16(pair words) * xs[i]
 __device__ __forceinline__ float dot8_bf16(uint4 v, const float* xs) {
   float acc = 0.f;
@@ -69,20 +87,36 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Byte offsets inside an NVFP4 blob (see the layout in moe_cache.h).
+// Byte offsets inside a 4-bit blob (see the layouts in moe_cache.h): three
+// code banks, then three scale banks of ih/16 bytes (NVFP4: e4m3 per 16;
+// Q4_0: fp16 per 32) or ih/32 (MXFP4: E8M0 per 32), then NVFP4's globals.
 struct Nvfp4Off {
   size_t code[3], scale[3], glob;
-  __device__ Nvfp4Off(int H, int I) {
+  __device__ Nvfp4Off(int H, int I, int fmt = MOE_W_NVFP4) {
     const size_t ih = (size_t)I * H;
+    const size_t sb = ih / (fmt == MOE_W_MXFP4 ? 32 : 16);
     code[0] = 0;
     code[1] = ih / 2;
     code[2] = ih;
     scale[0] = 3 * ih / 2;
-    scale[1] = scale[0] + ih / 16;
-    scale[2] = scale[1] + ih / 16;
-    glob = scale[2] + ih / 16;
+    scale[1] = scale[0] + sb;
+    scale[2] = scale[1] + sb;
+    glob = scale[2] + sb;
   }
 };
+// the scale of 32-element block j of a row of MXFP4 or Q4_0 scales
+template <int FMT>
+__device__ __forceinline__ float scale32(const uint8_t* scales, int j) {
+  if (FMT == MOE_W_MXFP4) return e8m0_to_f32(scales[j]);
+  return f16_bits_to_f32(reinterpret_cast<const uint16_t*>(scales)[j]);
+}
+// 32 codes of a 4-bit row dotted with 32 fp32 activations, before the scale
+template <int FMT>
+__device__ __forceinline__ float dot32_codes(uint4 c, const float* x) {
+  if (FMT == MOE_W_Q4_0)
+    return (dot8_q4(c.x, x) + dot8_q4(c.y, x + 8)) + (dot8_q4(c.z, x + 16) + dot8_q4(c.w, x + 24));
+  return (dot8_e2m1(c.x, x) + dot8_e2m1(c.y, x + 8)) + (dot8_e2m1(c.z, x + 16) + dot8_e2m1(c.w, x + 24));
+}
 
 // Dot of row n of an [rows, K] matrix with the fp32 vector xs[K] (in shared
 // memory), partial per lane; the caller reduces.  K is a multiple of 32.
@@ -103,6 +137,14 @@ __device__ __forceinline__ float row_dot_k32(const uint8_t* blob, int which, int
       const float p1 = dot8_e2m1(c.z, x + 16) + dot8_e2m1(c.w, x + 24);
       acc = fmaf(p0, e4m3_to_f32((uint8_t)(sc & 0xff)), acc);
       acc = fmaf(p1, e4m3_to_f32((uint8_t)(sc >> 8)), acc);
+    }
+  } else if (FMT == MOE_W_MXFP4 || FMT == MOE_W_Q4_0) {
+    const Nvfp4Off o(H, I, FMT);
+    const uint8_t* codes = blob + o.code[which] + (size_t)n * (K / 2);
+    const uint8_t* scales = blob + o.scale[which] + (size_t)n * (K / 32) * (FMT == MOE_W_Q4_0 ? 2 : 1);
+    for (int base = lane * 32; base < K; base += 1024) {
+      const uint4 c = *reinterpret_cast<const uint4*>(codes + base / 2);
+      acc = fmaf(dot32_codes<FMT>(c, xs + base), scale32<FMT>(scales, base / 32), acc);
     }
   } else {
     const size_t mat = (size_t)which * H * I * 2;
@@ -133,6 +175,15 @@ __device__ __forceinline__ float row_dot_k16(const uint8_t* blob, int which, int
       const float* x = xs + base;
       const float p = dot8_e2m1(c.x, x) + dot8_e2m1(c.y, x + 8);
       acc = fmaf(p, e4m3_to_f32(scales[base / 16]), acc);
+    }
+  } else if (FMT == MOE_W_MXFP4 || FMT == MOE_W_Q4_0) {
+    // 32-element blocks, one per lane per step (K a multiple of 32)
+    const Nvfp4Off o(H, I, FMT);
+    const uint8_t* codes = blob + o.code[which] + (size_t)n * (K / 2);
+    const uint8_t* scales = blob + o.scale[which] + (size_t)n * (K / 32) * (FMT == MOE_W_Q4_0 ? 2 : 1);
+    for (int base = lane * 32; base < K; base += 1024) {
+      const uint4 c = *reinterpret_cast<const uint4*>(codes + base / 2);
+      acc = fmaf(dot32_codes<FMT>(c, xs + base), scale32<FMT>(scales, base / 32), acc);
     }
   } else {
     const size_t mat = (size_t)which * H * I * 2;
@@ -253,21 +304,34 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+template <int FMT>
+cudaError_t set_limits_fmt(size_t xb, size_t hb, size_t sb) {
+  cudaError_t e = set_smem(up_kernel<FMT, false>, xb);
+  if (e == cudaSuccess) e = set_smem(up_kernel<FMT, true>, xb);
+  if (e == cudaSuccess) e = set_smem(down_combine_kernel<FMT>, hb);
+  if (e == cudaSuccess) e = set_smem(shared_down_kernel<FMT>, sb);
+  return e;
+}
+
+// f(std::integral_constant<int, FMT>) for the format wfmt
+template <typename F>
+cudaError_t by_format(int wfmt, F f) {
+  switch (wfmt) {
+    case MOE_W_NVFP4: return f(std::integral_constant<int, MOE_W_NVFP4>{});
+    case MOE_W_MXFP4: return f(std::integral_constant<int, MOE_W_MXFP4>{});
+    case MOE_W_Q4_0: return f(std::integral_constant<int, MOE_W_Q4_0>{});
+    default: return f(std::integral_constant<int, MOE_W_BF16>{});
+  }
+}
+
 }  // namespace
 
 cudaError_t gemv_set_smem_limits(int H, int I, int Is, int k_max) {
+  const size_t xb = (size_t)H * 4, hb = (size_t)k_max * I * 4, sb = (size_t)Is * 4;
   cudaError_t e = cudaSuccess;
-  const size_t xb = (size_t)H * 4;
-  if (e == cudaSuccess) e = set_smem(up_kernel<MOE_W_BF16, false>, xb);
-  if (e == cudaSuccess) e = set_smem(up_kernel<MOE_W_NVFP4, false>, xb);
-  if (e == cudaSuccess) e = set_smem(up_kernel<MOE_W_BF16, true>, xb);
-  if (e == cudaSuccess) e = set_smem(up_kernel<MOE_W_NVFP4, true>, xb);
-  const size_t hb = (size_t)k_max * I * 4;
-  if (e == cudaSuccess) e = set_smem(down_combine_kernel<MOE_W_BF16>, hb);
-  if (e == cudaSuccess) e = set_smem(down_combine_kernel<MOE_W_NVFP4>, hb);
-  const size_t sb = (size_t)Is * 4;
-  if (e == cudaSuccess) e = set_smem(shared_down_kernel<MOE_W_BF16>, sb);
-  if (e == cudaSuccess) e = set_smem(shared_down_kernel<MOE_W_NVFP4>, sb);
+  for (int f : {MOE_W_BF16, MOE_W_NVFP4, MOE_W_MXFP4, MOE_W_Q4_0})
+    if (e == cudaSuccess)
+      e = by_format(f, [&](auto fmt) { return set_limits_fmt<decltype(fmt)::value>(xb, hb, sb); });
   return e;
 }
 
@@ -279,18 +343,13 @@ cudaError_t launch_shared_expert(int wfmt, int H, int Is, const void* x, int n_r
   const dim3 gd((H + kWarps - 1) / kWarps, n_rows);
   const uint16_t* xx = static_cast<const uint16_t*>(x);
   const uint16_t* gw = static_cast<const uint16_t*>(gate_w);
-  if (wfmt == MOE_W_NVFP4) {
-    up_kernel<MOE_W_NVFP4, true><<<gu, kThreads, (size_t)H * 4, s>>>(none, H, Is, 0, xx, nullptr,
-                                                                     1, blob, gw, sc.hs, sc.gate);
-    shared_down_kernel<MOE_W_NVFP4><<<gd, kThreads, (size_t)Is * 4, s>>>(H, Is, blob, sc.hs,
-                                                                         sc.gate, sc.ys);
-  } else {
-    up_kernel<MOE_W_BF16, true><<<gu, kThreads, (size_t)H * 4, s>>>(none, H, Is, 0, xx, nullptr,
-                                                                    1, blob, gw, sc.hs, sc.gate);
-    shared_down_kernel<MOE_W_BF16><<<gd, kThreads, (size_t)Is * 4, s>>>(H, Is, blob, sc.hs,
-                                                                        sc.gate, sc.ys);
-  }
-  return cudaGetLastError();
+  return by_format(wfmt, [&](auto fmt) {
+    constexpr int F = decltype(fmt)::value;
+    up_kernel<F, true><<<gu, kThreads, (size_t)H * 4, s>>>(none, H, Is, 0, xx, nullptr, 1, blob,
+                                                           gw, sc.hs, sc.gate);
+    shared_down_kernel<F><<<gd, kThreads, (size_t)Is * 4, s>>>(H, Is, blob, sc.hs, sc.gate, sc.ys);
+    return cudaGetLastError();
+  });
 }
 
 cudaError_t launch_routed_up(const DevState& st, int wfmt, int H, int I, int layer,
@@ -298,15 +357,11 @@ cudaError_t launch_routed_up(const DevState& st, int wfmt, int H, int I, int lay
                              FfnScratch sc, cudaStream_t s) {
   const dim3 g((I + kWarps - 1) / kWarps, n_rows * k);
   const uint16_t* xx = static_cast<const uint16_t*>(x);
-  if (wfmt == MOE_W_NVFP4)
-    up_kernel<MOE_W_NVFP4, false><<<g, kThreads, (size_t)H * 4, s>>>(st, H, I, layer, xx, slot_ids,
-                                                                     k, nullptr, nullptr, sc.h,
-                                                                     nullptr);
-  else
-    up_kernel<MOE_W_BF16, false><<<g, kThreads, (size_t)H * 4, s>>>(st, H, I, layer, xx, slot_ids,
-                                                                    k, nullptr, nullptr, sc.h,
-                                                                    nullptr);
-  return cudaGetLastError();
+  return by_format(wfmt, [&](auto fmt) {
+    up_kernel<decltype(fmt)::value, false><<<g, kThreads, (size_t)H * 4, s>>>(
+        st, H, I, layer, xx, slot_ids, k, nullptr, nullptr, sc.h, nullptr);
+    return cudaGetLastError();
+  });
 }
 
 cudaError_t launch_routed_down_combine(const DevState& st, int wfmt, int H, int I, int layer,
@@ -316,13 +371,11 @@ cudaError_t launch_routed_down_combine(const DevState& st, int wfmt, int H, int 
   const dim3 g((H + kWarps - 1) / kWarps, n_rows);
   const size_t smem = (size_t)k * I * 4;
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-  if (wfmt == MOE_W_NVFP4)
-    down_combine_kernel<MOE_W_NVFP4><<<g, kThreads, smem, s>>>(st, H, I, layer, slot_ids, w, k,
-                                                               sc.h, shared_y, o);
-  else
-    down_combine_kernel<MOE_W_BF16><<<g, kThreads, smem, s>>>(st, H, I, layer, slot_ids, w, k,
-                                                              sc.h, shared_y, o);
-  return cudaGetLastError();
+  return by_format(wfmt, [&](auto fmt) {
+    down_combine_kernel<decltype(fmt)::value><<<g, kThreads, smem, s>>>(st, H, I, layer, slot_ids,
+                                                                        w, k, sc.h, shared_y, o);
+    return cudaGetLastError();
+  });
 }
 
 }  // namespace moe

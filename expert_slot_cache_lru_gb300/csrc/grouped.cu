@@ -14,7 +14,7 @@
 // therefore group the routes by expert and read each expert's weights once:
 //   1. group_kernel   (1 CTA): the CSR of routes per distinct expert, ascending
 //      expert id, routes ascending within a group -- the cache's route groups;
-//   2. xprep_kernel:  x as f16 (NVFP4 experts; per-row power-of-two scale so
+//   2. xprep_kernel:  x as f16 (4-bit experts; per-row power-of-two scale so
 //      that max |x| < 2^15, undone on the fp32 sums) or bf16 (bf16 experts);
 //   3. gup_kernel:    per (group, 256 rows of I): h[r] = silu(W_g x_b) * (W_u x_b)
 //      for every route r of the group, one row per thread -- each weight block
@@ -25,6 +25,8 @@
 // the data-dependent number of groups needs no host round trip.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -86,23 +88,63 @@ __device__ __forceinline__ float fma2b(uint32_t w2, uint32_t x2, float c) {
 }
 __device__ __forceinline__ float fp32_of_bf16(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
-// Offsets inside a blob (layout of moe_cache.h).
+// Offsets inside a blob (layout of moe_cache.h): the scale banks hold ih/16
+// bytes (NVFP4: e4m3 per 16; Q4_0: fp16 per 32) or ih/32 (MXFP4: E8M0 per 32).
 struct Off {
   size_t code[3], scale[3], glob, mat[3];
-  __device__ Off(int H, int I) {
+  __device__ Off(int H, int I, int fmt = MOE_W_NVFP4) {
     const size_t ih = (size_t)I * H;
+    const size_t sb = ih / (fmt == MOE_W_MXFP4 ? 32 : 16);
     code[0] = 0;
     code[1] = ih / 2;
     code[2] = ih;
     scale[0] = 3 * ih / 2;
-    scale[1] = scale[0] + ih / 16;
-    scale[2] = scale[1] + ih / 16;
-    glob = scale[2] + ih / 16;
+    scale[1] = scale[0] + sb;
+    scale[2] = scale[1] + sb;
+    glob = scale[2] + sb;
     mat[0] = 0;
     mat[1] = ih * 2;
     mat[2] = ih * 4;
   }
 };
+
+// MXFP4 and Q4_0: 32-element blocks.  The scale of block j of a row's scales
+// (E8M0 2^(e - 127), 0xFF NaN; or fp16 d), and a block's 32 codes (16 bytes)
+// as 16 half2 words: e2m1 values, or q - 8 for Q4_0 (exact in f16).
+template <int FMT>
+__device__ __forceinline__ float blk32_scale(const uint8_t* scales, int j) {
+  if (FMT == MOE_W_MXFP4) {
+    const uint32_t e = scales[j];
+    return e == 0 ? __uint_as_float(0x00400000u)
+                  : (e == 255 ? __uint_as_float(0x7fffffffu) : __uint_as_float(e << 23));
+  }
+  return __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(scales)[j]));
+}
+template <int FMT>
+__device__ __forceinline__ void blk32_decode(uint4 c, uint32_t d[16]) {
+  const uint32_t v[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int wd = 0; wd < 4; ++wd) {
+    if (FMT == MOE_W_Q4_0) {  // nibbles into the mantissa of f16 1024 + q, minus 1032
+      const uint32_t lo = v[wd] & 0x0F0F0F0Fu, hi = (v[wd] >> 4) & 0x0F0F0F0Fu;
+      const uint32_t m0 = __byte_perm(lo, hi, 0x5140), m1 = __byte_perm(lo, hi, 0x7362);
+      const uint32_t k = 0x64646464u;
+      const uint32_t t[4] = {__byte_perm(m0, k, 0x4140), __byte_perm(m0, k, 0x4342),
+                             __byte_perm(m1, k, 0x4140), __byte_perm(m1, k, 0x4342)};
+      const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&t[q]), bias);
+        d[4 * wd + q] = *reinterpret_cast<const uint32_t*>(&r);
+      }
+    } else {
+      d[4 * wd] = e2m1x2<0>(v[wd]);
+      d[4 * wd + 1] = e2m1x2<1>(v[wd]);
+      d[4 * wd + 2] = e2m1x2<2>(v[wd]);
+      d[4 * wd + 3] = e2m1x2<3>(v[wd]);
+    }
+  }
+}
 
 // The route groups buffer: [G, slot[R], start[R + 1], route[R]], R = max_routes.
 struct Groups {
@@ -322,6 +364,41 @@ __global__ void __launch_bounds__(kWT) gup_kernel(DevState st, int H, int I, int
             }
             ga[j] = fmaf(p, sg.x, fmaf(p2, sg.y, ga[j]));
             ua[j] = fmaf(q, su.x, fmaf(q2, su.y, ua[j]));
+          }
+        }
+      } else if (FMT == MOE_W_MXFP4 || FMT == MOE_W_Q4_0) {
+        // 32-element blocks: codes decoded once, applied to every staged route
+        const Off of(H, I, FMT);
+        const int sbr = (H / 32) * (FMT == MOE_W_Q4_0 ? 2 : 1);  // scale bytes per row
+        const uint8_t* gc = blob + of.code[0] + (size_t)ii * (H / 2);
+        const uint8_t* uc = blob + of.code[1] + (size_t)ii * (H / 2);
+        const uint8_t* gsc = blob + of.scale[0] + (size_t)ii * sbr;
+        const uint8_t* usc = blob + of.scale[1] + (size_t)ii * sbr;
+#pragma unroll 2
+        for (int blk = 0; blk < H / 32; ++blk) {
+          const uint4 gw = *reinterpret_cast<const uint4*>(gc + blk * 16);
+          const uint4 uw = *reinterpret_cast<const uint4*>(uc + blk * 16);
+          const float sg = blk32_scale<FMT>(gsc, blk), su = blk32_scale<FMT>(usc, blk);
+          uint32_t gd[16], ud[16];
+          blk32_decode<FMT>(gw, gd);
+          blk32_decode<FMT>(uw, ud);
+#pragma unroll
+          for (int j = 0; j < kNR; ++j) {
+            if (j >= nq) break;
+            const uint4* xr = xs + (size_t)j * Hu + blk * 4;  // 32 elements = 4 units
+            const uint4 x0 = xr[0], x1 = xr[1], x2 = xr[2], x3 = xr[3];
+            const uint32_t xv[16] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                     x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+            float p = 0.f, q = 0.f, p2 = 0.f, q2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              p = fma2h(gd[e], xv[e], p);
+              q = fma2h(ud[e], xv[e], q);
+              p2 = fma2h(gd[8 + e], xv[8 + e], p2);
+              q2 = fma2h(ud[8 + e], xv[8 + e], q2);
+            }
+            ga[j] = fmaf(p + p2, sg, ga[j]);
+            ua[j] = fmaf(q + q2, su, ua[j]);
           }
         }
       } else {
@@ -581,6 +658,43 @@ __global__ void __launch_bounds__(kWT) gdown_kernel(DevState st, int H, int I, i
             acc[j] = fmaf(p, sc.x, fmaf(p2, sc.y, acc[j]));
           }
         }
+      } else if (FMT == MOE_W_MXFP4 || FMT == MOE_W_Q4_0) {
+        const Off of(H, I, FMT);
+        const int sbr = (I / 32) * (FMT == MOE_W_Q4_0 ? 2 : 1);  // scale bytes per row
+        const uint8_t* dc = blob + of.code[2] + (size_t)nn * (I / 2);
+        const uint8_t* ds = blob + of.scale[2] + (size_t)nn * sbr;
+#pragma unroll 2
+        for (int blk = 0; blk < I / 32; ++blk) {
+          const uint4 cw = *reinterpret_cast<const uint4*>(dc + blk * 16);
+          const float sc = blk32_scale<FMT>(ds, blk);
+          uint32_t d2[16];
+          blk32_decode<FMT>(cw, d2);
+          float wf[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float2 f = f16x2_f32(d2[e]);
+            wf[2 * e] = f.x, wf[2 * e + 1] = f.y;
+          }
+#pragma unroll
+          for (int j = 0; j < kNR; ++j) {
+            if (j >= nq) break;
+            const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)j * I + blk * 32);
+            float p = 0.f, p2 = 0.f;
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const float4 hv = hp[e4], hv2 = hp[4 + e4];
+              p = fmaf(wf[4 * e4], hv.x, p);
+              p = fmaf(wf[4 * e4 + 1], hv.y, p);
+              p = fmaf(wf[4 * e4 + 2], hv.z, p);
+              p = fmaf(wf[4 * e4 + 3], hv.w, p);
+              p2 = fmaf(wf[16 + 4 * e4], hv2.x, p2);
+              p2 = fmaf(wf[16 + 4 * e4 + 1], hv2.y, p2);
+              p2 = fmaf(wf[16 + 4 * e4 + 2], hv2.z, p2);
+              p2 = fmaf(wf[16 + 4 * e4 + 3], hv2.w, p2);
+            }
+            acc[j] = fmaf(p + p2, sc, acc[j]);
+          }
+        }
       } else {
         const uint8_t* dm = blob + o.mat[2] + (size_t)nn * I * 2;
         for (int wd = 0; wd < I / 8; ++wd) {
@@ -727,7 +841,7 @@ __global__ void __launch_bounds__(kWT) gcombine_kernel(const DevState st, int H,
 }
 
 int g_sms = 0;
-int g_occ[2][2] = {{1, 1}, {1, 1}};  // resident CTAs per SM: [format][gate-up, down]
+int g_occ[4][2] = {{1, 1}, {1, 1}, {1, 1}, {1, 1}};  // resident CTAs per SM: [format][gate-up, down]
 int g_occ_staged[2] = {1, 1};        // ... of the staged NVFP4 kernels
 
 size_t gup_staged_smem(int H) { return (size_t)kNR * H * 2 + (size_t)kNS * (2 * kStC + 2 * kStS); }
@@ -743,7 +857,8 @@ bool staged_ok(int H, int I) {
 bool grouped_supported(int wfmt, int H, int I, int E) {
   const bool smem = (size_t)E * 16 <= 200 * 1024 && (size_t)kNR * H * 2 <= 200 * 1024 &&
                     (size_t)kNR * I * 4 <= 200 * 1024;
-  if (wfmt == MOE_W_NVFP4) return smem && H % 32 == 0 && I % 32 == 0;
+  if (wfmt == MOE_W_NVFP4 || wfmt == MOE_W_MXFP4 || wfmt == MOE_W_Q4_0)
+    return smem && H % 32 == 0 && I % 32 == 0;
   return wfmt == MOE_W_BF16 && smem && H % 8 == 0 && I % 8 == 0;
 }
 
@@ -758,19 +873,28 @@ cudaError_t grouped_init(int E, int H, int I) {
     if (e == cudaSuccess && bytes > 48 * 1024)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   };
-  lim(gup_kernel<MOE_W_NVFP4>, (size_t)kNR * H * 2);
-  lim(gup_kernel<MOE_W_BF16>, (size_t)kNR * H * 2);
-  lim(gdown_kernel<MOE_W_NVFP4>, (size_t)kNR * I * 4);
-  lim(gdown_kernel<MOE_W_BF16>, (size_t)kNR * I * 4);
+  const size_t ub = (size_t)kNR * H * 2, db = (size_t)kNR * I * 4;
+  lim(gup_kernel<MOE_W_NVFP4>, ub);
+  lim(gup_kernel<MOE_W_BF16>, ub);
+  lim(gup_kernel<MOE_W_MXFP4>, ub);
+  lim(gup_kernel<MOE_W_Q4_0>, ub);
+  lim(gdown_kernel<MOE_W_NVFP4>, db);
+  lim(gdown_kernel<MOE_W_BF16>, db);
+  lim(gdown_kernel<MOE_W_MXFP4>, db);
+  lim(gdown_kernel<MOE_W_Q4_0>, db);
   // persistent grids: as many CTAs as fit on the GPU at once
   auto occ = [&](auto kern, size_t bytes, int* out) {
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, kWT, bytes);
     if (*out < 1) *out = 1;
   };
-  occ(gup_kernel<MOE_W_BF16>, (size_t)kNR * H * 2, &g_occ[MOE_W_BF16][0]);
-  occ(gup_kernel<MOE_W_NVFP4>, (size_t)kNR * H * 2, &g_occ[MOE_W_NVFP4][0]);
-  occ(gdown_kernel<MOE_W_BF16>, (size_t)kNR * I * 4, &g_occ[MOE_W_BF16][1]);
-  occ(gdown_kernel<MOE_W_NVFP4>, (size_t)kNR * I * 4, &g_occ[MOE_W_NVFP4][1]);
+  occ(gup_kernel<MOE_W_BF16>, ub, &g_occ[MOE_W_BF16][0]);
+  occ(gup_kernel<MOE_W_NVFP4>, ub, &g_occ[MOE_W_NVFP4][0]);
+  occ(gup_kernel<MOE_W_MXFP4>, ub, &g_occ[MOE_W_MXFP4][0]);
+  occ(gup_kernel<MOE_W_Q4_0>, ub, &g_occ[MOE_W_Q4_0][0]);
+  occ(gdown_kernel<MOE_W_BF16>, db, &g_occ[MOE_W_BF16][1]);
+  occ(gdown_kernel<MOE_W_NVFP4>, db, &g_occ[MOE_W_NVFP4][1]);
+  occ(gdown_kernel<MOE_W_MXFP4>, db, &g_occ[MOE_W_MXFP4][1]);
+  occ(gdown_kernel<MOE_W_Q4_0>, db, &g_occ[MOE_W_Q4_0][1]);
   if (staged_ok(H, I)) {
     lim(gup_staged_kernel, gup_staged_smem(H));
     lim(gdown_staged_kernel, gdown_staged_smem(I));
@@ -797,7 +921,7 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
                                                  tc_any ? sc.dense : nullptr);
   const uint16_t* xx = static_cast<const uint16_t*>(x);
   const int sms = g_sms > 0 ? g_sms : 1;
-  const int fi = wfmt == MOE_W_NVFP4 ? MOE_W_NVFP4 : MOE_W_BF16;
+  const int fi = wfmt >= MOE_W_BF16 && wfmt <= MOE_W_Q4_0 ? wfmt : MOE_W_BF16;
   const int grid_u = sms * g_occ[fi][0], grid_d = sms * g_occ[fi][1];
   // NVFP4 with both kernel families available: per group by its route count
   // (auto), or all groups on one family (a forced mode)
@@ -817,12 +941,18 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
     if (cc && staged_ok(H, I))
       gdown_staged_kernel<<<sms * g_occ_staged[1], kWT, gdown_staged_smem(I), s>>>(
           st, H, I, layer, gr, sc.h, sc.y, tc_from);
-  } else if (wfmt == MOE_W_NVFP4) {
+  } else if (wfmt == MOE_W_NVFP4 || wfmt == MOE_W_MXFP4 || wfmt == MOE_W_Q4_0) {
+    // the CUDA-core kernels of the 4-bit format (x as f16 for every one)
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
-    gup_kernel<MOE_W_NVFP4><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,
-                                                                     sc.xinv, k, gr, sc.h);
-    gdown_kernel<MOE_W_NVFP4><<<grid_d, kWT, (size_t)kNR * I * 4, s>>>(st, H, I, layer, gr, sc.h,
-                                                                      sc.y);
+    auto run = [&](auto fmt) {
+      constexpr int F = decltype(fmt)::value;
+      gup_kernel<F><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16, sc.xinv, k,
+                                                             gr, sc.h);
+      gdown_kernel<F><<<grid_d, kWT, (size_t)kNR * I * 4, s>>>(st, H, I, layer, gr, sc.h, sc.y);
+    };
+    if (wfmt == MOE_W_MXFP4) run(std::integral_constant<int, MOE_W_MXFP4>{});
+    else if (wfmt == MOE_W_Q4_0) run(std::integral_constant<int, MOE_W_Q4_0>{});
+    else run(std::integral_constant<int, MOE_W_NVFP4>{});
   } else {
     xprep_kernel<MOE_W_BF16><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
     gup_kernel<MOE_W_BF16><<<grid_u, kWT, (size_t)kNR * H * 2, s>>>(st, H, I, layer, sc.x16,

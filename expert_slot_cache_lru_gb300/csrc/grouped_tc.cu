@@ -222,11 +222,11 @@ struct Off {
   }
 };
 
-// The route groups buffer of the cache: [G, slot[R], start[R + 1], route[R]].
+// The route groups buffer of the cache: [G, slot[R], start[R + 1], route[R]]
+// (the dense groups' ids come from their own list).
 struct Groups {
   const int32_t* base;
   int R;
-  __device__ int G() const { return base[0]; }
   __device__ int slot(int g) const { return base[1 + g]; }
   __device__ int start(int g) const { return base[1 + R + g]; }
   __device__ int route(int q) const { return base[2 + 2 * R + q]; }

@@ -418,8 +418,6 @@ static int run_shared(moe_cache* c, const void* d_x, int n_rows, const void* blo
                                  static_cast<const uint8_t*>(blob), gate, c->sc, c->st.status, s));
     return MOE_OK;
   }
-  if (c->d.wfmt != MOE_W_BF16 && c->d.wfmt != MOE_W_NVFP4)  // streaming kernels only
-    return MOE_ERR_UNSUPPORTED;
   CK(moe::launch_shared_expert(c->d.wfmt, c->d.hidden, c->d.shared_inter, d_x, n_rows,
                                static_cast<const uint8_t*>(blob), gate, c->sc, s));
   return MOE_OK;
@@ -435,7 +433,6 @@ static int run_routed(moe_cache* c, int layer, const void* d_x, const int32_t* s
                                  k, with_shared ? c->sc.ys : nullptr, d_out, c->sc, c->st.status, s));
     return MOE_OK;
   }
-  if (d.wfmt != MOE_W_BF16 && d.wfmt != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;  // streaming only
   if (k > 0 && moe::grouped_supported(d.wfmt, d.hidden, d.inter, d.n_experts)) {
     CK(moe::launch_routed_grouped(c->st, d.wfmt, d.hidden, d.inter, layer, d_x, slot_ids, w,
                                   n_rows, k, with_shared ? c->sc.ys : nullptr, d_out, c->sc,

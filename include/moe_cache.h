@@ -76,9 +76,10 @@
  *                scale; 3*H*I/2 + 3*H*I/32 bytes [P1 section 7 lists MXFP4
  *                among the expert formats; layout of the OCP Microscaling
  *                MXFP4 blocks].  element (n,k) = e2m1(code) * 2^(scale[n][k/32] - 127).
- *                Decode-sized steps only (the streaming kernels, H a multiple
- *                of 2048, I of 512) and the hybrid CPU executor; wider steps
- *                return MOE_ERR_UNSUPPORTED.
+ *                Every path but the tensor-core one: the decode-sized streaming
+ *                kernels (H a multiple of 2048, I of 512), the wide steps'
+ *                grouped kernels on the CUDA cores, the per-route kernels
+ *                beyond both, and the hybrid CPU executor.
  *   MOE_W_Q4_0:  the arithmetic of Q4_0 (blocks of 32 weights, weight =
  *                d * (q - 8) with q an unsigned 4-bit code and d an fp16
  *                scale) in the same banked layout: the three code banks (q,

@@ -438,6 +438,31 @@ def test_wide_step_tensor_cores_and_cuda_cores(routing, batch):
         m.moe_cache_set_wide_path(rigs[0].sc.handle, 3)
 
 
+@pytest.mark.parametrize("fmt", [synth.FMT_MXFP4, synth.FMT_Q4_0])
+def test_4bit_formats_wide_step_equals_oracle(fmt):
+    """Wide steps of MXFP4 and Q4_0 experts (formats listed in FreeToken PR
+    #491, section 7, "What did not change"): 40 rows x top-4 over 64 experts
+    (H 256, I 128) with a gated shared expert of the same format (I 128).
+    The routed experts take the grouped kernels on the CUDA cores, the shared
+    expert the per-row kernels (more rows than the streaming kernels take).
+    Two steps with misses: route groups and state exact, every row within the
+    fp4 tolerance of the fp64 layer."""
+    w = synth.scaled(synth.workloads()["wide_decode"], fmt=fmt, n_experts=64, top_k=4,
+                     hidden=256, inter=128, n_slots=64, batch=40, routing="uniform",
+                     prefill_frac=0.0, shared_inter=128)
+    rig = Rig(w)
+    st = Stepper(rig)
+    ids, wts = synth.make_routing(w, steps=2)
+    for t in range(2):
+        x = synth.make_hidden(w, t)
+        refs = st.step(t, ids[t], wts[t], x)
+        assert _gpu_groups(rig.sc, rig.sc.desc.max_routes) == refs[0]["groups"]
+        ref = rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0])
+        assert_close(st.out[0], ref, w.fmt, f"step {t}")
+    s = rig.sc.stats(0)
+    assert s["misses"] > 0 and s["status_bits"] == 0
+
+
 @pytest.mark.slow
 def test_hybrid_capped_prefetch_partial_plus_cpu():
     """Capped fetch (4 per layer) + look-ahead prefetch over 48 bf16 layers:
