@@ -83,6 +83,8 @@ def lib():
         L.om_blob_bytes.argtypes = [C.c_int, C.c_int, C.c_int]
         L.om_dequant.argtypes = [C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p]
         L.om_expert_ffn.argtypes = [C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_void_p, C.c_void_p]
+        L.om_lookahead_predict.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                           C.c_int, C.c_void_p, C.c_void_p]
         L.om_layer.argtypes = [C.c_int, C.c_void_p, C.c_int, C.c_int, C.c_int, C.c_void_p,
                                C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                C.c_void_p, C.c_int, C.c_void_p, C.c_void_p]
@@ -274,3 +276,21 @@ def layer(fmt: int, blobs, n_experts: int, hidden: int, inter: int, x_bf16, ids,
     if rc != 0:
         raise ValueError(f"om_layer rc={rc}")
     return out
+
+
+def lookahead_predict(x_bf16, router_bf16, k: int) -> tuple[np.ndarray, np.ndarray]:
+    """(pred int32 [B, k], z fp64 [B, E]): layer L+1's router on layer L's hidden
+    state, each row's k largest logits (see oracle.h)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    r = np.ascontiguousarray(router_bf16, dtype=np.uint16)
+    B, H = x.shape
+    E = r.shape[0]
+    if r.shape[1] != H:
+        raise ValueError("router and x widths differ")
+    pred = np.empty((B, k), np.int32)
+    z = np.empty((B, E), np.float64)
+    rc = lib().om_lookahead_predict(x.ctypes.data, r.ctypes.data, B, E, H, k, pred.ctypes.data,
+                                    z.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"om_lookahead_predict rc={rc}")
+    return pred, z

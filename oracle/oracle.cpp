@@ -730,4 +730,32 @@ int om_layer(int fmt, const uint8_t* const* blobs, int E, int H, int I, const ui
   return rc;
 }
 
+// The look-ahead producer: layer L+1's router on layer L's hidden state, each
+// row's k largest logits (ties and NaN as the header states), in the plain
+// order -- every dot product in fp64, then one sort of the row's experts.
+int om_lookahead_predict(const uint16_t* x, const uint16_t* router, int B, int E, int H, int k,
+                         int32_t* pred, double* z_out) {
+  if (!x || !router || !pred || B < 0 || E < 1 || H < 1 || k < 1 || k > E) return -1;
+  std::vector<double> z(E);
+  std::vector<int> order(E);
+  for (int b = 0; b < B; ++b) {
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h)
+        acc += om_bf16(router[(uint64_t)e * H + h]) * om_bf16(x[(uint64_t)b * H + h]);
+      z[e] = acc;
+      if (z_out) z_out[(uint64_t)b * E + e] = acc;
+    }
+    for (int e = 0; e < E; ++e) order[e] = e;
+    std::sort(order.begin(), order.end(), [&](int a, int c) {
+      const bool na = std::isnan(z[a]), nc = std::isnan(z[c]);
+      if (na != nc) return nc;              // a number before a NaN
+      if (!na && z[a] != z[c]) return z[a] > z[c];
+      return a < c;                         // equal (or both NaN): the lower id first
+    });
+    for (int r = 0; r < k; ++r) pred[(uint64_t)b * k + r] = order[r];
+  }
+  return 0;
+}
+
 }  // extern "C"

@@ -109,6 +109,19 @@ int om_layer(int fmt, const uint8_t* const* blobs, int n_experts, int hidden, in
              int n_rows, int k, const uint8_t* shared_blob, int shared_inter,
              const uint16_t* shared_gate_w, double* out);
 
+/* The look-ahead producer's prediction [llama.cpp fork PR #126 "cuda : MoE
+ * look-ahead expert prefetch (PR-A consumer) + LFRU eviction guard", sections
+ * What and "Open for PR-P1 (producer)": the predicted ids of layer L+1, made
+ * while layer L runs].  The pages leave the predictor open; the reading here
+ * applies layer L+1's router to layer L's hidden state.  For each row b:
+ * z[e] = sum_h router[e][h] * x[b][h] in fp64 (both operands bf16 bits, row e
+ * of router = expert e), stored in z_out[b*n_experts + e] when z_out is not
+ * NULL; pred[b*k + r] = the expert of rank r when the experts are ordered by z
+ * descending, then by id ascending, a NaN z ranking after every number.
+ * 1 <= k <= n_experts. */
+int om_lookahead_predict(const uint16_t* x, const uint16_t* router, int n_rows, int n_experts,
+                         int hidden, int k, int32_t* pred, double* z_out);
+
 #ifdef __cplusplus
 }
 #endif

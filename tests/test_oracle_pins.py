@@ -588,3 +588,55 @@ def test_guard_recency_byte_boundary(age, protected):
     assert oc.state()["clock"][0] - oc.state()["last_demand"][5] == age
     plan = oc.prefetch(0, [20])
     assert (plan == []) == protected
+
+
+# ----------------------------------------------------------------------------
+# The look-ahead producer (llama.cpp fork PR #126 "cuda : MoE look-ahead
+# expert prefetch (PR-A consumer) + LFRU eviction guard", sections What and
+# "Open for PR-P1 (producer)").  The pages leave the predictor open; the
+# reading: layer L+1's router applied to layer L's hidden state, each row's k
+# largest logits, ties to the lower id.
+
+def _bf16_bits(vals) -> np.ndarray:
+    """bf16 bits of values that bf16 holds exactly."""
+    return (np.asarray(vals, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _one_hot_router() -> np.ndarray:
+    """Row e holds e + 1 in column e mod 4 and zeros elsewhere, so that
+    z[b][e] = (e + 1) * x_b[e mod 4] exactly."""
+    r = np.zeros((8, 4), np.float32)
+    for e in range(8):
+        r[e, e % 4] = e + 1
+    return r
+
+
+def test_lookahead_predict_closed_form():
+    """x_0 = (1, 2, 3, 4): z = 1, 4, 9, 16, 5, 12, 21, 32, so the top 3 are
+    experts 7, 6, 3.  x_1 = (4, 3, 2, 1): z = 4, 6, 6, 4, 20, 18, 14, 8, so
+    the top 3 are 4, 5, 6.  A transposed product, the first row's x used for
+    every row, or an ascending order each fails."""
+    x = np.array([[1, 2, 3, 4], [4, 3, 2, 1]], np.float32)
+    pred, z = oracle.lookahead_predict(_bf16_bits(x), _bf16_bits(_one_hot_router()), 3)
+    assert pred.tolist() == [[7, 6, 3], [4, 5, 6]]
+    assert z.tolist() == [[1, 4, 9, 16, 5, 12, 21, 32], [4, 6, 6, 4, 20, 18, 14, 8]]
+
+
+def test_lookahead_predict_ties_negative_and_nan():
+    """The full order of x_1's logits has two ties (6 at experts 1 and 2, 4 at
+    0 and 3), each going to the lower id; negated x reverses the order of the
+    distinct values; a NaN router weight makes that expert's logit NaN, which
+    ranks after every number."""
+    router = _one_hot_router()
+    x1 = np.array([[4, 3, 2, 1]], np.float32)
+    pred, _ = oracle.lookahead_predict(_bf16_bits(x1), _bf16_bits(router), 8)
+    assert pred[0].tolist() == [4, 5, 6, 7, 1, 2, 0, 3]
+    pred, _ = oracle.lookahead_predict(_bf16_bits(-x1), _bf16_bits(router), 8)
+    assert pred[0].tolist() == [0, 3, 1, 2, 7, 6, 5, 4]  # -4,-4,-6,-6,-8,-14,-18,-20
+    router[7, 3] = np.nan
+    x0 = np.array([[1, 2, 3, 4]], np.float32)
+    pred, z = oracle.lookahead_predict(_bf16_bits(x0), _bf16_bits(router), 8)
+    assert math.isnan(z[0, 7])
+    assert pred[0].tolist() == [6, 3, 5, 2, 4, 1, 0, 7]
+    with pytest.raises(ValueError):
+        oracle.lookahead_predict(_bf16_bits(x0), _bf16_bits(router), 9)  # k > n_experts
