@@ -1003,6 +1003,10 @@ def run_native(args) -> None:
             roof = dec.routed_gemv_roofline(steps=2)
             print(json.dumps({"routed_only": True, "layers": L, **roof}), flush=True)
         return
+    if args.lookahead_only:
+        if rank == 0:
+            print(json.dumps({"lookahead_only": True, **lookahead_producer(dec)}), flush=True)
+        return
     if args.decode_only:  # profiler runs: the timed decode only, no sub-measurements
         if rank == 0:
             print(json.dumps({"decode_only": True, "layers": L, "slots": dec.w.n_slots,
@@ -1034,6 +1038,7 @@ def run_native(args) -> None:
     wide = wide_step(local)
     wide_zipf = wide_step(local, reps=3, routing="zipf")
     hyb = hybrid_step(local) if not args.no_hybrid else None
+    look = lookahead_producer(dec)
     tr = routed_traffic()
     line = {
         "metric": METRIC,
@@ -1087,6 +1092,7 @@ def run_native(args) -> None:
         "wide_decode_step": wide,
         "wide_decode_step_zipf": wide_zipf,
         "hybrid_decode": hyb,
+        "lookahead_producer": look,
         "gather": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in gather.items()},
         "setup_s": {k: round(v, 1) for k, v in dec.setup_s.items()},
         "clocks": sampler.summary(),
@@ -1150,6 +1156,72 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
+def lookahead_producer(dec, steps: int = 12, drifts=(0.25, 0.5, 1.0)) -> dict:
+    """The look-ahead producer (moe_lookahead_predict): layer L+1's router on
+    layer L's hidden state, at the decode's shape (256 experts, H 2048, one
+    row, top 8).  Its time per launch in a graph of one launch per layer (each
+    with its own 1 MiB router, so the routers stream from HBM), and its recall
+    of the next layer's true top 8 when the hidden states drift from layer to
+    layer (synth.drift_stream: x_{l+1} = (x_l + s n) / sqrt(1 + s^2)), the true
+    routing of layer l+1 being its router's top 8 on x_{l+1}."""
+    import torch
+
+    import synth
+    m, w = dec.m, dec.w
+    L, E, H, k = w.n_layers, w.n_experts, w.hidden, w.top_k
+    h = dec.cache.handle
+    routers = torch.stack([torch.from_numpy(synth.make_router(w, l).view(np.int16))
+                           for l in range(L)]).cuda()
+    x = torch.from_numpy(np.ascontiguousarray(synth.make_hidden(w, 0)[:, :1]).view(np.int16)).cuda()
+    pred = torch.zeros(L, k, dtype=torch.int32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def enqueue():
+        for l in range(L):
+            m.moe_lookahead_predict(h, x[l], routers[(l + 1) % L], 1, k, pred[l], s)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        enqueue()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        enqueue()
+    reps = 20
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):  # replays run on the current stream: make it s
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(reps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * L)
+    nbytes = E * H * 2 + H * 2 + k * 4
+    recall = {}
+    truth = torch.zeros(L, k, dtype=torch.int32, device="cuda")
+    guess = torch.zeros(L, k, dtype=torch.int32, device="cuda")
+    for sd in drifts:
+        hit = tot = 0
+        for t in range(steps):
+            xs = torch.from_numpy(synth.drift_stream(w, t, sd, batch=1).view(np.int16)).cuda()
+            for l in range(L - 1):
+                m.moe_lookahead_predict(h, xs[l + 1], routers[l + 1], 1, k, truth[l], s)
+                m.moe_lookahead_predict(h, xs[l], routers[l + 1], 1, k, guess[l], s)
+            torch.cuda.synchronize()
+            tr, gu = truth.cpu().numpy(), guess.cpu().numpy()
+            for l in range(L - 1):
+                hit += len(set(tr[l].tolist()) & set(gu[l].tolist()))
+                tot += k
+        recall[str(sd)] = round(hit / tot, 4)
+    return {"us_per_launch": round(us, 3), "launches_per_token": L,
+            "bytes_per_launch": nbytes, "achieved_gbs": round(nbytes / (us * 1e3), 1),
+            "recall_of_next_layer_top8_by_drift": recall, "steps_per_drift": steps,
+            "shape": f"{E} experts x H {H}, 1 row, top {k}"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -1177,6 +1249,8 @@ def main():
                     help="run only the wide decode step sub-measurement (profiler runs)")
     ap.add_argument("--wide-routing", choices=["uniform", "zipf"], default="uniform",
                     help="routing of the --wide-only step")
+    ap.add_argument("--lookahead-only", action="store_true",
+                    help="after the decode set-up, only the look-ahead producer's line")
     ap.add_argument("--routed-only", action="store_true",
                     help="after the decode, run only the routed FFN kernel's roofline graph "
                          "(profiler runs)")

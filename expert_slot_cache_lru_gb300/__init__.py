@@ -106,6 +106,7 @@ _SIGS = {
     "moe_hybrid_pause": [_vp, _i],
     "moe_schedule_trace": [_i, _i, _i, _i, _i, _i, _i, _vp, _i],
     "moe_decode_layer_plan": [_vp, _i, _i, _i, _i, _u, _vp, _i],
+    "moe_lookahead_predict": [_vp, _vp, _vp, _i, _i, _vp, _vp],
     "moe_hybrid_selftest": [_i, _i, _i, _vp, _i, _i, _i, _i, _i, _u, _vp],
     "moe_cpu_experts": [_i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _vp],
     "moe_strerror": [_i],
@@ -191,6 +192,13 @@ def moe_admit(cache: int, layer: int, d_ids, d_slot_ids, n_routes: int, fetch_ca
 
 def moe_prefetch(cache: int, layer: int, d_pred, n: int, stream=None) -> None:
     _check("moe_prefetch", _lib.moe_prefetch(cache, layer, _ptr(d_pred), n, _stream(stream)))
+
+
+def moe_lookahead_predict(cache: int, d_x, d_router, n_rows: int, k_pred: int, d_pred,
+                          stream=None) -> None:
+    """Predicted ids of the next layer (see moe_cache.h)."""
+    _check("moe_lookahead_predict", _lib.moe_lookahead_predict(
+        cache, _ptr(d_x), _ptr(d_router), n_rows, k_pred, _ptr(d_pred), _stream(stream)))
 
 
 def moe_gather_missing(cache: int, which: int = MOE_PLAN_DEMAND, stream=None) -> None:

@@ -168,6 +168,8 @@ struct FfnScratch {
   float* hinv;      // [max_routes] inverse of each route's h scale
   int32_t* dense;   // [1 + max_routes] the groups the tensor-core kernels take: count, ids
   int* gdone;       // [max_routes] pieces of each demand-plan expert copied by a fused layer
+  float* la_z;      // [max_rows][n_experts] the look-ahead producer's router logits
+  unsigned* la_ctr; // its CTAs done (zero between launches)
   // a fused layer with the admission inside the launch (three counters that only grow)
   unsigned long long* epoch;   // launches (each CTA adds one)
   unsigned long long* pseq;    // the admission's publication sequence
@@ -191,6 +193,12 @@ cudaError_t launch_routed_down_combine(const DevState& st, int wfmt, int H, int 
 // Streaming expert FFNs for decode-sized steps (ffn_stream.cu).
 bool ffn_stream_supported(int wfmt, int H, int I, int n_rows, int n_tasks);
 cudaError_t ffn_stream_init();
+
+// The look-ahead producer (lookahead.cu).
+bool lookahead_supported(int H, int E, int k);
+cudaError_t lookahead_init(int H);
+cudaError_t launch_lookahead(const void* x, const void* router, int n_rows, int H, int E, int k,
+                             float* z, unsigned* ctr, int32_t* pred, cudaStream_t s);
 cudaError_t launch_shared_stream(const DevState& st, int wfmt, int H, int Is, const void* x,
                                  int n_rows, const uint8_t* blob, const void* gate_w,
                                  FfnScratch sc, unsigned long long* status, cudaStream_t s);

@@ -171,6 +171,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
                o_lol = cv.take<int32_t>(vcap), o_hb = cv.take<const uint8_t*>(K),
                o_h = cv.take<float>(((size_t)d.max_routes + d.max_rows) * std::max(I, 1)),
                o_gdone = cv.take<int32_t>(std::max(d.max_routes, 1)),
+               o_laz = cv.take<float>((size_t)d.max_rows * d.n_experts),
+               o_lactr = cv.take<unsigned>(1),
                o_hs = cv.take<float>((size_t)d.max_rows * std::max(Is, 1)),
                o_gate = cv.take<float>(d.max_rows),
                o_ys = cv.take<float>((size_t)d.max_rows * std::max(H, 1)),
@@ -235,6 +237,8 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
   c->sc.hinv = reinterpret_cast<float*>(m + o_hinv);
   c->sc.dense = reinterpret_cast<int32_t*>(m + o_dense);
   c->sc.gdone = reinterpret_cast<int*>(m + o_gdone);
+  c->sc.la_z = reinterpret_cast<float*>(m + o_laz);
+  c->sc.la_ctr = reinterpret_cast<unsigned*>(m + o_lactr);
 
   // initial state: nothing resident, every clock at 1
   e = cudaMemset(c->mem, 0, c->mem_bytes);
@@ -274,6 +278,7 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     c->down_k_max = (int)std::min<size_t>(d.max_routes, (200 * 1024) / ((size_t)I * 4));
     e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
     if (e == cudaSuccess) e = moe::ffn_stream_init();
+    if (e == cudaSuccess && moe::lookahead_supported(H, d.n_experts, 1)) e = moe::lookahead_init(H);
     if (e == cudaSuccess && moe::grouped_supported(d.wfmt, H, I, d.n_experts))
       e = moe::grouped_init(d.n_experts, H, I);
     if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
@@ -374,6 +379,23 @@ int moe_prefetch(moe_cache* c, int layer, const int32_t* d_pred, int n, void* st
   if (n > c->d.max_pred) return MOE_ERR_CAPACITY;
   CK(moe::launch_prefetch(c->st, layer, d_pred, n, c->st.plan_pf[layer & 1], as_stream(stream)));
   c->last_pf_layer = layer;
+  return MOE_OK;
+}
+
+int moe_lookahead_predict(moe_cache* c, const void* d_x, const void* d_router, int n_rows,
+                          int k_pred, int32_t* d_pred, void* stream) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  const moe_cache_desc& d = c->d;
+  if (n_rows < 0 || k_pred < 1) return MOE_ERR_INVALID_ARG;
+  if (n_rows == 0) return MOE_OK;
+  if (!d_x || !d_router || !d_pred || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
+      (reinterpret_cast<uintptr_t>(d_router) & 15) || (reinterpret_cast<uintptr_t>(d_pred) & 3))
+    return MOE_ERR_INVALID_ARG;
+  if (d.hidden == 0) return MOE_ERR_STATE;
+  if (n_rows > d.max_rows) return MOE_ERR_CAPACITY;
+  if (!moe::lookahead_supported(d.hidden, d.n_experts, k_pred)) return MOE_ERR_UNSUPPORTED;
+  CK(moe::launch_lookahead(d_x, d_router, n_rows, d.hidden, d.n_experts, k_pred, c->sc.la_z,
+                           c->sc.la_ctr, d_pred, as_stream(stream)));
   return MOE_OK;
 }
 

@@ -264,6 +264,26 @@ MOE_API int moe_admit(moe_cache* c, int layer, const int32_t* d_ids, int32_t* d_
  * MOE_ERR_STATE if the cache was created with max_pred = 0. */
 MOE_API int moe_prefetch(moe_cache* c, int layer, const int32_t* d_pred, int n, void* stream);
 
+/* The look-ahead producer [llama.cpp fork PR #126 "cuda : MoE look-ahead
+ * expert prefetch (PR-A consumer) + LFRU eviction guard", sections What and
+ * "Open for PR-P1 (producer)"]: the predicted ids of layer L+1, computed while
+ * layer L runs, for moe_prefetch or moe_decode_layer's d_pred.  The pages
+ * leave the predictor open; this one applies layer L+1's router to the hidden
+ * state layer L has.  For each row b of d_x (bf16 [n_rows][hidden]):
+ *   z[e] = sum_h router[e][h] * x[b][h]   (d_router bf16 [n_experts][hidden],
+ *          row e = expert e's router weights; exact products, fp32 sums),
+ * and d_pred[b*k_pred + r], r = 0..k_pred-1, receives the expert of rank r by
+ * z, largest first, a tie going to the lower id, a NaN logit ranking below
+ * -inf.  d_pred int32 [n_rows * k_pred] may then be passed whole as
+ * (d_pred, n_rows * k_pred): the prefetch admission ignores repeats.
+ * Shapes: hidden a multiple of 1024 up to 4096, 1 <= k_pred <= min(32,
+ * n_experts), n_rows <= max_rows (else MOE_ERR_UNSUPPORTED / _CAPACITY);
+ * d_x and d_router 16-byte aligned, d_pred 4-byte (else MOE_ERR_INVALID_ARG).  One launch on
+ * `stream` that waits on nothing; graph-capturable.  Calls on different
+ * streams must not overlap (one logit buffer per cache). */
+MOE_API int moe_lookahead_predict(moe_cache* c, const void* d_x, const void* d_router, int n_rows,
+                                  int k_pred, int32_t* d_pred, void* stream);
+
 /* The gather, "copy_missing" [P2 Problem, What we changed]: copy every entry
  * of the demand or prefetch plan from its pinned host blob into its slot.  The
  * grid reads the device-side count, so the call needs no host sync and its

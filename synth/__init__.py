@@ -23,7 +23,12 @@ Recipe (all streams derived from ``numpy.random.SeedSequence([seed, stream,
   uniformly from the 16 codes 0x28..0x37 (0.25 .. 0.9375), one fp32 global
   scale per matrix uniform in [0.008, 0.014] -- about 0.02 rms per weight;
 * look-ahead predictions: each true next-layer id kept with probability 0.7,
-  else uniform over the experts.
+  else uniform over the experts;
+* router weights (the look-ahead producer's input): N(0, 1 / H) rounded to
+  bf16, one [E][H] matrix per layer;
+* a drifting hidden stream (the producer's accuracy): x of layer l + 1 is
+  (x_l + s n_l) / sqrt(1 + s^2) with n_l ~ N(0, 1), rounded to bf16 -- a
+  stand-in for a residual stream whose consecutive layers' inputs correlate.
 """
 from __future__ import annotations
 
@@ -41,6 +46,7 @@ FMT_Q4_0 = 3
 
 # stream ids of the seed sequence
 S_WEIGHTS, S_PERM, S_ROUTING, S_HIDDEN, S_PRED, S_RWEIGHTS, S_SHARED, S_PREFILL, S_ALIAS = range(1, 10)
+S_ROUTER, S_DRIFT = 10, 11
 
 
 # ----------------------------------------------------------------------------- RNG
@@ -380,6 +386,25 @@ def make_hidden(w: Workload, step: int, batch: int | None = None) -> np.ndarray:
     B = w.batch if batch is None else batch
     z = Rng(w.seed, S_HIDDEN, step, B).normal(w.n_layers * B * w.hidden)
     return to_bf16_bits(z).reshape(w.n_layers, B, w.hidden)
+
+
+def make_router(w: Workload, layer: int) -> np.ndarray:
+    """Router weights of a layer, bf16 bits [E][H] (row e: expert e)."""
+    z = Rng(w.seed, S_ROUTER, layer).normal(w.n_experts * w.hidden) / math.sqrt(w.hidden)
+    return to_bf16_bits(z).reshape(w.n_experts, w.hidden)
+
+
+def drift_stream(w: Workload, step: int, s: float, batch: int | None = None) -> np.ndarray:
+    """x [L, B, H] as bf16 bits: layer 0 N(0, 1), then x_{l+1} = (x_l + s n_l)
+    / sqrt(1 + s^2) (unit variance throughout)."""
+    B = w.batch if batch is None else batch
+    r = Rng(w.seed, S_DRIFT, step, B)
+    x = np.empty((w.n_layers, B, w.hidden), np.float32)
+    x[0] = r.normal(B * w.hidden).reshape(B, w.hidden)
+    for l in range(1, w.n_layers):
+        n = r.normal(B * w.hidden).reshape(B, w.hidden)
+        x[l] = (x[l - 1] + s * n) / math.sqrt(1.0 + s * s)
+    return to_bf16_bits(x)
 
 
 def make_predictions(w: Workload, ids_next_layer: np.ndarray, step: int, layer: int) -> np.ndarray:
