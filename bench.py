@@ -1003,6 +1003,12 @@ def run_native(args) -> None:
             roof = dec.routed_gemv_roofline(steps=2)
             print(json.dumps({"routed_only": True, "layers": L, **roof}), flush=True)
         return
+    if args.prefill_only:
+        if rank == 0:
+            print(json.dumps({"prefill_only": True, "on_demand": prefill_chunks(dec),
+                              "layer_major": prefill_chunks(dec, (128,), layer_major=True)}),
+                  flush=True)
+        return
     if args.lookahead_only:
         if rank == 0:
             print(json.dumps({"lookahead_only": True, **lookahead_producer(dec)}), flush=True)
@@ -1039,6 +1045,8 @@ def run_native(args) -> None:
     wide_zipf = wide_step(local, reps=3, routing="zipf")
     hyb = hybrid_step(local) if not args.no_hybrid else None
     look = lookahead_producer(dec)
+    pre = {"on_demand": prefill_chunks(dec),
+           "layer_major": prefill_chunks(dec, (128,), layer_major=True)}
     tr = routed_traffic()
     line = {
         "metric": METRIC,
@@ -1093,6 +1101,7 @@ def run_native(args) -> None:
         "wide_decode_step_zipf": wide_zipf,
         "hybrid_decode": hyb,
         "lookahead_producer": look,
+        "prefill_chunks": pre,
         "gather": {k: (round(v, 3) if isinstance(v, float) else v) for k, v in gather.items()},
         "setup_s": {k: round(v, 1) for k, v in dec.setup_s.items()},
         "clocks": sampler.summary(),
@@ -1154,6 +1163,79 @@ def run_reference(args) -> None:
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def prefill_chunks(dec, tokens=(16, 128), chunks: int = 4, layer_major: bool = False) -> dict:
+    """Prefill chunks through the decode workload's 40 layers [FreeToken PR
+    #680, Problem: DeepSeek-V4's on-demand prefill chunks, taken while
+    T * top_k < num_experts; Solution: one admission per layer, graph-capturable]:
+    a chunk of T tokens is one wide step per layer (admission, gather on the side
+    stream, grouped FFN with the tensor cores for dense groups, shared expert,
+    combine), on its own 3,164-slot cache over the decode's pinned blobs.  Chunk
+    0 starts cold; the median of the later chunks is the steady figure.  Each
+    chunk is timed with CUDA events around its 40 layer calls.  layer_major: a
+    chunk with more routes than experts also prefetches every expert of the next
+    layer (the look-ahead prefetch with all E ids as predictions), so that layer
+    l + 1's copies cross the host link while layer l computes."""
+    import torch
+
+    import synth
+    m, w0 = dec.m, dec.w
+    L, k = w0.n_layers, w0.top_k
+    out = {}
+    for T in tokens:
+        w = synth.scaled(w0, batch=T, steps=chunks)
+        storage = torch.empty(w.n_slots * dec.blobs.stride, dtype=torch.uint8, device="cuda")
+        cache = m.SlotCache(n_layers=L, n_experts=w.n_experts, n_slots=w.n_slots,
+                            pool_mode=m.MOE_POOL_SHARED, hidden=w.hidden, inter=w.inter,
+                            wfmt=w.fmt, shared_inter=w.shared_inter, slot_storage=storage,
+                            slot_stride=dec.blobs.stride, host_blob_ptrs=dec.blobs.addrs(),
+                            max_routes=T * k, max_rows=T, max_pred=w.n_experts)
+        lm = layer_major and T * k >= w.n_experts
+        every = torch.arange(w.n_experts, dtype=torch.int32, device="cuda")
+        ids, wts = synth.make_routing(w, steps=chunks)
+        slots = torch.empty(L, T * k, dtype=torch.int32, device="cuda")
+        y = torch.empty(L, T, w.hidden, dtype=torch.bfloat16, device="cuda")
+        cs, side = torch.cuda.Stream(), torch.cuda.Stream()
+        flags = m.MOE_FUSED | m.MOE_OVERLAP
+        rows = []
+        for c in range(chunks):
+            d_x = torch.from_numpy(synth.make_hidden(w, c).view(np.int16)).cuda()
+            d_ids = torch.from_numpy(ids[c].reshape(L, -1).copy()).cuda()
+            d_w = torch.from_numpy(wts[c].reshape(L, -1).copy()).cuda()
+            def counts():
+                st = [cache.stats(l) for l in range(L)]
+                return sum(x["misses"] for x in st), sum(x["pf_filled"] for x in st)
+            before = counts()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(cs):
+                e0.record(cs)
+                for l in range(L):
+                    sb, sg = dec.shared[l]
+                    pf = lm and l + 1 < L
+                    m.moe_decode_layer(cache.handle, l, d_x[l], d_ids[l], d_w[l], slots[l], T, k, -1,
+                                       every if pf else None, w.n_experts if pf else 0, sb, sg,
+                                       y[l], cs, side, flags)
+                e1.record(cs)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            after = counts()
+            rows.append((ms, after[0] - before[0], after[1] - before[1]))
+        plan = m.moe_decode_layer_plan(cache.handle, T, k, shared=True, pf=lm, flags=flags)
+        cache.close()
+        del storage
+        steady = rows[1:]
+        ms = statistics.median(r[0] for r in steady)
+        mi = statistics.median(r[1] for r in steady)
+        pfi = statistics.median(r[2] for r in steady)
+        out[str(T)] = {"routes_per_layer": T * k, "cold_chunk_ms": round(rows[0][0], 3),
+                       "cold_chunk_misses": rows[0][1], "ms_per_chunk": round(ms, 3),
+                       "tok_s": round(T / (ms * 1e-3), 1), "misses_per_chunk": mi,
+                       "prefetch_fills_per_chunk": pfi,
+                       "host_link_gbs": round((mi + pfi) * w.blob_bytes / (ms * 1e6), 1),
+                       "layer_major_prefetch": lm, "launches_per_layer": plan}
+    return out
 
 
 def lookahead_producer(dec, steps: int = 12, drifts=(0.25, 0.5, 1.0)) -> dict:
@@ -1249,6 +1331,8 @@ def main():
                     help="run only the wide decode step sub-measurement (profiler runs)")
     ap.add_argument("--wide-routing", choices=["uniform", "zipf"], default="uniform",
                     help="routing of the --wide-only step")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="after the decode set-up, only the prefill-chunk line")
     ap.add_argument("--lookahead-only", action="store_true",
                     help="after the decode set-up, only the look-ahead producer's line")
     ap.add_argument("--routed-only", action="store_true",

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from tests.gpu_util import Rig, assert_close, assert_state_equal
 
@@ -368,17 +369,22 @@ def _gpu_groups(sc, max_routes: int) -> list[tuple[int, list[int]]]:
     return [(int(slot[g]), [int(r) for r in route[start[g]:start[g + 1]]]) for g in range(G)]
 
 
-def wide_layer_oracle(rig, x, ids, wts, experts_per_call: int = 64) -> np.ndarray:
+def wide_layer_oracle(rig, x, ids, wts, experts_per_call: int = 64, layer: int = 0) -> np.ndarray:
     """The fp64 layer over every row, computed as a sum of partial layers over
     disjoint sets of experts (ascending id, `experts_per_call` at a time), so
-    that one oracle call dequantises at most that many experts."""
+    that one oracle call dequantises at most that many experts; the gated
+    shared expert (when the workload has one) is added once."""
     w = rig.w
+    blobs = [rig.blobs.addr(layer * w.n_experts + e) for e in range(w.n_experts)]
     used = np.unique(ids[(ids >= 0) & (ids < w.n_experts)])
     full = np.zeros((x.shape[0], w.hidden), np.float64)
     for c0 in range(0, len(used), experts_per_call):
         part = used[c0:c0 + experts_per_call]
         mask = np.isin(ids, part).astype(np.uint8)
-        full += rig.oracle_layer(0, x, ids, wts, mask=mask)
+        full += oracle.layer(w.fmt, blobs, w.n_experts, w.hidden, w.inter, x, ids, wts, mask=mask)
+    if w.shared_inter:  # every route masked off: the shared expert alone
+        none = np.zeros(np.shape(ids), np.uint8)
+        full += rig.oracle_layer(layer, x, ids, wts, mask=none)
     return full
 
 
@@ -436,6 +442,31 @@ def test_wide_step_tensor_cores_and_cuda_cores(routing, batch):
     assert_state_equal(rigs[0].sc, rigs[1].oc)
     with pytest.raises(m.MoeError):
         m.moe_cache_set_wide_path(rigs[0].sc.handle, 3)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("tokens", [16, 64])
+def test_prefill_chunk_through_the_layer(tokens):
+    """A prefill chunk at the decode workload's layer shape (256 NVFP4 experts,
+    H 2048, I 512, top-8, gated shared expert) goes through moe_decode_layer
+    as one wide step [FreeToken PR #680, Problem: DeepSeek-V4's on-demand
+    prefill chunks, taken while T * top_k < num_experts, and Tests: a chunk
+    admitted whole]: 16 tokens (128 routes, fewer than the experts) and 64
+    tokens (512 routes) over two layers from a cold cache.  One admission per
+    layer whatever the width; slot ids and state exact; every token's output
+    within the NVFP4 tolerance of the fp64 layer."""
+    w = synth.scaled(synth.workloads()["qwen3moe_decode"], n_layers=2, steps=1, batch=tokens,
+                     n_slots=600)
+    rig = Rig(w)
+    st = Stepper(rig)
+    ids, wts = synth.make_routing(w)
+    x = synth.make_hidden(w, 0)
+    st.step(0, ids[0], wts[0], x)
+    for layer in range(w.n_layers):
+        ref = wide_layer_oracle(rig, x[layer], ids[0, layer], wts[0, layer], layer=layer)
+        assert_close(st.out[layer], ref, w.fmt, f"{tokens} tokens, layer {layer}")
+        s = rig.sc.stats(layer)
+        assert s["calls"] == 1 and s["misses"] == s["lookups"] > 0
 
 
 @pytest.mark.parametrize("fmt", [synth.FMT_MXFP4, synth.FMT_Q4_0])
