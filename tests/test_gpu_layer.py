@@ -469,6 +469,33 @@ def test_prefill_chunk_through_the_layer(tokens):
         assert s["calls"] == 1 and s["misses"] == s["lookups"] > 0
 
 
+@pytest.mark.parametrize("mode", ["auto", "cuda_cores", "tensor_cores"])
+def test_wide_step_with_a_fetch_cap_skips_the_overflow_routes(mode):
+    """A wide step under a fetch cap [FreeToken PR #491, sections 4 and 5: the
+    misses beyond the cap come back as -1 and contribute nothing on the GPU]:
+    200 Zipf rows x top-4 over 64 NVFP4 experts from a cold cache, cap 5, so
+    many routes are -1 and the grouped kernels of every family must skip them.
+    Slot ids and state exact; every row equals the fp64 layer over the routes
+    that got a slot."""
+    import expert_slot_cache_lru_gb300 as m
+    w = synth.scaled(synth.workloads()["wide_decode"], n_experts=64, top_k=4, hidden=256,
+                     inter=128, n_slots=64, batch=200, routing="zipf", prefill_frac=0.0,
+                     fetch_cap=5)
+    rig = Rig(w)
+    m.moe_cache_set_wide_path(rig.sc.handle, {"auto": m.MOE_WIDE_AUTO,
+                                              "cuda_cores": m.MOE_WIDE_CUDA_CORES,
+                                              "tensor_cores": m.MOE_WIDE_TENSOR_CORES}[mode])
+    st = Stepper(rig)
+    ids, wts = synth.make_routing(w, steps=2)
+    for t in range(2):
+        x = synth.make_hidden(w, t)
+        refs = st.step(t, ids[t], wts[t], x)
+        slots = refs[0]["slots"].reshape(w.batch, w.top_k)
+        assert (slots < 0).any() and (slots >= 0).any()
+        ref = rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0], mask=(slots >= 0).astype(np.uint8))
+        assert_close(st.out[0], ref, w.fmt, f"step {t}")
+
+
 @pytest.mark.parametrize("fmt", [synth.FMT_MXFP4, synth.FMT_Q4_0])
 def test_4bit_formats_wide_step_equals_oracle(fmt):
     """Wide steps of MXFP4 and Q4_0 experts (formats listed in FreeToken PR

@@ -127,6 +127,21 @@ def test_lookahead_ties_go_to_the_lower_id():
     _check(got, x, router, 16)
 
 
+def test_lookahead_nan_logit_ranks_last():
+    """A NaN router weight makes expert 7's logit NaN in every row: the GPU
+    never picks it while any number remains, and ranks it last at k = n_experts."""
+    rig = _rig(20, 1024, 3)
+    router = synth.make_router(rig.w, 0)
+    router[7, 5] = 0x7fc0  # bf16 NaN
+    x = synth.make_hidden(rig.w, 3)[0]
+    got = _predict(rig, x, router, 19)
+    assert not (got == 7).any()
+    got = _predict(rig, x, router, 20)
+    assert (got[:, -1] == 7).all()
+    want, _ = oracle.lookahead_predict(x, router, 20)
+    assert (want[:, -1] == 7).all()
+
+
 def test_lookahead_graph_replay_and_repeat():
     """The launch resets its own counter: three launches on different inputs
     captured in one graph and replayed twice give the eager answers."""
