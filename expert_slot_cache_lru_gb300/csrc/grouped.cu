@@ -584,6 +584,169 @@ __global__ void __launch_bounds__(kWT, 2) gup_staged_kernel(DevState st, int H, 
   }
 }
 
+// ------------------------------------------------------------ 3c. gate / up, warp rows
+// The NVFP4 gate/up kernel for H = 1024 JH and I a multiple of kWB, with no
+// operand in shared memory.  A warp takes kWB consecutive rows of one group at
+// a time (units dealt over the grid's warps group-major, so neighbouring warps
+// stream neighbouring rows).  Lane L holds the 16-byte code chunks L, L + 32,
+// ... of each row (32 elements each, so every warp load is 512 contiguous
+// bytes, and its two block scales as one 16-bit load) and the same elements of
+// NQ routes' x in registers, loaded once per unit and pass; the routes left
+// after the full passes go one at a time.  Per row the lane decodes each chunk
+// once, sums each 16-element block's exact half-times-half products in fp32,
+// scales the block sums, and the warp reduces the lanes' gate and up sums of
+// every route with shuffles.  The next row's codes are in flight while a row
+// computes.
+constexpr int kWB = 16;  // rows per warp unit
+
+// the warp totals of g[q], u[q] (q < NQ): lane 16 q holds route q's gate total
+// in gt and its up total in ut
+template <int NQ>
+__device__ __forceinline__ void warp_gu_totals(const float (&g)[NQ], const float (&u)[NQ],
+                                               int lane, float& gt, float& ut) {
+  const bool h16 = lane & 16;
+  float v;
+  if (NQ == 1) {  // lanes < 16 keep g, lanes >= 16 keep u
+    v = (h16 ? u[0] : g[0]) + __shfl_xor_sync(0xffffffffu, h16 ? g[0] : u[0], 16);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+  } else {  // lanes < 16 keep route 0, lanes >= 16 route 1; then bit 3 picks g or u
+    const float k0 = (h16 ? g[NQ - 1] : g[0]) + __shfl_xor_sync(0xffffffffu, h16 ? g[0] : g[NQ - 1], 16);
+    const float k1 = (h16 ? u[NQ - 1] : u[0]) + __shfl_xor_sync(0xffffffffu, h16 ? u[0] : u[NQ - 1], 16);
+    const bool h8 = lane & 8;
+    v = (h8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+  }
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  gt = v;
+  ut = __shfl_xor_sync(0xffffffffu, v, NQ == 1 ? 16 : 8);
+}
+
+// one pass of a warp unit over NR routes (rt): kWB rows from row i0 of the
+// group's expert (code chunk 0 of row 0 of each bank at gc, uc; scales at gsc, usc)
+template <int JH, int NR>
+__device__ __forceinline__ void gup_warp_pass(const uint8_t* gc, const uint8_t* uc,
+                                              const uint8_t* gsc, const uint8_t* usc,
+                                              const uint16_t* __restrict__ x16,
+                                              const float* __restrict__ xinv, int k,
+                                              const int (&rt)[NR], float gs0, float gs1, int I,
+                                              int i0, int lane, float* __restrict__ h) {
+  constexpr int H = 1024 * JH;
+  // the lane's elements of each route's x
+  uint32_t xv[NR][JH][16];
+#pragma unroll
+  for (int q = 0; q < NR; ++q) {
+    const uint4* xp = reinterpret_cast<const uint4*>(x16 + (size_t)(rt[q] / k) * H);
+#pragma unroll
+    for (int j = 0; j < JH; ++j)
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 t = __ldg(xp + (lane + 32 * j) * 4 + v);
+        xv[q][j][4 * v] = t.x, xv[q][j][4 * v + 1] = t.y;
+        xv[q][j][4 * v + 2] = t.z, xv[q][j][4 * v + 3] = t.w;
+      }
+  }
+  uint4 cg[JH], cu[JH];
+  uint32_t sg[JH], su[JH];
+  auto load_row = [&](int r, uint4 (&a)[JH], uint4 (&b)[JH], uint32_t (&sa)[JH],
+                      uint32_t (&sb)[JH]) {
+#pragma unroll
+    for (int j = 0; j < JH; ++j) {
+      a[j] = __ldcs(reinterpret_cast<const uint4*>(gc + (size_t)r * (H / 2) + 512 * j));
+      b[j] = __ldcs(reinterpret_cast<const uint4*>(uc + (size_t)r * (H / 2) + 512 * j));
+      sa[j] = __ldcs(reinterpret_cast<const unsigned short*>(gsc + (size_t)r * (H / 16) + 64 * j));
+      sb[j] = __ldcs(reinterpret_cast<const unsigned short*>(usc + (size_t)r * (H / 16) + 64 * j));
+    }
+  };
+  load_row(0, cg, cu, sg, su);
+#pragma unroll 1
+  for (int r = 0; r < kWB; ++r) {
+    uint4 ng[JH], nu[JH];
+    uint32_t nsg[JH], nsu[JH];
+    load_row(min(r + 1, kWB - 1), ng, nu, nsg, nsu);  // the next row in flight
+    float ga[NR], ua[NR];
+#pragma unroll
+    for (int q = 0; q < NR; ++q) ga[q] = ua[q] = 0.f;
+#pragma unroll
+    for (int j = 0; j < JH; ++j) {
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {  // gate, then up
+        const uint4 c = m ? cu[j] : cg[j];
+        const float2 s = e4m3x2(m ? su[j] : sg[j]);
+        const uint32_t cv[4] = {c.x, c.y, c.z, c.w};
+        uint32_t d[16];
+#pragma unroll
+        for (int wd = 0; wd < 4; ++wd) {
+          d[4 * wd] = e2m1x2<0>(cv[wd]);
+          d[4 * wd + 1] = e2m1x2<1>(cv[wd]);
+          d[4 * wd + 2] = e2m1x2<2>(cv[wd]);
+          d[4 * wd + 3] = e2m1x2<3>(cv[wd]);
+        }
+#pragma unroll
+        for (int q = 0; q < NR; ++q) {
+          float p = 0.f, p2 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            p = fma2h(d[e], xv[q][j][e], p);
+            p2 = fma2h(d[8 + e], xv[q][j][8 + e], p2);
+          }
+          float& acc = m ? ua[q] : ga[q];
+          acc = fmaf(p2, s.y, fmaf(p, s.x, acc));
+        }
+      }
+    }
+    float gt, ut;
+    warp_gu_totals<NR>(ga, ua, lane, gt, ut);
+    const int q = lane >> 4;
+    if ((lane & 15) == 0 && q < NR) {
+      const int rq = rt[NR == 1 ? 0 : q];
+      const float xi = xinv[rq / k];
+      const float gg = gt * xi * gs0, uu = ut * xi * gs1;
+      h[(size_t)rq * I + i0 + r] = gg / (1.f + expf(-gg)) * uu;
+    }
+#pragma unroll
+    for (int j = 0; j < JH; ++j) cg[j] = ng[j], cu[j] = nu[j], sg[j] = nsg[j], su[j] = nsu[j];
+  }
+}
+
+template <int JH, int NQ>
+__global__ void __launch_bounds__(kWT, 2) gup_warp_kernel(DevState st, int I, int layer,
+                                                          const uint16_t* __restrict__ x16,
+                                                          const float* __restrict__ xinv, int k,
+                                                          Groups gr, float* __restrict__ h,
+                                                          int skip_from) {
+  constexpr int H = 1024 * JH;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (kWT / 32) + (threadIdx.x >> 5), Gw = gridDim.x * (kWT / 32);
+  const int G = gr.G(), nb = I / kWB;
+  const Off o(H, I);
+  const size_t pbase = (size_t)pool_of(st, layer) * st.S;
+  for (int un = gw; un < G * nb; un += Gw) {
+    const int g = un / nb, i0 = (un - g * nb) * kWB;
+    const int ra = gr.start()[g], rb = gr.start()[g + 1];
+    if (skip_from > 0 && rb - ra >= skip_from) continue;  // a dense group: the tensor cores take it
+    const uint8_t* blob = st.slots + (pbase + gr.slot()[g]) * st.stride;
+    const float gs0 = reinterpret_cast<const float*>(blob + o.glob)[0];
+    const float gs1 = reinterpret_cast<const float*>(blob + o.glob)[1];
+    // this lane's chunk 0 of row i0 in each bank (chunk j is 512 j bytes on)
+    const uint8_t* gc = blob + o.code[0] + (size_t)i0 * (H / 2) + lane * 16;
+    const uint8_t* uc = blob + o.code[1] + (size_t)i0 * (H / 2) + lane * 16;
+    const uint8_t* gsc = blob + o.scale[0] + (size_t)i0 * (H / 16) + lane * 2;
+    const uint8_t* usc = blob + o.scale[1] + (size_t)i0 * (H / 16) + lane * 2;
+    int q0 = ra;
+    for (; NQ > 1 && q0 + NQ <= rb; q0 += NQ) {  // full passes
+      int rt[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) rt[q] = gr.route()[q0 + q];
+      gup_warp_pass<JH, NQ>(gc, uc, gsc, usc, x16, xinv, k, rt, gs0, gs1, I, i0, lane, h);
+    }
+    for (; q0 < rb; ++q0) {  // the rest one route at a time
+      const int rt[1] = {gr.route()[q0]};
+      gup_warp_pass<JH, 1>(gc, uc, gsc, usc, x16, xinv, k, rt, gs0, gs1, I, i0, lane, h);
+    }
+  }
+}
+
 // ------------------------------------------------------------ 4. down
 // Work item (group g, 256 rows of H): every lane owns one output row n and
 // computes its whole dot product with the h of up to kNR of the group's
@@ -843,6 +1006,7 @@ __global__ void __launch_bounds__(kWT) gcombine_kernel(const DevState st, int H,
 int g_sms = 0;
 int g_occ[4][2] = {{1, 1}, {1, 1}, {1, 1}, {1, 1}};  // resident CTAs per SM: [format][gate-up, down]
 int g_occ_staged[2] = {1, 1};        // ... of the staged NVFP4 kernels
+int g_occ_warp = 1;                   // ... of the warp-row gate/up kernel for the cache's H
 
 size_t gup_staged_smem(int H) { return (size_t)kNR * H * 2 + (size_t)kNS * (2 * kStC + 2 * kStS); }
 size_t gdown_staged_smem(int I) { return (size_t)kNR * I * 4 + (size_t)kNS * (kStC + kStS); }
@@ -850,6 +1014,20 @@ size_t gdown_staged_smem(int I) { return (size_t)kNR * I * 4 + (size_t)kNS * (kS
 bool staged_ok(int H, int I) {
   return H % 64 == 0 && I % 64 == 0 && gup_staged_smem(H) <= 200 * 1024 &&
          gdown_staged_smem(I) <= 200 * 1024;
+}
+
+// the warp-row gate/up kernel: H = 1024 JH (two routes per pass up to 2048,
+// one above, where two routes' x would not fit in registers)
+bool warp_ok(int H, int I) { return H >= 1024 && H <= 4096 && H % 1024 == 0 && I % kWB == 0; }
+template <typename F>
+cudaError_t by_jh(int H, F f) {
+  switch (H / 1024) {
+    case 1: return f(gup_warp_kernel<1, 2>);
+    case 2: return f(gup_warp_kernel<2, 2>);
+    case 3: return f(gup_warp_kernel<3, 1>);
+    case 4: return f(gup_warp_kernel<4, 1>);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -901,6 +1079,12 @@ cudaError_t grouped_init(int E, int H, int I) {
     occ(gup_staged_kernel, gup_staged_smem(H), &g_occ_staged[0]);
     occ(gdown_staged_kernel, gdown_staged_smem(I), &g_occ_staged[1]);
   }
+  if (e == cudaSuccess && warp_ok(H, I))
+    e = by_jh(H, [&](auto kern) {
+      const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_occ_warp, kern, kWT, 0);
+      if (g_occ_warp < 1) g_occ_warp = 1;
+      return r;
+    });
   if (e == cudaSuccess && grouped_tc_supported(MOE_W_NVFP4, H, I)) e = grouped_tc_init();
   return e;
 }
@@ -931,9 +1115,16 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);
     const bool split = tc && cc && staged_ok(H, I);
     const int tc_from = !tc ? 0 : (split ? kTcMinRoutes : 1);  // tensor cores: groups >= this
-    if (cc && staged_ok(H, I))
+    if (cc && warp_ok(H, I)) {
+      const cudaError_t e = by_jh(H, [&](auto kern) {
+        kern<<<sms * g_occ_warp, kWT, 0, s>>>(st, I, layer, sc.x16, sc.xinv, k, gr, sc.h, tc_from);
+        return cudaGetLastError();
+      });
+      if (e != cudaSuccess) return e;
+    } else if (cc && staged_ok(H, I)) {
       gup_staged_kernel<<<sms * g_occ_staged[0], kWT, gup_staged_smem(H), s>>>(
           st, H, I, layer, sc.x16, sc.xinv, k, gr, sc.h, tc_from);
+    }
     if (tc) {
       cudaError_t e = launch_grouped_tc(st, H, I, layer, k, R, max_routes, sc, st.status, s);
       if (e != cudaSuccess) return e;

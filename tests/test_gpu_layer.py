@@ -444,6 +444,32 @@ def test_wide_step_tensor_cores_and_cuda_cores(routing, batch):
         m.moe_cache_set_wide_path(rigs[0].sc.handle, 3)
 
 
+@pytest.mark.parametrize("hidden,inter", [(1024, 64), (2048, 96), (3072, 64), (4096, 32)])
+def test_wide_step_warp_row_gate_up_every_width(hidden, inter):
+    """The gate/up kernel that keeps x in registers (H a multiple of 1,024, up
+    to 4,096; two routes per pass up to 2,048, one above): 32 NVFP4 experts,
+    top-4 over 24 rows, uniform routing, so groups of one to several routes
+    take full and partial passes.  I of 96 and 32 (not multiples of 64) leave
+    the down projection to the unstaged kernel.  Every row against the fp64 layer, in the CUDA-core
+    and the automatic mode."""
+    import expert_slot_cache_lru_gb300 as m
+    w = synth.scaled(synth.workloads()["wide_decode"], n_experts=32, top_k=4, hidden=hidden,
+                     inter=inter, n_slots=32, batch=24, routing="uniform", prefill_frac=0.0)
+    blobs = synth.HostBlobs(w, pinned=True)
+    for mode in (m.MOE_WIDE_CUDA_CORES, m.MOE_WIDE_AUTO):
+        rig = Rig(w, blobs=blobs)
+        m.moe_cache_set_wide_path(rig.sc.handle, mode)
+        st = Stepper(rig)
+        ids, wts = synth.make_routing(w, steps=2)
+        for t in range(2):
+            x = synth.make_hidden(w, t)
+            refs = st.step(t, ids[t], wts[t], x)
+            sizes = [len(r) for _, r in refs[0]["groups"]]
+            assert max(sizes) >= 3 and min(sizes) == 1, sizes
+            ref = rig.oracle_layer(0, x[0], ids[t, 0], wts[t, 0])
+            assert_close(st.out[0], ref, w.fmt, f"H {hidden}, step {t}, mode {mode}")
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("tokens", [16, 64])
 def test_prefill_chunk_through_the_layer(tokens):
