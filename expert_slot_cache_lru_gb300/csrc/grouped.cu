@@ -983,6 +983,142 @@ __global__ void __launch_bounds__(kWT, 2) gdown_staged_kernel(DevState st, int H
   }
 }
 
+// ------------------------------------------------------------ 4c. down, warp rows
+// The NVFP4 down kernel for I = 256 M (M = 1 .. 4), with no operand in shared
+// memory.  A warp takes kWD consecutive output rows of one group at a time
+// (units dealt as in gup_warp_kernel), 8 / NR rows per step.  Lane L holds
+// elements [8ML, 8ML + 8M) of each row (M code words: the warp's M loads
+// cover the row's I / 2 bytes) and its one or two block scales, and the same
+// elements of NR routes' h in registers.  Each 8-element half block's exact
+// e2m1 * h products are summed in fp32 and scaled by the block's e4m3 scale;
+// a step's 8 (row, route) lane sums are then reduced across the warp together,
+// each shuffle level halving the values a lane keeps.
+constexpr int kWD = 32;  // output rows per warp unit
+
+// the warp totals of v[0 .. NV), NV = 4 or 8: lane L ends with the total of
+// value L / (32 / NV)
+template <int NV>
+__device__ __forceinline__ float warp_sum_scatter(float (&v)[NV], int lane) {
+  static_assert(NV == 4 || NV == 8, "four or eight values");
+  constexpr int kLv = NV == 8 ? 3 : 2;  // levels at which a lane gives away half its values
+#pragma unroll
+  for (int l = 0; l < kLv; ++l) {
+    const int s = 16 >> l, half = NV >> (l + 1);
+    const bool up = lane & s;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float keep = up ? v[i + half] : v[i], send = up ? v[i] : v[i + half];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  float t = v[0];
+#pragma unroll
+  for (int s = 16 >> kLv; s > 0; s >>= 1) t += __shfl_xor_sync(0xffffffffu, t, s);
+  return t;
+}
+
+// one pass of a warp unit over NR routes (rt): kWD rows from output row n0
+// (this lane's code word 0 of row n0 at cw0, the row's scales at sc0)
+template <int M, int NR>
+__device__ __forceinline__ void gdown_warp_pass(const uint8_t* cw0, const uint8_t* sc0,
+                                                const float* __restrict__ h, const int (&rt)[NR],
+                                                float gs2, int H, int n0, int lane,
+                                                float* __restrict__ y) {
+  constexpr int I = 256 * M, RG = 8 / NR;
+  float hv[NR][8 * M];
+#pragma unroll
+  for (int q = 0; q < NR; ++q) {
+    const float4* hp = reinterpret_cast<const float4*>(h + (size_t)rt[q] * I + 8 * M * lane);
+#pragma unroll
+    for (int v = 0; v < 2 * M; ++v) {
+      const float4 t = __ldcg(hp + v);
+      hv[q][4 * v] = t.x, hv[q][4 * v + 1] = t.y, hv[q][4 * v + 2] = t.z, hv[q][4 * v + 3] = t.w;
+    }
+  }
+  // the lane's half blocks M L + t (t < M) lie in blocks b0 and, if `two`, b0 + 1
+  const int b0 = (M * lane) >> 1;
+  const bool two = ((M * lane + M - 1) >> 1) != b0;
+#pragma unroll 1
+  for (int r0 = 0; r0 < kWD; r0 += RG) {
+    uint32_t cw[RG][M], sc[RG];
+#pragma unroll
+    for (int rr = 0; rr < RG; ++rr) {
+      const uint32_t* cr = reinterpret_cast<const uint32_t*>(cw0 + (size_t)(r0 + rr) * (I / 2));
+#pragma unroll
+      for (int t = 0; t < M; ++t) cw[rr][t] = __ldcs(cr + t);
+      const unsigned char* sr = sc0 + (size_t)(r0 + rr) * (I / 16) + b0;
+      sc[rr] = __ldcs(sr) | (two ? (uint32_t)__ldcs(sr + 1) << 8 : 0u);
+    }
+    float acc[8];
+#pragma unroll
+    for (int rr = 0; rr < RG; ++rr) {
+      const float2 s = e4m3x2(sc[rr]);
+      float a[NR];
+#pragma unroll
+      for (int q = 0; q < NR; ++q) a[q] = 0.f;
+#pragma unroll
+      for (int t = 0; t < M; ++t) {
+        const float st = ((M * lane + t) >> 1) == b0 ? s.x : s.y;
+        float wf[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float2 f = f16x2_f32(b == 0   ? e2m1x2<0>(cw[rr][t])
+                                     : b == 1 ? e2m1x2<1>(cw[rr][t])
+                                     : b == 2 ? e2m1x2<2>(cw[rr][t])
+                                              : e2m1x2<3>(cw[rr][t]));
+          wf[2 * b] = f.x, wf[2 * b + 1] = f.y;
+        }
+#pragma unroll
+        for (int q = 0; q < NR; ++q) {
+          float p = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) p = fmaf(wf[e], hv[q][8 * t + e], p);
+          a[q] = fmaf(p, st, a[q]);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < NR; ++q) acc[rr * NR + q] = a[q];
+    }
+    const float tot = warp_sum_scatter<8>(acc, lane);
+    if ((lane & 3) == 0) {
+      const int vi = lane >> 2, rr = vi / NR, q = vi - rr * NR;
+      y[(size_t)rt[q] * H + n0 + r0 + rr] = tot * gs2;
+    }
+  }
+}
+
+template <int M, int NQ>
+__global__ void __launch_bounds__(kWT, 2) gdown_warp_kernel(DevState st, int H, int layer,
+                                                            Groups gr, const float* __restrict__ h,
+                                                            float* __restrict__ y, int skip_from) {
+  constexpr int I = 256 * M;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (kWT / 32) + (threadIdx.x >> 5), Gw = gridDim.x * (kWT / 32);
+  const int G = gr.G(), nb = H / kWD;
+  const Off o(H, I);
+  const size_t pbase = (size_t)pool_of(st, layer) * st.S;
+  for (int un = gw; un < G * nb; un += Gw) {
+    const int g = un / nb, n0 = (un - g * nb) * kWD;
+    const int ra = gr.start()[g], rb = gr.start()[g + 1];
+    if (skip_from > 0 && rb - ra >= skip_from) continue;  // a dense group: the tensor cores take it
+    const uint8_t* blob = st.slots + (pbase + gr.slot()[g]) * st.stride;
+    const float gs2 = reinterpret_cast<const float*>(blob + o.glob)[2];
+    const uint8_t* cw0 = blob + o.code[2] + (size_t)n0 * (I / 2) + 4 * M * lane;
+    const uint8_t* sc0 = blob + o.scale[2] + (size_t)n0 * (I / 16);
+    int q0 = ra;
+    for (; NQ > 1 && q0 + NQ <= rb; q0 += NQ) {  // full passes
+      int rt[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) rt[q] = gr.route()[q0 + q];
+      gdown_warp_pass<M, NQ>(cw0, sc0, h, rt, gs2, H, n0, lane, y);
+    }
+    for (; q0 < rb; ++q0) {  // the rest one route at a time
+      const int rt[1] = {gr.route()[q0]};
+      gdown_warp_pass<M, 1>(cw0, sc0, h, rt, gs2, H, n0, lane, y);
+    }
+  }
+}
+
 // ------------------------------------------------------------ 5. combine
 __global__ void __launch_bounds__(kWT) gcombine_kernel(const DevState st, int H, int k,
                                                        const int32_t* __restrict__ slot_ids,
@@ -1007,6 +1143,7 @@ int g_sms = 0;
 int g_occ[4][2] = {{1, 1}, {1, 1}, {1, 1}, {1, 1}};  // resident CTAs per SM: [format][gate-up, down]
 int g_occ_staged[2] = {1, 1};        // ... of the staged NVFP4 kernels
 int g_occ_warp = 1;                   // ... of the warp-row gate/up kernel for the cache's H
+int g_occ_dwarp = 1;                  // ... of the warp-row down kernel for the cache's I
 
 size_t gup_staged_smem(int H) { return (size_t)kNR * H * 2 + (size_t)kNS * (2 * kStC + 2 * kStS); }
 size_t gdown_staged_smem(int I) { return (size_t)kNR * I * 4 + (size_t)kNS * (kStC + kStS); }
@@ -1019,6 +1156,20 @@ bool staged_ok(int H, int I) {
 // the warp-row gate/up kernel: H = 1024 JH (two routes per pass up to 2048,
 // one above, where two routes' x would not fit in registers)
 bool warp_ok(int H, int I) { return H >= 1024 && H <= 4096 && H % 1024 == 0 && I % kWB == 0; }
+// the warp-row down kernel: I = 256 M, M = 1 .. 4; H in whole units
+bool down_warp_ok(int H, int I) {
+  return I >= 256 && I <= 1024 && I % 256 == 0 && H % kWD == 0;
+}
+template <typename F>
+cudaError_t by_m(int I, F f) {
+  switch (I / 256) {
+    case 1: return f(gdown_warp_kernel<1, 2>);
+    case 2: return f(gdown_warp_kernel<2, 2>);
+    case 3: return f(gdown_warp_kernel<3, 2>);
+    case 4: return f(gdown_warp_kernel<4, 2>);
+    default: return cudaErrorInvalidValue;
+  }
+}
 template <typename F>
 cudaError_t by_jh(int H, F f) {
   switch (H / 1024) {
@@ -1085,6 +1236,12 @@ cudaError_t grouped_init(int E, int H, int I) {
       if (g_occ_warp < 1) g_occ_warp = 1;
       return r;
     });
+  if (e == cudaSuccess && down_warp_ok(H, I))
+    e = by_m(I, [&](auto kern) {
+      const cudaError_t r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_occ_dwarp, kern, kWT, 0);
+      if (g_occ_dwarp < 1) g_occ_dwarp = 1;
+      return r;
+    });
   if (e == cudaSuccess && grouped_tc_supported(MOE_W_NVFP4, H, I)) e = grouped_tc_init();
   return e;
 }
@@ -1129,9 +1286,16 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
       cudaError_t e = launch_grouped_tc(st, H, I, layer, k, R, max_routes, sc, st.status, s);
       if (e != cudaSuccess) return e;
     }
-    if (cc && staged_ok(H, I))
+    if (cc && down_warp_ok(H, I)) {
+      const cudaError_t e = by_m(I, [&](auto kern) {
+        kern<<<sms * g_occ_dwarp, kWT, 0, s>>>(st, H, layer, gr, sc.h, sc.y, tc_from);
+        return cudaGetLastError();
+      });
+      if (e != cudaSuccess) return e;
+    } else if (cc && staged_ok(H, I)) {
       gdown_staged_kernel<<<sms * g_occ_staged[1], kWT, gdown_staged_smem(I), s>>>(
           st, H, I, layer, gr, sc.h, sc.y, tc_from);
+    }
   } else if (wfmt == MOE_W_NVFP4 || wfmt == MOE_W_MXFP4 || wfmt == MOE_W_Q4_0) {
     // the CUDA-core kernels of the 4-bit format (x as f16 for every one)
     xprep_kernel<MOE_W_NVFP4><<<n_rows, kWT, 0, s>>>(xx, H, sc.x16, sc.xinv);

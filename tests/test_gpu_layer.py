@@ -444,14 +444,17 @@ def test_wide_step_tensor_cores_and_cuda_cores(routing, batch):
         m.moe_cache_set_wide_path(rigs[0].sc.handle, 3)
 
 
-@pytest.mark.parametrize("hidden,inter", [(1024, 64), (2048, 96), (3072, 64), (4096, 32)])
-def test_wide_step_warp_row_gate_up_every_width(hidden, inter):
-    """The gate/up kernel that keeps x in registers (H a multiple of 1,024, up
-    to 4,096; two routes per pass up to 2,048, one above): 32 NVFP4 experts,
-    top-4 over 24 rows, uniform routing, so groups of one to several routes
-    take full and partial passes.  I of 96 and 32 (not multiples of 64) leave
-    the down projection to the unstaged kernel.  Every row against the fp64 layer, in the CUDA-core
-    and the automatic mode."""
+@pytest.mark.parametrize("hidden,inter", [(1024, 64), (2048, 96), (3072, 64), (4096, 32),
+                                          (1024, 1024), (2048, 768), (3072, 512), (4096, 256)])
+def test_wide_step_warp_row_kernels_every_width(hidden, inter):
+    """The gate/up and down kernels that keep x and h in registers: gate/up for
+    H a multiple of 1,024 up to 4,096 (two routes per pass up to 2,048, one
+    above), down for I of 256, 512, 768 and 1,024 (lanes holding one or two
+    block scales).  32 NVFP4 experts, top-4 over 24 rows, uniform routing, so
+    groups of one to several routes take full and partial passes.  The first
+    four shapes leave the down projection to the other CUDA-core kernels (I of
+    96 and 32 to the unstaged one).  Every row against the fp64 layer, in the
+    CUDA-core and the automatic mode."""
     import expert_slot_cache_lru_gb300 as m
     w = synth.scaled(synth.workloads()["wide_decode"], n_experts=32, top_k=4, hidden=hidden,
                      inter=inter, n_slots=32, batch=24, routing="uniform", prefill_frac=0.0)
