@@ -992,7 +992,8 @@ __global__ void __launch_bounds__(kWT, 2) gdown_staged_kernel(DevState st, int H
 // elements of NR routes' h in registers.  Each 8-element half block's exact
 // e2m1 * h products are summed in fp32 and scaled by the block's e4m3 scale;
 // a step's 8 (row, route) lane sums are then reduced across the warp together,
-// each shuffle level halving the values a lane keeps.
+// each shuffle level halving the values a lane keeps.  The next step's rows
+// are in flight while a step computes.
 constexpr int kWD = 32;  // output rows per warp unit
 
 // the warp totals of v[0 .. NV), NV = 4 or 8: lane L ends with the total of
@@ -1038,9 +1039,7 @@ __device__ __forceinline__ void gdown_warp_pass(const uint8_t* cw0, const uint8_
   // the lane's half blocks M L + t (t < M) lie in blocks b0 and, if `two`, b0 + 1
   const int b0 = (M * lane) >> 1;
   const bool two = ((M * lane + M - 1) >> 1) != b0;
-#pragma unroll 1
-  for (int r0 = 0; r0 < kWD; r0 += RG) {
-    uint32_t cw[RG][M], sc[RG];
+  auto load_step = [&](int r0, uint32_t (&cw)[RG][M], uint32_t (&sc)[RG]) {
 #pragma unroll
     for (int rr = 0; rr < RG; ++rr) {
       const uint32_t* cr = reinterpret_cast<const uint32_t*>(cw0 + (size_t)(r0 + rr) * (I / 2));
@@ -1049,6 +1048,13 @@ __device__ __forceinline__ void gdown_warp_pass(const uint8_t* cw0, const uint8_
       const unsigned char* sr = sc0 + (size_t)(r0 + rr) * (I / 16) + b0;
       sc[rr] = __ldcs(sr) | (two ? (uint32_t)__ldcs(sr + 1) << 8 : 0u);
     }
+  };
+  uint32_t cw[RG][M], sc[RG];
+  load_step(0, cw, sc);
+#pragma unroll 1
+  for (int r0 = 0; r0 < kWD; r0 += RG) {
+    uint32_t ncw[RG][M], nsc[RG];
+    load_step(min(r0 + RG, kWD - RG), ncw, nsc);  // the next step's rows in flight
     float acc[8];
 #pragma unroll
     for (int rr = 0; rr < RG; ++rr) {
@@ -1083,6 +1089,12 @@ __device__ __forceinline__ void gdown_warp_pass(const uint8_t* cw0, const uint8_
     if ((lane & 3) == 0) {
       const int vi = lane >> 2, rr = vi / NR, q = vi - rr * NR;
       y[(size_t)rt[q] * H + n0 + r0 + rr] = tot * gs2;
+    }
+#pragma unroll
+    for (int rr = 0; rr < RG; ++rr) {
+      sc[rr] = nsc[rr];
+#pragma unroll
+      for (int t = 0; t < M; ++t) cw[rr][t] = ncw[rr][t];
     }
   }
 }
