@@ -82,15 +82,10 @@ cudaError_t launch_pin(const DevState& st, int layer, int slot, int pinned, cuda
 }
 
 cudaError_t admit_set_smem_limits(int E, int S) {
-  cudaError_t e = cudaFuncSetAttribute(admit_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)admit_smem_bytes(E, S));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(admit_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)admit_smem_bytes(E, S));
+  cudaError_t e = raise_smem_limit(admit_kernel<true>, admit_smem_bytes(E, S));
+  if (e == cudaSuccess) e = raise_smem_limit(admit_kernel<false>, admit_smem_bytes(E, S));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefetch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(2ull * E * sizeof(int)));
+  return raise_smem_limit(prefetch_kernel, 2ull * E * sizeof(int));
 }
 
 }  // namespace moe

@@ -11,6 +11,19 @@
 
 namespace moe {
 
+// Raises kern's dynamic shared-memory limit to `bytes` and never lowers it: the
+// limit belongs to the kernel, not to a cache, so a cache created later with
+// smaller shapes must leave an earlier cache's launches valid.  The caller
+// holds moe_cache_create's setup lock (the read and the write are not atomic).
+// (The default limit is 48 KiB less the kernel's static shared memory.)
+template <typename K>
+inline cudaError_t raise_smem_limit(K kern, size_t bytes) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess || (size_t)fa.maxDynamicSharedSizeBytes >= bytes) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
 // Everything a kernel needs to reach the cache state; passed by value.
 struct DevState {
   int L, E, S, P;          // layers, experts per layer, slots per pool, pools

@@ -300,8 +300,7 @@ down_combine_kernel(DevState st, int H, int I, int layer, const int32_t* __restr
 
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return raise_smem_limit(kernel, bytes);
 }
 
 template <int FMT>

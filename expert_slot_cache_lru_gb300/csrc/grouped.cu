@@ -1207,12 +1207,9 @@ cudaError_t grouped_init(int E, int H, int I) {
   int dev;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess && (size_t)E * 12 > 48 * 1024)
-    e = cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)E * 12));
+  if (e == cudaSuccess) e = raise_smem_limit(group_kernel, (size_t)E * 12);
   auto lim = [&](auto kern, size_t bytes) {
-    if (e == cudaSuccess && bytes > 48 * 1024)
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) e = raise_smem_limit(kern, bytes);
   };
   const size_t ub = (size_t)kNR * H * 2, db = (size_t)kNR * I * 4;
   lim(gup_kernel<MOE_W_NVFP4>, ub);

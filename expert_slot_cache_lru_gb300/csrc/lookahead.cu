@@ -161,8 +161,9 @@ cudaError_t by_width(int H, F f) {
 }
 }  // namespace
 
-// the kernel's shared-memory limit (once per device, for the cache's H; set
-// whatever its size: the static part counts against the default 48 KiB too)
+// the kernel's shared-memory limit for the cache's H (each H has its own
+// kernel, so no other cache lowers it).  Set whatever its size: the static part
+// counts against the default 48 KiB too.
 cudaError_t lookahead_init(int H) {
   const size_t smem = (size_t)kLaChunk * H * 2;
   return by_width(H, [&](auto kern) {

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -49,6 +50,7 @@ struct moe_cache {
 namespace {
 
 thread_local char g_cuda_err[256] = "";
+std::mutex g_setup_mu;  // serialises the kernel set-up of moe_cache_create
 
 int cuda_fail(cudaError_t e, const char* what) {
   std::snprintf(g_cuda_err, sizeof g_cuda_err, "%.160s: %.80s (%d)", what, cudaGetErrorString(e), (int)e);
@@ -271,17 +273,25 @@ int moe_cache_create(const moe_cache_desc* desc, moe_cache** out) {
     if (e != cudaSuccess) return fail(cuda_fail(e, "host blob table"));
   }
 
-  e = moe::admit_set_smem_limits(d.n_experts, d.n_slots);
-  if (e != cudaSuccess) return fail(cuda_fail(e, "admission shared memory"));
+  {
+    // kernel attributes and occupancy figures are per kernel, shared by every
+    // cache: one create at a time sets them (limits only ever rise)
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    e = moe::admit_set_smem_limits(d.n_experts, d.n_slots);
+    if (e != cudaSuccess) return fail(cuda_fail(e, "admission shared memory"));
+    if (compute) {
+      // the down kernel stages k routes' intermediates in shared memory
+      c->down_k_max = (int)std::min<size_t>(d.max_routes, (200 * 1024) / ((size_t)I * 4));
+      e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
+      if (e == cudaSuccess) e = moe::ffn_stream_init();
+      if (e == cudaSuccess && moe::lookahead_supported(H, d.n_experts, 1))
+        e = moe::lookahead_init(H);
+      if (e == cudaSuccess && moe::grouped_supported(d.wfmt, H, I, d.n_experts))
+        e = moe::grouped_init(d.n_experts, H, I);
+      if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
+    }
+  }
   if (compute) {
-    // the down kernel stages k routes' intermediates in shared memory
-    c->down_k_max = (int)std::min<size_t>(d.max_routes, (200 * 1024) / ((size_t)I * 4));
-    e = moe::gemv_set_smem_limits(H, I, Is, c->down_k_max);
-    if (e == cudaSuccess) e = moe::ffn_stream_init();
-    if (e == cudaSuccess && moe::lookahead_supported(H, d.n_experts, 1)) e = moe::lookahead_init(H);
-    if (e == cudaSuccess && moe::grouped_supported(d.wfmt, H, I, d.n_experts))
-      e = moe::grouped_init(d.n_experts, H, I);
-    if (e != cudaSuccess) return fail(cuda_fail(e, "GEMV shared memory"));
     // a layer launch with the admission inside copies an uncapped step's misses
     // into staging entries while the admission runs: up to max_routes of them,
     // within 64 MB

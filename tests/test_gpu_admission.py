@@ -102,6 +102,24 @@ def test_max_experts_and_slots():
         assert_state_equal(rig.sc, rig.oc, what=f"step {step}")
 
 
+def test_a_smaller_cache_leaves_a_larger_caches_limits():
+    """Shared-memory limits belong to the kernels, not to a cache: a 512-expert,
+    4,000-slot pool keeps its admission state in 54 KB of shared memory, and
+    creating a 16-expert, 8-slot cache afterwards must not lower the limit the
+    larger cache's admissions need.  Both keep admitting with the state exact."""
+    big = synth.Workload("big", 1, 512, 8, 0, 0, 0, 4000, False, 1, 1, 7)
+    small = synth.Workload("small", 1, 16, 2, 0, 0, 0, 8, False, 1, 1, 8)
+    rnd = np.random.default_rng(11)
+    rb = Rig(big, storage=False, max_routes=512)
+    _admit(rb, 0, rnd.integers(0, 512, 400).astype(np.int32))
+    rs = Rig(small, storage=False)
+    for step in range(3):
+        _admit(rs, 0, rnd.integers(0, 16, 6).astype(np.int32))
+        _admit(rb, 0, rnd.integers(0, 512, 400).astype(np.int32))
+    assert_state_equal(rb.sc, rb.oc, what="the larger cache")
+    assert_state_equal(rs.sc, rs.oc, what="the smaller cache")
+
+
 def test_qwen3moe_admission_sequence():
     """The 40-layer, 3,164-slot routing of the decode benchmark, admission
     only: state exact after every token (radix select over old stamps)."""
