@@ -112,7 +112,7 @@ def test_a_smaller_cache_leaves_a_larger_caches_limits():
     rnd = np.random.default_rng(11)
     rb = Rig(big, storage=False, max_routes=512)
     _admit(rb, 0, rnd.integers(0, 512, 400).astype(np.int32))
-    rs = Rig(small, storage=False)
+    rs = Rig(small, storage=False, max_routes=8)
     for step in range(3):
         _admit(rs, 0, rnd.integers(0, 16, 6).astype(np.int32))
         _admit(rb, 0, rnd.integers(0, 512, 400).astype(np.int32))
