@@ -598,6 +598,11 @@ __global__ void __launch_bounds__(kWT, 2) gup_staged_kernel(DevState st, int H, 
 // every route with shuffles.  The next row's codes are in flight while a row
 // computes.
 constexpr int kWB = 16;  // rows per warp unit
+constexpr int kPfAhead = 3;  // rows (steps) ahead that the warp-row kernels ask L2 to fetch
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 // the warp totals of g[q], u[q] (q < NQ): lane 16 q holds route q's gate total
 // in gt and its up total in ut
@@ -658,9 +663,21 @@ __device__ __forceinline__ void gup_warp_pass(const uint8_t* gc, const uint8_t* 
       sb[j] = __ldcs(reinterpret_cast<const unsigned short*>(usc + (size_t)r * (H / 16) + 64 * j));
     }
   };
+  auto prefetch_row = [&](int r) {  // into L2, kPfAhead rows before the row's loads
+#pragma unroll
+    for (int j = 0; j < JH; ++j) {
+      prefetch_l2(gc + (size_t)r * (H / 2) + 512 * j);
+      prefetch_l2(uc + (size_t)r * (H / 2) + 512 * j);
+    }
+    prefetch_l2(gsc + (size_t)r * (H / 16));
+    prefetch_l2(usc + (size_t)r * (H / 16));
+  };
+#pragma unroll
+  for (int r = 1; r < kPfAhead; ++r) prefetch_row(r);
   load_row(0, cg, cu, sg, su);
 #pragma unroll 1
   for (int r = 0; r < kWB; ++r) {
+    if (r + kPfAhead < kWB) prefetch_row(r + kPfAhead);
     uint4 ng[JH], nu[JH];
     uint32_t nsg[JH], nsu[JH];
     load_row(min(r + 1, kWB - 1), ng, nu, nsg, nsu);  // the next row in flight
@@ -1049,10 +1066,21 @@ __device__ __forceinline__ void gdown_warp_pass(const uint8_t* cw0, const uint8_
       sc[rr] = __ldcs(sr) | (two ? (uint32_t)__ldcs(sr + 1) << 8 : 0u);
     }
   };
+  auto prefetch_step = [&](int r0) {  // into L2, kPfAhead steps before the step's loads
+#pragma unroll
+    for (int rr = 0; rr < RG; ++rr) {
+      prefetch_l2(cw0 + (size_t)(r0 + rr) * (I / 2));
+      prefetch_l2(sc0 + (size_t)(r0 + rr) * (I / 16) + b0);
+    }
+  };
+#pragma unroll
+  for (int k = 1; k < kPfAhead; ++k)
+    if (k * RG < kWD) prefetch_step(k * RG);
   uint32_t cw[RG][M], sc[RG];
   load_step(0, cw, sc);
 #pragma unroll 1
   for (int r0 = 0; r0 < kWD; r0 += RG) {
+    if (r0 + kPfAhead * RG < kWD) prefetch_step(r0 + kPfAhead * RG);
     uint32_t ncw[RG][M], nsc[RG];
     load_step(min(r0 + RG, kWD - RG), ncw, nsc);  // the next step's rows in flight
     float acc[8];
