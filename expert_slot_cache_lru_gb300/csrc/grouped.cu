@@ -10,19 +10,24 @@
 //
 // A wide step (hundreds of rows, top-k) routes ~1-10 rows to each of hundreds
 // of experts: about two multiply-adds per weight byte, so the work is bound by
-// reading every resident expert once from HBM, not by arithmetic.  The kernels
+// reading every resident expert once from HBM (and, on the CUDA cores, by the
+// instructions of the exact products), not by the tensor cores.  The kernels
 // therefore group the routes by expert and read each expert's weights once:
 //   1. group_kernel   (1 CTA): the CSR of routes per distinct expert, ascending
 //      expert id, routes ascending within a group -- the cache's route groups;
 //   2. xprep_kernel:  x as f16 (4-bit experts; per-row power-of-two scale so
 //      that max |x| < 2^15, undone on the fp32 sums) or bf16 (bf16 experts);
-//   3. gup_kernel:    per (group, 256 rows of I): h[r] = silu(W_g x_b) * (W_u x_b)
-//      for every route r of the group, one row per thread -- each weight block
-//      is decoded once and applied to up to four routes at a time;
-//   4. gdown_kernel:  per (group, 256 rows of H): y[r] = gs_d * W_d h[r];
+//   3. gate/up:       h[r] = silu(W_g x_b) * (W_u x_b) for every route r of a
+//      group -- NVFP4 at H = 1024 JH: gup_warp_kernel (a warp per 16 rows,
+//      lanes over K, x in registers); other shapes: gup_staged_kernel /
+//      gup_kernel (a thread per row, x broadcast from shared memory);
+//   4. down:          y[r] = gs_d * W_d h[r] -- NVFP4 at I = 256 M:
+//      gdown_warp_kernel (a warp per 32 rows, h in registers); other shapes:
+//      gdown_staged_kernel / gdown_kernel;
 //   5. combine_kernel: out[b][n] = bf16( sum_j w[b,j] y[b*k+j][n] + ys[b][n] ).
 // Kernels 3 and 4 are persistent (a few CTAs per SM walk the work items), so
-// the data-dependent number of groups needs no host round trip.
+// the data-dependent number of groups needs no host round trip.  Expert groups
+// of many routes may go to the tensor cores instead (grouped_tc.cu).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
