@@ -504,16 +504,18 @@ def test_prefill_chunk_through_the_layer(tokens):
 
 
 @pytest.mark.parametrize("mode", ["auto", "cuda_cores", "tensor_cores"])
-def test_wide_step_with_a_fetch_cap_skips_the_overflow_routes(mode):
+@pytest.mark.parametrize("hidden,inter", [(256, 128), (1024, 256)])
+def test_wide_step_with_a_fetch_cap_skips_the_overflow_routes(mode, hidden, inter):
     """A wide step under a fetch cap [FreeToken PR #491, sections 4 and 5: the
     misses beyond the cap come back as -1 and contribute nothing on the GPU]:
     200 Zipf rows x top-4 over 64 NVFP4 experts from a cold cache, cap 5, so
-    many routes are -1 and the grouped kernels of every family must skip them.
-    Slot ids and state exact; every row equals the fp64 layer over the routes
-    that got a slot."""
+    many routes are -1 and the grouped kernels of every family must skip them
+    (H 256: the thread-per-row CUDA-core kernels; H 1,024, I 256: the warp-row
+    ones).  Slot ids and state exact; every row equals the fp64 layer over the
+    routes that got a slot."""
     import expert_slot_cache_lru_gb300 as m
-    w = synth.scaled(synth.workloads()["wide_decode"], n_experts=64, top_k=4, hidden=256,
-                     inter=128, n_slots=64, batch=200, routing="zipf", prefill_frac=0.0,
+    w = synth.scaled(synth.workloads()["wide_decode"], n_experts=64, top_k=4, hidden=hidden,
+                     inter=inter, n_slots=64, batch=200, routing="zipf", prefill_frac=0.0,
                      fetch_cap=5)
     rig = Rig(w)
     m.moe_cache_set_wide_path(rig.sc.handle, {"auto": m.MOE_WIDE_AUTO,
