@@ -18,7 +18,7 @@
 //   2. xprep_kernel:  x as f16 (4-bit experts; per-row power-of-two scale so
 //      that max |x| < 2^15, undone on the fp32 sums) or bf16 (bf16 experts);
 //   3. gate/up:       h[r] = silu(W_g x_b) * (W_u x_b) for every route r of a
-//      group -- NVFP4 at H = 1024 JH: gup_warp_kernel (a warp per 16 rows,
+//      group -- NVFP4 at H = 1024 JH: gup_warp_kernel (a warp per 8 rows,
 //      lanes over K, x in registers); other shapes: gup_staged_kernel /
 //      gup_kernel (a thread per row, x broadcast from shared memory);
 //   4. down:          y[r] = gs_d * W_d h[r] -- NVFP4 at I = 256 M:
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kWT, 2) gup_staged_kernel(DevState st, int H, 
 // scales the block sums, and the warp reduces the lanes' gate and up sums of
 // every route with shuffles.  The next row's codes are in flight while a row
 // computes.
-constexpr int kWB = 16;  // rows per warp unit
+constexpr int kWB = 8;   // rows per warp unit
 constexpr int kPfAhead = 3;  // rows (steps) ahead that the warp-row kernels ask L2 to fetch
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
