@@ -684,7 +684,7 @@ def wide_step(dev: int, reps: int = 5, routing: str = "uniform") -> dict:
     slots = d_slots.cpu().numpy()
     distinct = len(set(int(v) for v in slots if v >= 0))
     _, counts = np.unique(slots[slots >= 0], return_counts=True)
-    dense_groups = int((counts >= 8).sum())
+    dense_groups = int((counts >= 4).sum())
     ffn_bytes = distinct * w.blob_bytes + w.batch * w.hidden * 2 * 2 + R * 8
     times = []
     for _ in range(reps):
@@ -758,9 +758,9 @@ def wide_step(dev: int, reps: int = 5, routing: str = "uniform") -> dict:
             "gather_ms": round(t_gat, 3),
             "gather_gbs": round(st["fetched"] * w.blob_bytes / (t_gat * 1e-3) / 1e9, 1),
             "admission_us_graph": adm_graph,
-            "ffn_path": "automatic: expert groups of >= 8 routes on the tensor cores (tcgen05), "
+            "ffn_path": "automatic: expert groups of >= 4 routes on the tensor cores (tcgen05), "
                         "the rest on the CUDA cores",
-            "groups_ge_8_routes": dense_groups,
+            "groups_ge_4_routes": dense_groups,
             "ffn_ms_first": round(t_ffn, 3), "ffn_ms": round(t_ffn_hot, 3),
             "ffn_bytes": ffn_bytes, "ffn_gbs": round(ffn_bytes / (t_ffn_hot * 1e-3) / 1e9, 1),
             "ffn_ms_all_cuda_cores": round(forced["cuda_cores"], 3),

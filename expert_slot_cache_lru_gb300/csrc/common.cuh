@@ -257,8 +257,10 @@ cudaError_t launch_routed_grouped(const DevState& st, int wfmt, int H, int I, in
 // 100 cycles to issue whatever its N, i.e. ~20 fp4 weights per cycle per SM,
 // half of what HBM delivers to an SM; the CUDA-core kernels reread nothing and
 // win while a group has few routes.  In the automatic mode groups of at least
-// kTcMinRoutes routes go to the tensor cores and the rest to the CUDA cores.
-constexpr int kTcMinRoutes = 8;
+// kTcMinRoutes routes go to the tensor cores and the rest to the CUDA cores (4
+// measured best of 3, 4, 6, 8, 12, 16 and 24 on the wide step's Zipf and
+// uniform routings).
+constexpr int kTcMinRoutes = 4;
 bool grouped_tc_supported(int wfmt, int H, int I);
 cudaError_t grouped_tc_init();
 cudaError_t launch_grouped_tc(const DevState& st, int H, int I, int layer, int k, int n_routes,

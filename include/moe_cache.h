@@ -447,7 +447,7 @@ MOE_API int moe_device_views(moe_cache* c, moe_views* out);
  * to 32 routes, fp32 accumulators in tensor memory; h is rounded to f16 with a
  * per-route power-of-two scale before the down GEMM) and the CUDA cores (fp32
  * h).  A tensor-core MMA costs the same whatever its route count, so:
- *   MOE_WIDE_AUTO (the default): groups of at least 8 routes on the tensor
+ *   MOE_WIDE_AUTO (the default): groups of at least 4 routes on the tensor
  *     cores, smaller groups on the CUDA cores -- the tensor cores only where
  *     the group is a real dense contraction;
  *   MOE_WIDE_CUDA_CORES: every group on the CUDA cores;

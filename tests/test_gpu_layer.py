@@ -396,8 +396,9 @@ def test_wide_decode_step(routing, min_misses):
     grouped routed FFNs.  Every slot id exact; the route groups the GPU built
     equal the oracle's; every one of the 600 rows' outputs within the NVFP4
     tolerance of the fp64 layer.  Uniform routing gives every expert one to a
-    few routes (all on the CUDA cores); Zipf routing gives some experts dozens,
-    which the automatic mode sends to the tensor cores."""
+    few routes (37 groups of four or more go to the tensor cores in the
+    automatic mode, the rest to the CUDA cores); Zipf routing gives some
+    experts dozens (47 groups of four or more)."""
     w = synth.scaled(synth.workloads()["wide_decode"], routing=routing)
     rig = Rig(w)
     rig.prefill(0, synth.prefill_ids(w))
@@ -412,7 +413,7 @@ def test_wide_decode_step(routing, min_misses):
     s = rig.sc.stats(0)
     assert s["fetched"] == s["misses"] > min_misses and s["evictions"] == 0
     if routing == "zipf":
-        assert max(len(r) for _, r in refs[0]["groups"]) >= 8  # tensor-core groups
+        assert max(len(r) for _, r in refs[0]["groups"]) >= 4  # tensor-core groups
 
 
 @pytest.mark.parametrize("routing,batch", [("zipf", 200), ("uniform", 40)])
@@ -443,7 +444,7 @@ def test_wide_step_tensor_cores_and_cuda_cores(routing, batch):
             assert_close(st.out[0], ref, w.fmt, f"step {t}, mode {mode}")
         if routing == "zipf":
             sizes = [len(r) for _, r in refs[0]["groups"]]
-            assert max(sizes) > 32 and min(sizes) < 8, sizes
+            assert max(sizes) > 32 and min(sizes) < 4, sizes
     assert_state_equal(rigs[0].sc, rigs[1].oc)
     with pytest.raises(m.MoeError):
         m.moe_cache_set_wide_path(rigs[0].sc.handle, 3)
