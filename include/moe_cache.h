@@ -215,7 +215,10 @@ typedef struct {
  * descriptor (MOE_ERR_CONFIG), translates each host blob pointer to a device
  * address (cudaHostGetDevicePointer; MOE_ERR_CONFIG if a pointer is not
  * pinned, mapped memory), allocates state and scratch (MOE_ERR_CUDA on
- * failure) and creates the events.  Uses the current CUDA device. */
+ * failure) and creates the events.  Uses the current CUDA device.  It also
+ * raises the library kernels' shared-memory limits to what this cache's shapes
+ * need (never lowers them, so caches of other shapes stay valid); creates on
+ * several threads take turns for that part.  Thread-safe. */
 MOE_API int moe_cache_create(const moe_cache_desc* desc, moe_cache** out);
 
 /* Free all cache-owned memory and events after synchronising the device. */
