@@ -150,7 +150,7 @@ class ClockSampler:
             mx = C.c_uint()
             if self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, C.byref(mx)) == 0:
                 self.max_mhz = mx.value
-        except Exception as ex:  # pragma: no cover - depends on the box
+        except Exception as ex:  # pragma: no cover - depends on the machine
             self.err = str(ex)
             self.nvml = None
 
